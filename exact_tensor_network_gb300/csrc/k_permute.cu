@@ -1,0 +1,77 @@
+// Leaf permutation: caller's storage order -> lifetime order.
+//
+// Lifetime ordering ("Crossing the single-GPU memory wall", section 1.4)
+// removes every runtime transpose of intermediates; what is left is one
+// reordering of each leaf that is not already stored in lifetime order,
+// done here once per slice (a sliced leaf is read at the slice's offset).
+// Many small leaves share one launch: each job owns a contiguous range of
+// CTAs.  Destination writes are linear and coalesced; the source side is a
+// gather through the job's strides.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tn {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kItems = 4;
+
+__global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant__ PermLaunch a) {
+    // Find this CTA's job (uniform across the CTA).
+    int lo = 0, hi = a.njobs - 1;
+    const int b = blockIdx.x;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cta_start[mid] <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    const int j = lo;
+    const PermDesc &d = a.table[a.job[j]];
+    const int ctas = a.cta_start[j + 1] - a.cta_start[j];
+    const int local = b - a.cta_start[j];
+    const float2 *src = a.src[j];
+    float2 *dst = d.dst_off < 0 ? a.out : reinterpret_cast<float2 *>(a.arena + d.dst_off);
+    const int rank = d.rank;
+    const int64_t size = d.size;
+    const int64_t step = (int64_t)ctas * kThreads * kItems;
+    for (int64_t base = (int64_t)local * kThreads * kItems; base < size; base += step) {
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int64_t e = base + it * kThreads + threadIdx.x;
+            if (e >= size) break;
+            int64_t rem = e, so = 0;
+            for (int r = rank - 1; r >= 0; --r) {
+                const int64_t dim = d.dims[r];
+                const int64_t q = rem / dim;
+                so += (rem - q * dim) * d.sstride[r];
+                rem = q;
+            }
+            float2 v = src[so];
+            if (a.accumulate) {
+                const float2 o = dst[e];
+                v.x += o.x;
+                v.y += o.y;
+            }
+            dst[e] = v;
+        }
+    }
+}
+
+}  // namespace
+
+int permute_ctas(int64_t size) {
+    const int64_t per = (int64_t)kThreads * kItems;
+    int64_t c = (size + per - 1) / per;
+    if (c < 1) c = 1;
+    if (c > 4096) c = 4096;
+    return (int)c;
+}
+
+cudaError_t launch_permute(const PermLaunch &args, int total_ctas, cudaStream_t stream) {
+    if (args.njobs <= 0) return cudaSuccess;
+    permute_kernel<<<total_ctas, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace tn

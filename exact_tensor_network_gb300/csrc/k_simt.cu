@@ -1,0 +1,102 @@
+// General node kernel on CUDA cores (fp32 complex FMA).
+//
+// Computes one pairwise step of "Crossing the single-GPU memory wall"
+// (section 1.1) in the GEMM form that lifetime ordering (section 1.4) gives
+// every node: A is a row-major [m, k] matrix, B a row-major [n, k] matrix,
+// and output entry (i, j) = sum_k A[i, k] * B[j, k] lands at
+// offM(i) + offN(j), which covers outputs whose order interleaves M and N
+// modes without any transpose pass.
+//
+// 64 x 64 output tile per CTA, 256 threads each owning a 4 x 4 block of
+// complex accumulators; K staged through shared memory 16 entries at a
+// time.  Any shape works (ragged edges are masked); the tensor-core and
+// streaming kernels take the shapes they are faster on.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tn {
+
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 16, TM = 4, TN = 4;
+constexpr int kThreads = (BM / TM) * (BN / TN);
+
+__global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_constant__ NodeArgs a) {
+    __shared__ float2 As[BK][BM + 1];
+    __shared__ float2 Bs[BK][BN + 1];
+    const int tid = threadIdx.x;
+    const int tx = tid % (BN / TN), ty = tid / (BN / TN);
+    const int64_t mt = (a.m + BM - 1) / BM, nt = (a.n + BN - 1) / BN;
+    const int64_t tiles = mt * nt;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t i0 = (tile / nt) * BM, j0 = (tile % nt) * BN;
+        float2 acc[TM][TN];
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+            for (int c = 0; c < TN; ++c) acc[r][c] = make_float2(0.f, 0.f);
+        for (int64_t k0 = 0; k0 < a.k; k0 += BK) {
+            // stage A[i0:i0+BM, k0:k0+BK] and B[j0:j0+BN, k0:k0+BK]
+            for (int e = tid; e < BM * BK; e += kThreads) {
+                const int r = e / BK, c = e % BK;
+                const int64_t i = i0 + r, kk = k0 + c;
+                As[c][r] = (i < a.m && kk < a.k) ? a.A[i * a.k + kk] : make_float2(0.f, 0.f);
+            }
+            for (int e = tid; e < BN * BK; e += kThreads) {
+                const int r = e / BK, c = e % BK;
+                const int64_t j = j0 + r, kk = k0 + c;
+                Bs[c][r] = (j < a.n && kk < a.k) ? a.B[j * a.k + kk] : make_float2(0.f, 0.f);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                float2 av[TM], bv[TN];
+#pragma unroll
+                for (int r = 0; r < TM; ++r) av[r] = As[kk][ty * TM + r];
+#pragma unroll
+                for (int c = 0; c < TN; ++c) bv[c] = Bs[kk][tx * TN + c];
+#pragma unroll
+                for (int r = 0; r < TM; ++r)
+#pragma unroll
+                    for (int c = 0; c < TN; ++c) cfma(acc[r][c], av[r], bv[c]);
+            }
+            __syncthreads();
+        }
+        int64_t offn[TN];
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const int64_t j = j0 + tx * TN + c;
+            offn[c] = j < a.n ? sep_offset(a.ln, j) : 0;
+        }
+#pragma unroll
+        for (int r = 0; r < TM; ++r) {
+            const int64_t i = i0 + ty * TM + r;
+            if (i >= a.m) continue;
+            const int64_t offm = sep_offset(a.lm, i);
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                const int64_t j = j0 + tx * TN + c;
+                if (j >= a.n) continue;
+                float2 v = acc[r][c];
+                float2 *p = a.C + offm + offn[c];
+                if (a.accumulate) {
+                    const float2 o = *p;
+                    v.x += o.x;
+                    v.y += o.y;
+                }
+                *p = v;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
+    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
+    const int64_t grid = tiles < 152 * 16 ? tiles : 152 * 16;
+    simt_node_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace tn

@@ -1,0 +1,128 @@
+// Internal plan structures shared by the host planner and the executor.
+//
+// The planner turns (network, tree, slices) into: the lifetime order of
+// every tensor ("Crossing the single-GPU memory wall", section 1.4), one
+// GEMM descriptor per tree step (section 1.1: A = [m, k], B = [n, k], both
+// row-major, output entry (i, j) stored at offM(i) + offN(j)), one
+// permutation job per leaf that is not already stored in lifetime order,
+// and a workspace layout built from buffer lifetimes.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/tn.h"
+
+namespace tn {
+
+constexpr int kMaxRank = 64;       // modes per tensor accepted by tn_plan
+constexpr int kMaxPermRank = 16;   // leaf permutation rank after merging axes
+constexpr int kMaxRuns = 12;       // runs per side of a separable output layout
+constexpr uint64_t kAlign = 256;   // workspace alignment of every buffer
+
+// Output side layout.  An index i in [0, prod ext) is split mixed-radix into
+// digits (run 0 most significant); its offset is sum digit[r] * stride[r]
+// (in elements).  The modes of M (or N) that sit next to each other in the
+// output's order form one run.
+struct SepLayout {
+    int32_t nrun;
+    int32_t pad;
+    int64_t ext[kMaxRuns];
+    int64_t stride[kMaxRuns];
+};
+
+// Where a tensor lives during execution.
+enum PlaceKind : int32_t { PLACE_WS = 0, PLACE_LEAF = 1, PLACE_OUT = 2 };
+struct Place {
+    int32_t kind;
+    int32_t leaf;     // PLACE_LEAF: user leaf index
+    uint64_t off;     // PLACE_WS: byte offset into the workspace arena
+};
+
+// Device-side leaf permutation job (lives in the workspace descriptor
+// table).  Destination index is row-major over dims (lifetime order);
+// source offset is sum digit[d] * sstride[d] from the (slice-shifted) user
+// pointer.
+struct PermDesc {
+    int64_t size;           // elements
+    int64_t dst_off;        // byte offset into the arena, or -1 = output
+    int32_t rank;
+    int32_t slot;           // index of the source pointer in the launch
+    int64_t dims[kMaxPermRank];
+    int64_t sstride[kMaxPermRank];
+};
+
+struct LeafPlan {
+    int32_t leaf;
+    bool in_place;          // consumed straight from the caller's pointer
+    int64_t size;           // elements after slicing
+    Place place;            // where the consumer reads it
+    PermDesc perm;          // valid when !in_place
+    // slicing: sliced modes this leaf carries, as (slice position, stride)
+    std::vector<std::pair<int32_t, int64_t>> slice_terms;
+};
+
+struct NodePlan {
+    int32_t step, a, b, out;
+    uint64_t m, n, k;
+    Place pa, pb, pc;
+    SepLayout lm, ln;
+    int32_t cls;
+    int32_t level;          // 1 + max level of operand nodes (leaves: 0)
+    bool is_root;
+    int32_t layout;         // 0: C = [M|N], 1: C = [N|M], 2: interleaved
+};
+
+struct Plan {
+    // inputs (copied)
+    int32_t n_tensors = 0, n_modes = 0, precision = 0;
+    std::vector<int64_t> extents;
+    std::vector<std::vector<int32_t>> leaf_modes;
+    std::vector<int32_t> open_modes;
+    std::vector<int32_t> pairs;       // 2 per step
+    std::vector<int32_t> slice_modes;
+
+    // derived
+    std::vector<std::vector<int32_t>> orders;   // per SSA id
+    std::vector<NodePlan> nodes;
+    std::vector<LeafPlan> leaves;
+    std::vector<int32_t> consumer;              // per SSA id, -1 for root
+    uint64_t ct_slice = 0, ct_total = 0, cs = 0, n_slices = 1;
+    uint64_t out_elems = 1;
+    std::vector<int64_t> slice_ext;             // extents of sliced modes
+
+    // execution layout
+    int32_t policy = TN_POLICY_AUTO;
+    uint64_t table_off = 0, table_bytes = 0;    // PermDesc table
+    uint64_t arena_off = 0, arena_bytes = 0;
+    uint64_t ws_bytes = 0;
+    std::vector<PermDesc> perm_table;
+    std::vector<int32_t> perm_leaves;           // leaf of each table entry
+
+    // measurement
+    bool profiling = false;
+    std::vector<void *> events;                 // cudaEvent_t pairs
+    std::vector<tn_launch_record> records;
+    uint64_t launches_per_exec = 0;
+
+    // binding
+    void *ws = nullptr;
+    uint64_t ws_size = 0;
+    int device = -1;
+
+    std::string last_error;
+};
+
+// Build the plan; returns TN_OK or an error with plan->last_error (or err)
+// describing it.
+tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices *sl,
+                     Plan *plan, std::string *err);
+
+// Classify nodes under plan->policy and lay out the workspace.
+tn_status layout_plan(Plan *plan);
+
+// Destroy the plan's CUDA events (exec.cu).
+void release_events(Plan *plan);
+
+}  // namespace tn

@@ -1,0 +1,258 @@
+/*
+ * tn.h: C ABI of the GB300 exact tensor-network contraction executor.
+ *
+ * A network is contracted pairwise along a fixed binary tree.  Before any
+ * device work, tn_plan() fixes the storage order of every tensor by the
+ * GEMM-oriented "lifetime ordering" of "Crossing the single-GPU memory wall:
+ * multi-GPU large-scale tensor network contraction" (digest of arXiv
+ * 2606.01852), section 1.4: walking the tree back from the root, each
+ * operand stores the output's modes it owns, in the output's order, followed
+ * by the summed modes.  Every step A x B -> C then reads A as a row-major
+ * [m, k] matrix and B as a row-major [n, k] matrix (section 1.1 names M, N
+ * and K); no intermediate is ever transposed.  Only leaves are permuted.
+ * Intermediates larger than memory are handled by slicing (section 1.1):
+ * fixing the sliced modes splits the contraction into independent
+ * sub-contractions whose results add up in the output.
+ *
+ * Conventions for every call:
+ *   - Storage is row-major: the last listed mode varies fastest.
+ *   - Values are complex64: interleaved (re, im) float pairs, 8 bytes each.
+ *   - Mode ids are 0 .. n_modes-1.  A closed mode appears in exactly two
+ *     tensors, an open mode in exactly one.  Hyperedges, traces (a mode twice
+ *     in one tensor) and modes that appear nowhere are rejected.
+ *   - No call throws; every failure is a tn_status.  A plan is not
+ *     thread-safe: use it from one host thread and one stream at a time.
+ *   - tn_plan() does no device work.  The library never allocates device
+ *     memory: the caller provides the workspace.
+ */
+#ifndef TN_GB300_H
+#define TN_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TN_API __attribute__((visibility("default")))
+#else
+#define TN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tn_status {
+    TN_OK = 0,
+    TN_EINVAL = 1,     /* malformed network, tree, slice set or argument */
+    TN_ENOMEM = 2,     /* workspace missing or smaller than required */
+    TN_EOVERFLOW = 3,  /* a size or FLOP count exceeds 64 bits */
+    TN_ECUDA = 4,      /* a CUDA runtime call failed (see tn_last_error) */
+    TN_EDEVICE = 5,    /* a kernel reported an inconsistency on the device */
+    TN_ETIMEOUT = 6,   /* a bounded device-side wait gave up */
+    TN_ENOTIMPL = 7    /* valid request this build does not support */
+} tn_status;
+
+/* Arithmetic of the tensor-core contraction of dense nodes.  Small and
+ * bandwidth-bound nodes use fp32 CUDA-core arithmetic in every mode.
+ * Intermediates are complex64 in HBM in every mode. */
+enum {
+    TN_PREC_TF32X3 = 0, /* split precision: x = hi + lo (hi = x rounded to
+                           tf32, lo = x - hi); products hi*hi + hi*lo + lo*hi
+                           accumulated in fp32 (fp32-level accuracy) */
+    TN_PREC_BF16 = 1,   /* tensor-core operands rounded to bf16 (round to
+                           nearest even), fp32 accumulation */
+    TN_PREC_FP32 = 2    /* every node on CUDA-core fp32 FMA */
+};
+
+/* Node classes reported by tn_plan_node_class and forced by
+ * tn_plan_set_policy. */
+enum {
+    TN_NODE_SIMT = 0,      /* general CUDA-core tiled kernel */
+    TN_NODE_DENSE = 1,     /* tcgen05 tensor-core kernel */
+    TN_NODE_STREAM = 2,    /* bandwidth-bound kernel (small n or k) */
+    TN_NODE_TINY = 3       /* batched tiny nodes, many per launch */
+};
+
+enum {
+    TN_POLICY_AUTO = 0,    /* classify every node by its shape */
+    TN_POLICY_SIMT = 1,    /* every node on the general CUDA-core kernel */
+    TN_POLICY_NO_TINY = 2  /* auto, but no batched tiny-node launches */
+};
+
+/*
+ * Network description (section 1.1; section 3.1 describes the same data as
+ * an einsum string plus per-mode extents).  All arrays are caller-owned and
+ * only read during tn_plan(), which copies what it needs.
+ *   n_tensors     number of leaves (>= 1)
+ *   ranks[t]      number of modes of leaf t (0 allowed: a scalar)
+ *   modes[t]      the ranks[t] mode ids of leaf t, in its storage order
+ *   n_modes       number of mode ids
+ *   extents[x]    dimension of mode x (>= 1)
+ *   n_open        number of open modes
+ *   open_modes    open mode ids in the order of the result's axes (the
+ *                 root order that section 1.4 takes as given)
+ *   precision     one of TN_PREC_*
+ */
+typedef struct tn_network {
+    int32_t n_tensors;
+    const int32_t *ranks;
+    const int32_t *const *modes;
+    int32_t n_modes;
+    const int64_t *extents;
+    int32_t n_open;
+    const int32_t *open_modes;
+    int32_t precision;
+} tn_network;
+
+/*
+ * Contraction tree in SSA form (section 3.4 lists a tree as ordered steps
+ * with two operands and an output each).  Step s contracts the ids
+ * pairs[2s] (operand A, whose kept modes form M) and pairs[2s+1] (operand B,
+ * kept modes N); leaves are ids 0 .. n_tensors-1 and step s produces id
+ * n_tensors + s.  Every id is consumed exactly once; the last step is the
+ * root.  n_steps must be n_tensors - 1.
+ */
+typedef struct tn_tree {
+    int32_t n_steps;
+    const int32_t *pairs;
+} tn_tree;
+
+/* Sliced modes (section 1.1): closed modes only.  Slices run in
+ * lexicographic order of the sliced indices, the first listed mode most
+ * significant.  n = 0 (or a NULL pointer to this struct) means no slicing. */
+typedef struct tn_slices {
+    int32_t n;
+    const int32_t *modes;
+} tn_slices;
+
+typedef struct tn_plan_s tn_plan_t;
+
+/* Stream handle; the same type as cudaStream_t (NULL = legacy stream). */
+typedef struct CUstream_st *tn_stream_t;
+
+/*
+ * Validate the inputs, compute mode lifetimes, the lifetime order of every
+ * tensor, every node's GEMM shape (m, n, k), C_t = sum of 8 m n k over the
+ * nodes times the number of slices, C_s = the largest intermediate in
+ * elements, the kernel class of every node, and the workspace layout.
+ * Host only.  On success *out owns a new plan (free with tn_plan_destroy).
+ * Errors: TN_EINVAL (malformed input; see tn_last_error(NULL)),
+ * TN_EOVERFLOW, TN_ENOTIMPL (more modes per tensor than supported).
+ */
+TN_API tn_status tn_plan(const tn_network *network, const tn_tree *tree,
+                  const tn_slices *slices, tn_plan_t **out);
+
+/* Release a plan (NULL is ignored).  Does not free the workspace. */
+TN_API void tn_plan_destroy(tn_plan_t *plan);
+
+/* C_t over all slices: sum over nodes of 8 m n k (one complex multiply-add
+ * counted as 8 real flops), times the number of slices. */
+TN_API tn_status tn_plan_flops(const tn_plan_t *plan, uint64_t *ct);
+
+/* C_s: the largest step output, in elements (per slice). */
+TN_API tn_status tn_plan_peak(const tn_plan_t *plan, uint64_t *cs);
+
+/* Number of slices: product of the sliced modes' extents (1 if none). */
+TN_API tn_status tn_plan_num_slices(const tn_plan_t *plan, uint64_t *n);
+
+/* Number of steps (n_tensors - 1). */
+TN_API tn_status tn_plan_num_steps(const tn_plan_t *plan, int32_t *n);
+
+/* Lifetime order of tensor `id` (leaf or step output, SSA numbering):
+ * writes min(len, cap) mode ids into buf and the full length into *len.
+ * Sliced modes are not part of any order. */
+TN_API tn_status tn_plan_mode_order(const tn_plan_t *plan, int32_t id, int32_t *buf,
+                             int32_t cap, int32_t *len);
+
+/* GEMM shape of step `step`: mnk[0] = m, mnk[1] = n, mnk[2] = k. */
+TN_API tn_status tn_plan_node_mnk(const tn_plan_t *plan, int32_t step, uint64_t mnk[3]);
+
+/* Kernel class (TN_NODE_*) the executor will use for step `step`. */
+TN_API tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t *cls);
+
+/* Choose how nodes are classified (TN_POLICY_*).  Call before
+ * tn_plan_workspace_bytes / tn_plan_set_workspace; it resets the workspace
+ * binding. */
+TN_API tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy);
+
+/* Device workspace the plan needs, in bytes (intermediates, permuted
+ * leaves, descriptor tables and a device status word). */
+TN_API tn_status tn_plan_workspace_bytes(const tn_plan_t *plan, uint64_t *bytes);
+
+/*
+ * Bind device memory as the workspace: dev_ptr must be 256-byte aligned
+ * device memory of at least tn_plan_workspace_bytes() bytes, owned by the
+ * caller and left alone by everyone else until the plan is destroyed or
+ * rebound.  Uploads the plan's descriptor tables (synchronous copy) on the
+ * current device.  Errors: TN_EINVAL (NULL or misaligned), TN_ENOMEM (too
+ * small), TN_ECUDA.
+ */
+TN_API tn_status tn_plan_set_workspace(tn_plan_t *plan, void *dev_ptr, uint64_t bytes);
+
+/*
+ * Contract the network: enqueue all slices and all steps on `stream`.
+ *   leaf_ptrs[t]  device pointer to leaf t in its own storage order
+ *                 (complex64, contiguous, 8-byte aligned); read only, must
+ *                 stay valid until the enqueued work completes.
+ *   out_ptr       device pointer to the result (complex64, open-mode order,
+ *                 product of the open extents entries; 1 entry if none).
+ *                 Overwritten with the sum over all slices.
+ * Asynchronous: returns after enqueueing.  Launch-time failures give
+ * TN_ECUDA; device-side problems surface through tn_plan_check().
+ * Errors: TN_EINVAL (NULL pointers), TN_ENOMEM (no workspace bound).
+ */
+TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                     tn_stream_t stream);
+
+/* After the stream has been synchronised: read and clear the device status
+ * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or
+ * TN_ETIMEOUT (a bounded wait inside a kernel gave up). */
+TN_API tn_status tn_plan_check(tn_plan_t *plan);
+
+/* ---- measurement ------------------------------------------------------ */
+
+/* Kernel ids in launch records. */
+enum {
+    TN_KERNEL_PERMUTE = 0,      /* leaf permutation batch */
+    TN_KERNEL_SIMT = 1,         /* general CUDA-core node kernel */
+    TN_KERNEL_DENSE_TF32X3 = 2, /* tcgen05 node kernel, split tf32 */
+    TN_KERNEL_DENSE_BF16 = 3,   /* tcgen05 node kernel, bf16 operands */
+    TN_KERNEL_STREAM = 4,       /* bandwidth-bound node kernel */
+    TN_KERNEL_TINY = 5          /* batched tiny-node kernel */
+};
+
+/* One kernel launch of a profiled tn_execute.  flops = 8 m n k of the
+ * node(s) it ran; bytes = the algorithmic HBM bytes (every operand read
+ * once, the output written once, plus read once more when accumulating). */
+typedef struct tn_launch_record {
+    int32_t kernel;   /* TN_KERNEL_* */
+    int32_t step;     /* tree step, or -1 for launches covering many */
+    float ms;         /* device time between CUDA events around the launch */
+    uint64_t flops;
+    uint64_t bytes;
+} tn_launch_record;
+
+/* Number of kernel launches one tn_execute makes (all slices). */
+TN_API tn_status tn_plan_launches(const tn_plan_t *plan, uint64_t *n);
+
+/* Enable (1) or disable (0) launch timing.  While enabled, tn_execute
+ * records a CUDA event before and after every launch on its stream (events
+ * are created by the plan and freed with it).  Off by default. */
+TN_API tn_status tn_plan_set_profiling(tn_plan_t *plan, int32_t enable);
+
+/* After a profiled tn_execute has completed (stream synchronised): copy up
+ * to cap records into buf and the number recorded into *len. */
+TN_API tn_status tn_plan_profile_read(tn_plan_t *plan, tn_launch_record *buf, int32_t cap,
+                                      int32_t *len);
+
+/* Static text for a status code. */
+TN_API const char *tn_status_string(tn_status status);
+
+/* Text of the last failure on this plan; with plan == NULL, of the last
+ * failed tn_plan() call on this thread.  Valid until the next call. */
+TN_API const char *tn_last_error(const tn_plan_t *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TN_GB300_H */

