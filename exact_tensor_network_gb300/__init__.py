@@ -82,6 +82,7 @@ SIGNATURES = {
     "tn_plan_workspace_bytes": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_workspace": (ctypes.c_int, [_P, _P, ctypes.c_uint64]),
     "tn_execute": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
+    "tn_execute_static": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_check": (ctypes.c_int, [_P]),
     "tn_plan_launches": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_profiling": (ctypes.c_int, [_P, ctypes.c_int32]),
@@ -204,6 +205,13 @@ def tn_plan_set_workspace(plan: int, dev_ptr: int, nbytes: int) -> None:
 def tn_execute(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream: int = 0) -> None:
     arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
     _check(lib().tn_execute(plan, arr, out_ptr, stream), plan)
+
+
+def tn_execute_static(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream: int = 0) -> None:
+    """tn_execute on the library's fixed device scratch array, for callers
+    that cannot allocate device memory (no workspace needed; see tn.h)."""
+    arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
+    _check(lib().tn_execute_static(plan, arr, out_ptr, stream), plan)
 
 
 def tn_plan_check(plan: int) -> None:

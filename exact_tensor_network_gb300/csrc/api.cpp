@@ -15,11 +15,6 @@ tn_status check_plan(Plan *p);
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len);
 }  // namespace tn
 
-struct tn_plan_s {
-    tn::Plan p;
-    ~tn_plan_s() { tn::release_events(&p); }
-};
-
 namespace {
 thread_local std::string g_plan_error;
 }

@@ -126,3 +126,9 @@ tn_status layout_plan(Plan *plan);
 void release_events(Plan *plan);
 
 }  // namespace tn
+
+// The opaque handle behind tn_plan_t.
+struct tn_plan_s {
+    tn::Plan p;
+    ~tn_plan_s() { tn::release_events(&p); }
+};

@@ -203,6 +203,31 @@ TN_API tn_status tn_plan_set_workspace(tn_plan_t *plan, void *dev_ptr, uint64_t 
 TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
                      tn_stream_t stream);
 
+/*
+ * tn_execute for callers that cannot allocate device memory (the paper has
+ * no counterpart; this is a convenience of this library).  Some callers may
+ * not allocate after start-up: real-time loops, plugins inside a host
+ * runtime that owns all device memory, code running where the allocator is
+ * off limits.  This call needs no tn_plan_set_workspace: it runs the same
+ * kernels as tn_execute with a 32 MiB scratch array that the library keeps
+ * in device global memory (every GPU that loads the library holds it until
+ * the process exits).  It calls no allocating routine.
+ *   - Plans whose tn_plan_workspace_bytes exceeds 32 MiB: TN_ENOMEM, with
+ *     nothing enqueued.
+ *   - All calls share the array.  Each call clears the status word and
+ *     uploads its plan's descriptor table on `stream` before its kernels;
+ *     calls whose GPU work overlaps (other streams, unordered threads) race
+ *     on the array.  Order them on one stream.
+ *   - The first call on a device looks up the array's address on that
+ *     device (which must be current) and caches it: make that first call
+ *     before any stream capture.
+ *   - tn_plan_check() does not report these calls' device status; launch
+ *     timing is suspended during them.
+ * Arguments, result and other errors as for tn_execute.
+ */
+TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                                   tn_stream_t stream);
+
 /* After the stream has been synchronised: read and clear the device status
  * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or
  * TN_ETIMEOUT (a bounded wait inside a kernel gave up). */

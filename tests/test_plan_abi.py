@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol():
     for name in names:
         assert hasattr(L, name), name
     # the binding knows them all too
-    assert set(names) <= set(tn.SIGNATURES) | {"tn_execute_static"}
+    assert set(names) <= set(tn.SIGNATURES)
 
 
 @functools.lru_cache(maxsize=1)
