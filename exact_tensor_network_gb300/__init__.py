@@ -25,7 +25,7 @@ PRECISIONS = {"tf32x3": TN_PREC_TF32X3, "bf16": TN_PREC_BF16, "fp32": TN_PREC_FP
 TN_NODE_SIMT, TN_NODE_DENSE, TN_NODE_STREAM, TN_NODE_TINY = 0, 1, 2, 3
 NODE_CLASS_NAMES = {0: "simt", 1: "dense", 2: "stream", 3: "tiny"}
 # policies
-TN_POLICY_AUTO, TN_POLICY_SIMT, TN_POLICY_NO_TINY = 0, 1, 2
+TN_POLICY_AUTO, TN_POLICY_SIMT, TN_POLICY_NO_TINY, TN_POLICY_DENSE = 0, 1, 2, 3
 
 
 class TNError(RuntimeError):

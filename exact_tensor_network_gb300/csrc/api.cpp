@@ -98,7 +98,7 @@ tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t *cls) 
 }
 
 tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy) {
-    if (!plan || policy < TN_POLICY_AUTO || policy > TN_POLICY_NO_TINY) return TN_EINVAL;
+    if (!plan || policy < TN_POLICY_AUTO || policy > TN_POLICY_DENSE) return TN_EINVAL;
     plan->p.policy = policy;
     return tn::layout_plan(&plan->p);
 }

@@ -1,6 +1,7 @@
 // Small device helpers shared by the kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -20,6 +21,39 @@ __device__ __forceinline__ int64_t sep_offset(const SepLayout &L, int64_t i) {
         i = q;
     }
     return off;
+}
+
+// x rounded to tf32 (10-bit mantissa, round to nearest, ties away), as fp32.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Store entry `off` of a tensor in format `fmt` (see Fmt in plan.h); planes
+// are `plane` entries apart.  `accumulate` adds into a C64 destination.
+__device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plane, int64_t off,
+                                            float2 v, int32_t accumulate) {
+    if (fmt == FMT_C64) {
+        float2 *p = static_cast<float2 *>(dst) + off;
+        if (accumulate) {
+            const float2 o = *p;
+            v.x += o.x;
+            v.y += o.y;
+        }
+        *p = v;
+    } else if (fmt == FMT_SPLIT4) {
+        float *p = static_cast<float *>(dst) + off;
+        const float rh = to_tf32(v.x), ih = to_tf32(v.y);
+        p[0] = rh;
+        p[plane] = ih;
+        p[2 * plane] = to_tf32(v.x - rh);
+        p[3 * plane] = to_tf32(v.y - ih);
+    } else {
+        __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
+        p[0] = __float2bfloat16_rn(v.x);
+        p[plane] = __float2bfloat16_rn(v.y);
+    }
 }
 
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {

@@ -16,9 +16,23 @@
 
 namespace tn {
 
+// Node classes.  A node goes to the tensor cores when its operands can be
+// TMA-tiled (k entries per row a multiple of 16 bytes in the planar
+// format), its tiles are reasonably full (m, n >= 64, k >= 16), and its
+// arithmetic intensity with planar operand bytes (16 per tf32x3 entry,
+// 4 per bf16 entry, 8 per output entry) is high enough to be
+// compute-bound rather than bandwidth-bound.
 int classify(const Plan &p, const NodePlan &nd) {
-    (void)nd;
     if (p.policy == TN_POLICY_SIMT || p.precision == TN_PREC_FP32) return TN_NODE_SIMT;
+    const bool bf16 = p.precision == TN_PREC_BF16;
+    const uint64_t kq = bf16 ? 8 : 4;
+    if (p.policy == TN_POLICY_DENSE) return nd.k % kq == 0 ? TN_NODE_DENSE : TN_NODE_SIMT;
+    if (nd.k % kq == 0 && nd.k >= 16 && nd.m >= 64 && nd.n >= 64) {
+        const double in_b = bf16 ? 4.0 : 16.0;
+        const double m = (double)nd.m, n = (double)nd.n, k = (double)nd.k;
+        const double intensity = 8.0 * m * n * k / (in_b * (m * k + n * k) + 8.0 * m * n);
+        if (intensity >= 24.0) return TN_NODE_DENSE;
+    }
     return TN_NODE_SIMT;
 }
 
@@ -70,6 +84,34 @@ tn_status cuda_fail(Plan *p, cudaError_t e, const char *what) {
     return TN_ECUDA;
 }
 
+// TMA maps of every tensor-core node's planar operands inside the current
+// workspace (host-side encoding only; rebuilt when the workspace moves).
+tn_status build_dense_maps(Plan *p) {
+    p->dense_maps.clear();
+    char *arena = static_cast<char *>(p->ws) + p->arena_off;
+    const bool bf16 = p->precision == TN_PREC_BF16;
+    for (size_t s = 0; s < p->nodes.size(); ++s) {
+        const NodePlan &nd = p->nodes[s];
+        if (nd.cls != TN_NODE_DENSE) continue;
+        if (nd.pa.kind != PLACE_WS || nd.pb.kind != PLACE_WS) {
+            p->last_error = "tensor-core operand not in the workspace";
+            return TN_EDEVICE;
+        }
+        DenseMaps dm;
+        std::memset(&dm, 0, sizeof(dm));
+        dm.node = (int32_t)s;
+        std::string err;
+        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, bf16, &err) ||
+            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, bf16, &err)) {
+            p->last_error = "step " + std::to_string(s) + ": " + err;
+            return TN_ECUDA;
+        }
+        p->dense_maps.push_back(dm);
+    }
+    p->maps_ws = p->ws;
+    return TN_OK;
+}
+
 }  // namespace
 
 tn_status upload_tables(Plan *p) {
@@ -80,7 +122,11 @@ tn_status upload_tables(Plan *p) {
                        p->perm_table.size() * sizeof(PermDesc), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(p, e, "uploading the permutation table");
     }
-    return TN_OK;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(p, e, "querying the SM count");
+    return build_dense_maps(p);
 }
 
 tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
@@ -94,8 +140,20 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     const int nsl = (int)p->slice_modes.size();
     std::vector<int64_t> digit(nsl, 0);
     std::vector<const float2 *> leaf_src(n);
-    PermLaunch *pl = new PermLaunch;
     tn_status st = TN_OK;
+    if (p->maps_ws != p->ws) {
+        st = build_dense_maps(p);
+        if (st != TN_OK) return st;
+    }
+    if (p->num_sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(p, e, "querying the SM count");
+    }
+    std::vector<int32_t> map_of(p->nodes.size(), -1);
+    for (size_t i = 0; i < p->dense_maps.size(); ++i) map_of[p->dense_maps[i].node] = (int32_t)i;
+    PermLaunch *pl = new PermLaunch;
     Recorder rec{p, stream};
     p->records.clear();
 
@@ -147,22 +205,50 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                     default: return out;
                 }
             };
-            NodeArgs a;
-            std::memset(&a, 0, sizeof(a));
-            a.A = resolve(nd.pa);
-            a.B = resolve(nd.pb);
-            a.C = resolve(nd.pc);
-            a.m = (int64_t)nd.m;
-            a.n = (int64_t)nd.n;
-            a.k = (int64_t)nd.k;
-            a.lm = nd.lm;
-            a.ln = nd.ln;
-            a.accumulate = (nd.is_root && sigma > 0) ? 1 : 0;
-            a.precision = p->precision;
-            a.status = status;
-            rec.begin(TN_KERNEL_SIMT, nd.step, 8 * nd.m * nd.n * nd.k, node_bytes(nd, a.accumulate));
-            cudaError_t e = launch_simt_node(a, stream);
-            rec.end();
+            const int32_t accumulate = (nd.is_root && sigma > 0) ? 1 : 0;
+            const uint64_t flops = 8 * nd.m * nd.n * nd.k;
+            cudaError_t e;
+            if (nd.cls == TN_NODE_DENSE) {
+                alignas(128) DenseArgs dargs;
+                std::memset(&dargs, 0, sizeof(dargs));
+                DenseArgs *d = &dargs;
+                const DenseMaps &dm = p->dense_maps[map_of[nd.step]];
+                std::memcpy(&d->tmA, &dm.a, sizeof(CUtensorMap));
+                std::memcpy(&d->tmB, &dm.b, sizeof(CUtensorMap));
+                d->C = resolve(nd.pc);
+                d->m = (int64_t)nd.m;
+                d->n = (int64_t)nd.n;
+                d->k = (int64_t)nd.k;
+                d->lm = nd.lm;
+                d->ln = nd.ln;
+                d->accumulate = accumulate;
+                d->out_fmt = nd.out_fmt;
+                d->bf16 = p->precision == TN_PREC_BF16;
+                d->status = status;
+                const uint64_t in_b = d->bf16 ? 4 : 16;
+                rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
+                          in_b * (nd.m * nd.k + nd.n * nd.k) +
+                              fmt_bytes(nd.out_fmt) * nd.m * nd.n * (accumulate ? 2 : 1));
+                e = launch_dense(*d, p->num_sms, stream);
+                rec.end();
+            } else {
+                NodeArgs a;
+                std::memset(&a, 0, sizeof(a));
+                a.A = resolve(nd.pa);
+                a.B = resolve(nd.pb);
+                a.C = resolve(nd.pc);
+                a.m = (int64_t)nd.m;
+                a.n = (int64_t)nd.n;
+                a.k = (int64_t)nd.k;
+                a.lm = nd.lm;
+                a.ln = nd.ln;
+                a.accumulate = accumulate;
+                a.out_fmt = nd.out_fmt;
+                a.status = status;
+                rec.begin(TN_KERNEL_SIMT, nd.step, flops, node_bytes(nd, accumulate));
+                e = launch_simt_node(a, stream);
+                rec.end();
+            }
             if (e != cudaSuccess) {
                 st = cuda_fail(p, e, "launching a node kernel");
                 break;

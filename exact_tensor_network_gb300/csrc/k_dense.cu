@@ -1,0 +1,503 @@
+// Tensor-core node kernel (tcgen05 + TMA + TMEM) for dense pairwise steps.
+//
+// Computes the step C[i, j] = sum_k A[i, k] * B[j, k] of "Crossing the
+// single-GPU memory wall" (section 1.1) in the transpose-free GEMM form
+// that lifetime ordering (section 1.4) gives every node: both operands are
+// row-major with k fastest ("K-major" in tensor-core terms), so TMA loads
+// their tiles as they lie in memory.
+//
+// Complex arithmetic on real tensor cores.  The producer of each operand
+// stores it planar (re and im planes; for the tf32x3 mode each plane is
+// also split into hi = tf32(x) and lo = tf32(x - hi), the split-precision
+// scheme of Markidis et al. 2018 / Ootomo & Yokota 2022).  A tile of B is
+// loaded as the stack [Br; Bi] (256 rows), so one MMA with N = 256 gives
+// both Ar*Br and Ar*Bi.  Two TMEM accumulators of 128 lanes x 256 fp32
+// columns hold
+//     D1 = Ar * [Br; Bi]^T = [ArBr | ArBi],  D2 = Ai * [Br; Bi]^T = [AiBr | AiBi]
+// and the epilogue forms Cr = ArBr - AiBi, Ci = ArBi + AiBr.  In tf32x3
+// mode each product X*Y is hi*hi + hi*lo + lo*hi (lo*lo dropped).
+//
+// Accuracy: the tensor core's fp32 accumulation loses a little on every
+// accumulation, and over thousands of k-steps that loss grows linearly with
+// k.  So the k range of a tile is cut into chunks of 256; each chunk is
+// accumulated in TMEM from zero, then drained into fp32 registers of the
+// epilogue warps with ordinary rounded adds (periodic promotion).
+//
+// Structure: persistent kernel, one CTA of 384 threads per SM.  Warpgroup
+// 0: warp 0 issues TMA loads into a ring of shared-memory stages, warp 1
+// issues the MMAs (one thread) and owns the TMEM allocation.  Warpgroups 1
+// and 2 (8 warps) drain TMEM: warp w reads TMEM lane quarter w % 4 (rows)
+// and one half of the tile's columns, keeps 64 complex running sums per
+// thread, and at the end of the tile stores them through the node's
+// separable output offsets in the format the consumer wants.  Registers
+// are moved from warpgroup 0 to the draining warpgroups with setmaxnreg.
+// Output tiles are 128 x 128 complex entries, visited in groups of 8 row
+// tiles so that concurrently running CTAs share operand tiles in L2.
+// Every wait on an mbarrier is bounded: on timeout the CTA raises an abort
+// flag, the roles leave their loops, in-flight copies and MMAs are drained
+// (also bounded), TMEM is released and the status word records
+// ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tn {
+
+namespace {
+
+constexpr int BM = 128;                 // complex output rows per tile
+constexpr int BN = 128;                 // complex output columns per tile
+constexpr int ROW_BYTES = 64;           // K bytes per smem row (64-byte swizzle)
+constexpr int PLANE_TILE = BM * ROW_BYTES;   // 8 KiB: 128 rows of one plane
+constexpr int THREADS = 384;            // 3 warpgroups
+constexpr int DRAIN_WARPS = 8;
+constexpr int CHUNK_K = 256;            // complex k accumulated in TMEM per drain
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+// register split: launched with 168 per thread (384 x 168 = 64512)
+constexpr int REGS_LOW = 56, REGS_HIGH = 224;
+
+template <bool BF16>
+struct Cfg {
+    static constexpr int A_PLANES = BF16 ? 2 : 4;
+    static constexpr int B_STACKS = BF16 ? 1 : 2;       // stacks of 256 rows
+    static constexpr int KB = BF16 ? 32 : 16;           // complex k per stage
+    static constexpr int K_INSTR = BF16 ? 16 : 8;       // k per MMA instruction
+    static constexpr int CHUNK_STAGES = CHUNK_K / KB;
+    static constexpr int STAGE_BYTES = (A_PLANES + 2 * B_STACKS) * PLANE_TILE;
+    static constexpr int STAGES = BF16 ? 6 : 3;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    // instruction descriptor: D f32, A/B tf32 (2) or bf16 (1), both K-major,
+    // N = 256, M = 128
+    static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
+                                      ((BF16 ? 1u : 2u) << 10) | ((256u >> 3) << 17) |
+                                      ((128u >> 4) << 24);
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity`; false if the CTA's abort
+// flag is up or the wait ran past the time limit (which raises the flag).
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
+// 64 bytes, 8-row core groups 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(4) << 61);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+    if constexpr (BF16) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(Cfg<true>::IDESC), "r"(acc));
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(Cfg<false>::IDESC), "r"(acc));
+    }
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Output tile of linear tile index t: groups of 8 row tiles, columns inside.
+__device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t ntiles, int64_t &mt,
+                                            int64_t &nt) {
+    const int64_t G = 8;
+    const int64_t group = G * ntiles;
+    const int64_t g = t / group;
+    const int64_t first = g * G;
+    const int64_t gm = (mtiles - first) < G ? (mtiles - first) : G;
+    const int64_t r = t - g * group;
+    mt = first + r % gm;
+    nt = r / gm;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant__ DenseArgs a) {
+    using C = Cfg<BF16>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + C::STAGES);
+    const uint32_t tmem_full = smem_u32(bars + 2 * C::STAGES);
+    const uint32_t tmem_empty = smem_u32(bars + 2 * C::STAGES + 1);
+    const uint32_t drain = smem_u32(bars + 2 * C::STAGES + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * C::STAGES + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, DRAIN_WARPS);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + BN - 1) / BN;
+    const int64_t tiles = mtiles * ntiles;
+    const int nkb = static_cast<int>((a.k + C::KB - 1) / C::KB);
+    const int nchunks = (nkb + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+        if (warp == 0 && lane == 0) {
+            // ---- TMA producer ----
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued = 0, last_par = 0;   // bit s: stage s has a load; its parity
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                int64_t mt, nt;
+                tile_coords(t, mtiles, ntiles, mt, nt);
+                const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = full0 + 8 * stage;
+                    mbar_expect_tx(bar, C::STAGE_BYTES);
+                    const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
+                    const int32_t kx = kb * C::KB;
+#pragma unroll
+                    for (int p = 0; p < C::A_PLANES; ++p)
+                        tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
+                    // B planes in the same order land as the stacks [re; im]
+                    // of each split part (hi stack, then lo stack)
+                    const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
+#pragma unroll
+                    for (int p = 0; p < C::A_PLANES; ++p)
+                        tma_load_3d(bbase + p * PLANE_TILE, &a.tmB, bar, kx, yn, p);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (issued & (1u << s)) drain_wait(full0 + 8 * s, (last_par >> s) & 1);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---- MMA issuer ----
+            const uint32_t d1 = tmem, d2 = tmem + 256;
+            uint32_t stage = 0, phase = 0, tphase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                for (int ch = 0; ch < nchunks && ok; ++ch) {
+                    if (!wait_bounded(tmem_empty, tphase ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const int kb_end = min(nkb, (ch + 1) * C::CHUNK_STAGES);
+                    for (int kb = ch * C::CHUNK_STAGES; kb < kb_end; ++kb) {
+                        if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
+                        const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
+                        const bool first = kb == ch * C::CHUNK_STAGES;
+#pragma unroll
+                        for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+                            const uint32_t off = kk * 32;   // 32 bytes of K per instruction
+                            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                            if constexpr (BF16) {
+                                const uint64_t ar = sdesc(base + off);
+                                const uint64_t ai = sdesc(base + PLANE_TILE + off);
+                                const uint64_t b = sdesc(bbase + off);
+                                mma<true>(d1, ar, b, acc);
+                                mma<true>(d2, ai, b, acc);
+                            } else {
+                                const uint64_t arh = sdesc(base + off);
+                                const uint64_t aih = sdesc(base + PLANE_TILE + off);
+                                const uint64_t arl = sdesc(base + 2 * PLANE_TILE + off);
+                                const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
+                                const uint64_t bh = sdesc(bbase + off);
+                                const uint64_t bl = sdesc(bbase + 2 * PLANE_TILE + off);
+                                mma<false>(d1, arl, bh, acc);
+                                mma<false>(d1, arh, bl, 1);
+                                mma<false>(d1, arh, bh, 1);
+                                mma<false>(d2, ail, bh, acc);
+                                mma<false>(d2, aih, bl, 1);
+                                mma<false>(d2, aih, bh, 1);
+                            }
+                        }
+                        mma_commit(empty0 + 8 * stage);
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(tmem_full);
+                    tphase ^= 1;
+                }
+            }
+            mma_commit(drain);
+            drain_wait(drain, 0);
+        }
+        __syncwarp();
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        // ---- drain: TMEM chunks -> fp32 running sums -> global ----
+        const int q = warp & 3;                 // TMEM lane quarter (rows)
+        const int h = (warp - 4) >> 2;          // column half of the tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const int64_t plane = a.m * a.n;
+        const int nl = a.ln.nrun;
+        const int64_t last_ext = nl > 0 ? a.ln.ext[nl - 1] : 1;
+        const int64_t last_stride = nl > 0 ? a.ln.stride[nl - 1] : 0;
+        uint32_t tphase = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            int64_t mt, nt;
+            tile_coords(t, mtiles, ntiles, mt, nt);
+            float sr[64], si[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sr[c] = si[c] = 0.f;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                int okv = 0;
+                if (lane == 0) okv = wait_bounded(tmem_full, tphase, abort_flag) ? 1 : 0;
+                okv = __shfl_sync(0xffffffffu, okv, 0);
+                if (!okv) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t col = h * 64 + cc * 16;
+                    float rr[16], ri[16], ir[16], ii[16];
+                    tmem_ld16(lane_base + col, rr);
+                    tmem_ld16(lane_base + 128 + col, ri);
+                    tmem_ld16(lane_base + 256 + col, ir);
+                    tmem_ld16(lane_base + 384 + col, ii);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        sr[cc * 16 + c] += rr[c] - ii[c];
+                        si[cc * 16 + c] += ri[c] + ir[c];
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tmem_empty);
+                tphase ^= 1;
+            }
+            if (!ok) break;
+            const int64_t i = mt * BM + q * 32 + lane;
+            if (i < a.m) {
+                const int64_t offm = sep_offset(a.lm, i);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int64_t j0 = nt * BN + h * 64 + cc * 16;
+                    if (j0 >= a.n) break;
+                    const bool fast = (j0 % last_ext) + 16 <= last_ext;
+                    const int64_t offn0 = sep_offset(a.ln, j0);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (j0 + c >= a.n) break;
+                        const int64_t offn =
+                            fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
+                        store_entry(a.C, a.out_fmt, plane, offm + offn,
+                                    make_float2(sr[cc * 16 + c], si[cc * 16 + c]), a.accumulate);
+                    }
+                }
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+    if (threadIdx.x == 0 && *abort_flag && a.status)
+        atomicCAS(&a.status->code, ERR_NONE, ERR_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream) {
+    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    if (grid <= 0) return cudaSuccess;
+    if (args.bf16) {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(dense_kernel<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<true>::SMEM);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        dense_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, stream>>>(args);
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(dense_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<false>::SMEM);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        dense_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, stream>>>(args);
+    }
+    return cudaGetLastError();
+}
+
+bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
+                        std::string *err) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+            *err = "cuTensorMapEncodeTiled is unavailable";
+            return false;
+        }
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t esz = bf16 ? 2 : 4;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(bf16 ? 2 : 4)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * esz,
+                                   static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ROW_BYTES / esz), BM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed with " + std::to_string(static_cast<int>(r));
+        return false;
+    }
+    return true;
+}
+
+}  // namespace tn

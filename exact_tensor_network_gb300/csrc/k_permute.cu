@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
     const int ctas = a.cta_start[j + 1] - a.cta_start[j];
     const int local = b - a.cta_start[j];
     const float2 *src = a.src[j];
-    float2 *dst = d.dst_off < 0 ? a.out : reinterpret_cast<float2 *>(a.arena + d.dst_off);
+    void *dst = d.dst_off < 0 ? static_cast<void *>(a.out) : static_cast<void *>(a.arena + d.dst_off);
+    const int32_t fmt = d.dst_off < 0 ? (int32_t)FMT_C64 : d.fmt;
     const int rank = d.rank;
     const int64_t size = d.size;
     const int64_t step = (int64_t)ctas * kThreads * kItems;
@@ -47,13 +48,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
                 so += (rem - q * dim) * d.sstride[r];
                 rem = q;
             }
-            float2 v = src[so];
-            if (a.accumulate) {
-                const float2 o = dst[e];
-                v.x += o.x;
-                v.y += o.y;
-            }
-            dst[e] = v;
+            store_entry(dst, fmt, size, e, src[so], a.accumulate);
         }
     }
 }

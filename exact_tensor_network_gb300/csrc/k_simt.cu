@@ -77,14 +77,7 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             for (int c = 0; c < TN; ++c) {
                 const int64_t j = j0 + tx * TN + c;
                 if (j >= a.n) continue;
-                float2 v = acc[r][c];
-                float2 *p = a.C + offm + offn[c];
-                if (a.accumulate) {
-                    const float2 o = *p;
-                    v.x += o.x;
-                    v.y += o.y;
-                }
-                *p = v;
+                store_entry(a.C, a.out_fmt, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate);
             }
         }
     }

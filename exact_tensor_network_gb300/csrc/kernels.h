@@ -1,9 +1,11 @@
 // Launchers of the device kernels and the small structs they take by value.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <string>
 
 #include "plan.h"
 
@@ -20,13 +22,35 @@ struct DevStatus {
 struct NodeArgs {
     const float2 *A;
     const float2 *B;
-    float2 *C;
+    void *C;
     int64_t m, n, k;
     SepLayout lm, ln;
     int32_t accumulate;   // 1: add into C (later slices of the root)
-    int32_t precision;
+    int32_t out_fmt;      // Fmt of C; planes are m*n entries apart
     DevStatus *status;
 };
+
+// One tensor-core node.  A and B are planar (FMT_SPLIT4 or FMT_BF2) and
+// reached through 3-D TMA maps over (k, rows, plane).
+struct DenseArgs {
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    void *C;
+    int64_t m, n, k;
+    SepLayout lm, ln;
+    int32_t accumulate;
+    int32_t out_fmt;
+    int32_t bf16;         // operands are FMT_BF2 (else FMT_SPLIT4)
+    DevStatus *status;
+};
+
+cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream);
+
+// Build the TMA map of a planar operand: rows x k entries per plane.
+// Returns false (with a message) when the driver call is unavailable or
+// rejects the shape.
+bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
+                        std::string *err);
 
 constexpr int kPermBatch = 512;   // permutation jobs per launch
 

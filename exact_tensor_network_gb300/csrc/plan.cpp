@@ -293,7 +293,8 @@ tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices
         int64_t size = 1;
         for (int64_t d : dims) size *= d;
         lp.size = size;
-        lp.in_place = dims.empty() || (dims.size() == 1 && sst[0] == 1);
+        lp.identity = dims.empty() || (dims.size() == 1 && sst[0] == 1);
+        lp.in_place = lp.identity;
         if ((int)dims.size() > kMaxPermRank)
             return fail(TN_ENOTIMPL, "leaf permutation needs more than 16 axes after merging");
         lp.perm.size = size;
@@ -355,27 +356,32 @@ tn_status layout_plan(Plan *p) {
     const int S = (int)p->nodes.size();
     for (auto &nd : p->nodes) nd.cls = classify(*p, nd);
 
+    // Storage formats: operands of tensor-core nodes are written planar by
+    // their producers; everything else is complex64.
+    p->fmt.assign(n + S, FMT_C64);
+    const int32_t dense_fmt = p->precision == TN_PREC_BF16 ? FMT_BF2 : FMT_SPLIT4;
+    for (const auto &nd : p->nodes)
+        if (nd.cls == TN_NODE_DENSE) p->fmt[nd.a] = p->fmt[nd.b] = dense_fmt;
+    for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
+
     std::vector<Interval> iv;
-    // leaves that need a permuted copy
     p->perm_table.clear();
     p->perm_leaves.clear();
     for (int t = 0; t < n; ++t) {
         LeafPlan &lp = p->leaves[t];
-        const bool to_out = (S == 0);
-        if (to_out) {
+        lp.in_place = S > 0 && lp.identity && p->fmt[t] == FMT_C64;
+        if (S == 0) {
             lp.place = {PLACE_OUT, t, 0};
         } else if (lp.in_place) {
             lp.place = {PLACE_LEAF, t, 0};
         } else {
-            iv.push_back({(uint64_t)lp.size * 8, -1, p->consumer[t], t, 0});
+            iv.push_back({(uint64_t)lp.size * fmt_bytes(p->fmt[t]), -1, p->consumer[t], t, 0});
         }
     }
     for (int s = 0; s < S; ++s) {
         const NodePlan &nd = p->nodes[s];
-        if (!nd.is_root) {
-            uint64_t bytes = nd.m * nd.n * 8;
-            iv.push_back({bytes, s, p->consumer[nd.out], nd.out, 0});
-        }
+        if (!nd.is_root)
+            iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), s, p->consumer[nd.out], nd.out, 0});
     }
     p->arena_bytes = place_buffers(iv);
     std::vector<Place> where(n + S, Place{PLACE_WS, -1, 0});
@@ -387,7 +393,7 @@ tn_status layout_plan(Plan *p) {
         if (S == 0 || !lp.in_place) {
             PermDesc d = lp.perm;
             d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
-            d.slot = 0;
+            d.fmt = (S == 0) ? FMT_C64 : p->fmt[t];
             p->perm_table.push_back(d);
             p->perm_leaves.push_back(t);
         }
@@ -404,6 +410,8 @@ tn_status layout_plan(Plan *p) {
     p->arena_off = p->table_off + p->table_bytes;
     p->ws_bytes = p->arena_off + p->arena_bytes;
     p->launches_per_exec = launches_per_slice(*p) * p->n_slices;
+    p->dense_maps.clear();
+    p->maps_ws = nullptr;
     p->ws = nullptr;
     p->ws_size = 0;
     return TN_OK;

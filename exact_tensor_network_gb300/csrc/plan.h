@@ -8,6 +8,8 @@
 // and a workspace layout built from buffer lifetimes.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (type only; the driver is reached at run time)
+
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -32,6 +34,16 @@ struct SepLayout {
     int64_t stride[kMaxRuns];
 };
 
+// Storage format of a tensor in HBM.  Every tensor is C64 except the
+// operands of tensor-core (dense) nodes, which their producer writes in the
+// planar form the tensor-core kernel loads with TMA:
+//   FMT_SPLIT4: four fp32 planes [re_hi, im_hi, re_lo, im_lo], each the
+//               tensor's row-major entries; hi = x rounded to tf32,
+//               lo = (x - hi) rounded to tf32 (16 bytes per entry)
+//   FMT_BF2:    two bf16 planes [re, im] (4 bytes per entry)
+enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2 };
+inline uint64_t fmt_bytes(int32_t f) { return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : 8; }
+
 // Where a tensor lives during execution.
 enum PlaceKind : int32_t { PLACE_WS = 0, PLACE_LEAF = 1, PLACE_OUT = 2 };
 struct Place {
@@ -48,13 +60,14 @@ struct PermDesc {
     int64_t size;           // elements
     int64_t dst_off;        // byte offset into the arena, or -1 = output
     int32_t rank;
-    int32_t slot;           // index of the source pointer in the launch
+    int32_t fmt;            // destination format (Fmt); planes are `size` apart
     int64_t dims[kMaxPermRank];
     int64_t sstride[kMaxPermRank];
 };
 
 struct LeafPlan {
     int32_t leaf;
+    bool identity;          // caller's layout already is the lifetime order
     bool in_place;          // consumed straight from the caller's pointer
     int64_t size;           // elements after slicing
     Place place;            // where the consumer reads it
@@ -72,6 +85,14 @@ struct NodePlan {
     int32_t level;          // 1 + max level of operand nodes (leaves: 0)
     bool is_root;
     int32_t layout;         // 0: C = [M|N], 1: C = [N|M], 2: interleaved
+    int32_t out_fmt;        // format the output is stored in (Fmt)
+};
+
+// Launch data of a tensor-core node, built when the workspace is bound:
+// 3-D TMA maps (k, rows, planes) over the planar operands.
+struct DenseMaps {
+    CUtensorMap a, b;
+    int32_t node;
 };
 
 struct Plan {
@@ -99,6 +120,10 @@ struct Plan {
     uint64_t ws_bytes = 0;
     std::vector<PermDesc> perm_table;
     std::vector<int32_t> perm_leaves;           // leaf of each table entry
+    std::vector<int32_t> fmt;                   // per SSA id (Fmt)
+    std::vector<DenseMaps> dense_maps;          // per dense node, set at bind
+    void *maps_ws = nullptr;                    // workspace the maps point into
+    int num_sms = 0;
 
     // measurement
     bool profiling = false;

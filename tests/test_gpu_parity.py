@@ -134,9 +134,11 @@ def test_extent_one_modes():
 def test_simt_policy_matches_auto():
     import exact_tensor_network_gb300 as tn
     net, tree, _ = configs.random_60()
+    ref = _ref(net, tree)
     a, _ = run_gpu(net, tree, policy=tn.TN_POLICY_AUTO)
     b, _ = run_gpu(net, tree, policy=tn.TN_POLICY_SIMT)
-    assert_close(a, b, what="auto vs simt")
+    assert_close(a, ref, what="auto policy vs oracle")
+    assert_close(b, ref, what="simt policy vs oracle")
 
 
 def test_profiling_records_every_launch():
