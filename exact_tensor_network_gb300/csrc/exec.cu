@@ -33,12 +33,84 @@ int classify(const Plan &p, const NodePlan &nd) {
         const double intensity = 8.0 * m * n * k / (in_b * (m * k + n * k) + 8.0 * m * n);
         if (intensity >= 24.0) return TN_NODE_DENSE;
     }
+    if (std::min(nd.m, nd.n) <= (uint64_t)kStreamMaxN) return TN_NODE_STREAM;
     return TN_NODE_SIMT;
 }
 
+namespace {
+
+// Stream-kernel shape: threads per row of A and rows per CTA.
+void stream_shape(uint64_t rows, uint64_t k, int *lanes, int64_t *rows_per_cta) {
+    int l = 1;
+    while (l < 32 && (uint64_t)l * 8 < k) l *= 2;
+    const int64_t groups = 256 / l;
+    int64_t mult = (int64_t)(rows / ((uint64_t)groups * 4 * kTargetCtas));
+    if (mult < 1) mult = 1;
+    *lanes = l;
+    *rows_per_cta = groups * mult;
+}
+
+constexpr uint64_t kPartialBudget = 1ull << 30;   // bytes of split-K partials per node
+
+}  // namespace
+
+// Split-K for the CUDA-core classes: cut k when the node alone would not
+// give every SM two CTAs, keeping chunks of at least 64 entries.
+void choose_split(const Plan &p, NodePlan &nd) {
+    (void)p;
+    nd.ksplit = 1;
+    nd.kchunk = (int64_t)nd.k;
+    nd.swap = 0;
+    uint64_t units = 0, outs = nd.m * nd.n;
+    if (nd.cls == TN_NODE_DENSE) {
+        // tensor-core tiles are 128 x 128 and one CTA runs per SM; splits are
+        // whole multiples of the 256-entry accumulation chunk
+        const uint64_t tiles = ((nd.m + 127) / 128) * ((nd.n + 127) / 128);
+        const uint64_t sms = kTargetCtas / 2;
+        if (tiles >= sms || nd.k < 512) return;
+        uint64_t s = std::min<uint64_t>((sms + tiles - 1) / tiles, nd.k / 256);
+        s = std::min<uint64_t>(s, kPartialBudget / (8 * outs));
+        if (s < 2) return;
+        uint64_t chunk = (nd.k + s - 1) / s;
+        chunk = (chunk + 255) / 256 * 256;
+        const uint64_t ks = (nd.k + chunk - 1) / chunk;
+        if (ks < 2) return;
+        nd.kchunk = (int64_t)chunk;
+        nd.ksplit = (int32_t)ks;
+        return;
+    }
+    if (nd.cls == TN_NODE_STREAM) {
+        nd.swap = nd.m < nd.n ? 1 : 0;
+        const uint64_t rows = std::max(nd.m, nd.n);
+        int lanes;
+        int64_t rpc;
+        stream_shape(rows, nd.k, &lanes, &rpc);
+        units = (rows + rpc - 1) / rpc;
+    } else if (nd.cls == TN_NODE_SIMT) {
+        units = ((nd.m + 63) / 64) * ((nd.n + 63) / 64);
+    } else {
+        return;
+    }
+    if (units >= (uint64_t)kTargetCtas || nd.k < 128) return;
+    uint64_t s = std::min<uint64_t>((kTargetCtas + units - 1) / units, nd.k / 64);
+    s = std::min<uint64_t>(s, kPartialBudget / (8 * outs));
+    s = std::min<uint64_t>(s, 4096);
+    if (s < 2) return;
+    uint64_t chunk = (nd.k + s - 1) / s;
+    chunk = (chunk + 15) / 16 * 16;
+    nd.kchunk = (int64_t)chunk;
+    nd.ksplit = (int32_t)((nd.k + chunk - 1) / chunk);
+    if (nd.ksplit < 2) {
+        nd.ksplit = 1;
+        nd.kchunk = (int64_t)nd.k;
+    }
+}
+
 uint64_t launches_per_slice(const Plan &p) {
-    const uint64_t perm = (p.perm_table.size() + kPermBatch - 1) / kPermBatch;
-    return perm + p.nodes.size();
+    uint64_t n = (p.perm_table.size() + kPermBatch - 1) / kPermBatch + p.nodes.size();
+    for (const auto &nd : p.nodes)
+        if (nd.ksplit > 1) ++n;   // the split-K reduction
+    return n;
 }
 
 void release_events(Plan *p) {
@@ -225,11 +297,39 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                 d->out_fmt = nd.out_fmt;
                 d->bf16 = p->precision == TN_PREC_BF16;
                 d->status = status;
+                d->ksplit = nd.ksplit;
+                d->kchunk = nd.kchunk;
+                d->part = reinterpret_cast<float2 *>(arena + nd.part.off);
                 const uint64_t in_b = d->bf16 ? 4 : 16;
                 rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +
                               fmt_bytes(nd.out_fmt) * nd.m * nd.n * (accumulate ? 2 : 1));
                 e = launch_dense(*d, p->num_sms, stream);
+                rec.end();
+            } else if (nd.cls == TN_NODE_STREAM) {
+                StreamArgs a;
+                std::memset(&a, 0, sizeof(a));
+                // B is the small side: swap operands (C^T = B A^T) when m is
+                a.A = resolve(nd.swap ? nd.pb : nd.pa);
+                a.B = resolve(nd.swap ? nd.pa : nd.pb);
+                a.C = resolve(nd.pc);
+                a.part = reinterpret_cast<float2 *>(arena + nd.part.off);
+                a.m = (int64_t)(nd.swap ? nd.n : nd.m);
+                a.n = (int64_t)(nd.swap ? nd.m : nd.n);
+                a.k = (int64_t)nd.k;
+                a.kchunk = nd.kchunk;
+                a.ksplit = nd.ksplit;
+                a.lm = nd.swap ? nd.ln : nd.lm;
+                a.ln = nd.swap ? nd.lm : nd.ln;
+                a.accumulate = accumulate;
+                a.out_fmt = nd.out_fmt;
+                int lanes;
+                int64_t rpc;
+                stream_shape((uint64_t)a.m, nd.k, &lanes, &rpc);
+                a.lanes = lanes;
+                a.rows_per_cta = (int32_t)rpc;
+                rec.begin(TN_KERNEL_STREAM, nd.step, flops, node_bytes(nd, accumulate));
+                e = launch_stream_node(a, stream);
                 rec.end();
             } else {
                 NodeArgs a;
@@ -245,8 +345,33 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                 a.accumulate = accumulate;
                 a.out_fmt = nd.out_fmt;
                 a.status = status;
+                a.ksplit = nd.ksplit;
+                a.kchunk = nd.kchunk;
+                a.part = reinterpret_cast<float2 *>(arena + nd.part.off);
                 rec.begin(TN_KERNEL_SIMT, nd.step, flops, node_bytes(nd, accumulate));
                 e = launch_simt_node(a, stream);
+                rec.end();
+            }
+            if (e == cudaSuccess && nd.ksplit > 1) {
+                ReduceArgs r;
+                std::memset(&r, 0, sizeof(r));
+                const bool sw = nd.cls == TN_NODE_STREAM && nd.swap;
+                r.part = reinterpret_cast<const float2 *>(arena + nd.part.off);
+                r.C = resolve(nd.pc);
+                r.m = (int64_t)(sw ? nd.n : nd.m);
+                r.n = (int64_t)(sw ? nd.m : nd.n);
+                r.ksplit = nd.ksplit;
+                r.lm = sw ? nd.ln : nd.lm;
+                r.ln = sw ? nd.lm : nd.ln;
+                r.accumulate = accumulate;
+                r.out_fmt = nd.out_fmt;
+                const int32_t kid = nd.cls == TN_NODE_STREAM ? TN_KERNEL_STREAM
+                                    : nd.cls == TN_NODE_DENSE
+                                        ? (p->precision == TN_PREC_BF16 ? TN_KERNEL_DENSE_BF16
+                                                                        : TN_KERNEL_DENSE_TF32X3)
+                                        : TN_KERNEL_SIMT;
+                rec.begin(kid, nd.step, 0, 0);
+                e = launch_splitk_reduce(r, stream);
                 rec.end();
             }
             if (e != cudaSuccess) {

@@ -68,7 +68,10 @@ struct Cfg {
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
     static constexpr int STAGE_BYTES = (A_PLANES + 2 * B_STACKS) * PLANE_TILE;
     static constexpr int STAGES = BF16 ? 6 : 3;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    // stages, alignment slack, barriers, then one 32 x 16 complex staging
+    // tile per drain warp for coalesced stores
+    static constexpr int STAGING = DRAIN_WARPS * 32 * 16 * 8;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + STAGING;
     // instruction descriptor: D f32, A/B tf32 (2) or bf16 (1), both K-major,
     // N = 256, M = 128
     static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
@@ -251,7 +254,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + BN - 1) / BN;
     const int64_t tiles = mtiles * ntiles;
     const int nkb = static_cast<int>((a.k + C::KB - 1) / C::KB);
-    const int nchunks = (nkb + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
+    // work item w = (tile w / ksplit, k split w % ksplit); a split covers kbs
+    // k-blocks
+    const int ksplit = a.ksplit > 1 ? a.ksplit : 1;
+    const int64_t work = tiles * ksplit;
+    const int kbs = ksplit > 1 ? static_cast<int>(a.kchunk / C::KB) : nkb;
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
@@ -260,11 +267,14 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, last_par = 0;   // bit s: stage s has a load; its parity
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
+                const int64_t t = w / ksplit;
+                const int sp = static_cast<int>(w - t * ksplit);
                 int64_t mt, nt;
                 tile_coords(t, mtiles, ntiles, mt, nt);
                 const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * BN);
-                for (int kb = 0; kb < nkb; ++kb) {
+                const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
@@ -299,15 +309,20 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             const uint32_t d1 = tmem, d2 = tmem + 256;
             uint32_t stage = 0, phase = 0, tphase = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                for (int ch = 0; ch < nchunks && ok; ++ch) {
+            for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
+                const int64_t t = w / ksplit;
+                const int sp = static_cast<int>(w - t * ksplit);
+                const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+                const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
+                for (int ch = 0; ch < nch && ok; ++ch) {
                     if (!wait_bounded(tmem_empty, tphase ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     fence_after();
-                    const int kb_end = min(nkb, (ch + 1) * C::CHUNK_STAGES);
-                    for (int kb = ch * C::CHUNK_STAGES; kb < kb_end; ++kb) {
+                    const int kb_beg = kb0 + ch * C::CHUNK_STAGES;
+                    const int kb_end = min(kb1, kb_beg + C::CHUNK_STAGES);
+                    for (int kb = kb_beg; kb < kb_end; ++kb) {
                         if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
                             ok = false;
                             break;
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         fence_after();
                         const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
                         const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
-                        const bool first = kb == ch * C::CHUNK_STAGES;
+                        const bool first = kb == kb_beg;
 #pragma unroll
                         for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
                             const uint32_t off = kk * 32;   // 32 bytes of K per instruction
@@ -366,15 +381,31 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const int nl = a.ln.nrun;
         const int64_t last_ext = nl > 0 ? a.ln.ext[nl - 1] : 1;
         const int64_t last_stride = nl > 0 ? a.ln.stride[nl - 1] : 0;
+        // split-K partials are plain row-major C64; otherwise the node's
+        // output.  When consecutive rows are adjacent in the output (its
+        // fastest mode is in M) thread-per-row stores coalesce as they are;
+        // otherwise each warp transposes 32 x 16 blocks through shared memory
+        // so that 16 lanes store 16 consecutive columns.
+        const bool plain = ksplit > 1;
+        const bool rows_adjacent =
+            !plain && a.lm.nrun > 0 && a.lm.stride[a.lm.nrun - 1] == 1;
+        const int32_t fmt = plain ? (int32_t)FMT_C64 : a.out_fmt;
+        const int32_t accum = plain ? 0 : a.accumulate;
+        float2 *stage_tile = reinterpret_cast<float2 *>(
+            smem + C::STAGES * C::STAGE_BYTES + 256 + (warp - 4) * 32 * 16 * 8);
         uint32_t tphase = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
+            const int64_t t = w / ksplit;
+            const int sp = static_cast<int>(w - t * ksplit);
+            const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+            const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
             int64_t mt, nt;
             tile_coords(t, mtiles, ntiles, mt, nt);
             float sr[64], si[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) sr[c] = si[c] = 0.f;
-            for (int ch = 0; ch < nchunks; ++ch) {
+            for (int ch = 0; ch < nch; ++ch) {
                 int okv = 0;
                 if (lane == 0) okv = wait_bounded(tmem_full, tphase, abort_flag) ? 1 : 0;
                 okv = __shfl_sync(0xffffffffu, okv, 0);
@@ -404,23 +435,58 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 tphase ^= 1;
             }
             if (!ok) break;
-            const int64_t i = mt * BM + q * 32 + lane;
-            if (i < a.m) {
-                const int64_t offm = sep_offset(a.lm, i);
+            void *dst = plain ? static_cast<void *>(a.part + (int64_t)sp * plane) : a.C;
+            const int64_t i0 = mt * BM + q * 32;
+            const int64_t i = i0 + lane;
+            const int64_t offm = i < a.m ? (plain ? i * a.n : sep_offset(a.lm, i)) : 0;
+            if (rows_adjacent) {
+                if (i < a.m) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int64_t j0 = nt * BN + h * 64 + cc * 16;
+                        if (j0 >= a.n) break;
+                        const bool fast = (j0 % last_ext) + 16 <= last_ext;
+                        const int64_t offn0 = sep_offset(a.ln, j0);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            if (j0 + c >= a.n) break;
+                            const int64_t offn =
+                                fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
+                            store_entry(dst, fmt, plane, offm + offn,
+                                        make_float2(sr[cc * 16 + c], si[cc * 16 + c]), accum);
+                        }
+                    }
+                }
+            } else {
+                const int c = lane & 15;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int64_t j0 = nt * BN + h * 64 + cc * 16;
-                    if (j0 >= a.n) break;
-                    const bool fast = (j0 % last_ext) + 16 <= last_ext;
-                    const int64_t offn0 = sep_offset(a.ln, j0);
+                    if (j0 >= a.n) break;   // warp-uniform
+                    // own row's 16 values, columns xor-swizzled by row
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (j0 + c >= a.n) break;
-                        const int64_t offn =
-                            fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
-                        store_entry(a.C, a.out_fmt, plane, offm + offn,
-                                    make_float2(sr[cc * 16 + c], si[cc * 16 + c]), a.accumulate);
+                    for (int x = 0; x < 16; ++x)
+                        stage_tile[lane * 16 + (x ^ (lane & 15))] =
+                            make_float2(sr[cc * 16 + x], si[cc * 16 + x]);
+                    __syncwarp();
+                    const int64_t j = j0 + c;
+                    int64_t offn = 0;
+                    if (j < a.n) {
+                        if (plain) {
+                            offn = j;
+                        } else {
+                            const bool fast = (j0 % last_ext) + 16 <= last_ext;
+                            offn = fast ? sep_offset(a.ln, j0) + c * last_stride : sep_offset(a.ln, j);
+                        }
                     }
+#pragma unroll 4
+                    for (int it = 0; it < 16; ++it) {
+                        const int r = 2 * it + (lane >> 4);
+                        const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
+                        const int64_t om = __shfl_sync(0xffffffffu, offm, r);
+                        if (i0 + r < a.m && j < a.n) store_entry(dst, fmt, plane, om + offn, v, accum);
+                    }
+                    __syncwarp();
                 }
             }
         }

@@ -28,24 +28,29 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
     const int tx = tid % (BN / TN), ty = tid / (BN / TN);
     const int64_t mt = (a.m + BM - 1) / BM, nt = (a.n + BN - 1) / BN;
     const int64_t tiles = mt * nt;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t work = tiles * a.ksplit;
+    for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
+        const int64_t tile = w / a.ksplit;
+        const int split = (int)(w - tile * a.ksplit);
+        const int64_t kbeg = a.ksplit > 1 ? split * a.kchunk : 0;
+        const int64_t kend = a.ksplit > 1 ? min(a.k, kbeg + a.kchunk) : a.k;
         const int64_t i0 = (tile / nt) * BM, j0 = (tile % nt) * BN;
         float2 acc[TM][TN];
 #pragma unroll
         for (int r = 0; r < TM; ++r)
 #pragma unroll
             for (int c = 0; c < TN; ++c) acc[r][c] = make_float2(0.f, 0.f);
-        for (int64_t k0 = 0; k0 < a.k; k0 += BK) {
+        for (int64_t k0 = kbeg; k0 < kend; k0 += BK) {
             // stage A[i0:i0+BM, k0:k0+BK] and B[j0:j0+BN, k0:k0+BK]
             for (int e = tid; e < BM * BK; e += kThreads) {
                 const int r = e / BK, c = e % BK;
                 const int64_t i = i0 + r, kk = k0 + c;
-                As[c][r] = (i < a.m && kk < a.k) ? a.A[i * a.k + kk] : make_float2(0.f, 0.f);
+                As[c][r] = (i < a.m && kk < kend) ? a.A[i * a.k + kk] : make_float2(0.f, 0.f);
             }
             for (int e = tid; e < BN * BK; e += kThreads) {
                 const int r = e / BK, c = e % BK;
                 const int64_t j = j0 + r, kk = k0 + c;
-                Bs[c][r] = (j < a.n && kk < a.k) ? a.B[j * a.k + kk] : make_float2(0.f, 0.f);
+                Bs[c][r] = (j < a.n && kk < kend) ? a.B[j * a.k + kk] : make_float2(0.f, 0.f);
             }
             __syncthreads();
 #pragma unroll
@@ -61,6 +66,21 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
                     for (int c = 0; c < TN; ++c) cfma(acc[r][c], av[r], bv[c]);
             }
             __syncthreads();
+        }
+        if (a.ksplit > 1) {
+            // plain partial sums of this k range
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                const int64_t i = i0 + ty * TM + r;
+                if (i >= a.m) continue;
+                float2 *dst = a.part + ((int64_t)split * a.m + i) * a.n;
+#pragma unroll
+                for (int c = 0; c < TN; ++c) {
+                    const int64_t j = j0 + tx * TN + c;
+                    if (j < a.n) dst[j] = acc[r][c];
+                }
+            }
+            continue;
         }
         int64_t offn[TN];
 #pragma unroll
@@ -86,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
 }  // namespace
 
 cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
-    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
+    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN) * args.ksplit;
     const int64_t grid = tiles < 152 * 16 ? tiles : 152 * 16;
     simt_node_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(args);
     return cudaGetLastError();

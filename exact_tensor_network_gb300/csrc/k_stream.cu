@@ -1,0 +1,118 @@
+// Bandwidth-bound node kernel and the split-K reduction.
+//
+// Nodes with a small side (n <= 16 after swapping the operands when m is
+// the small one) are gate-like contractions, outer products and dot products:
+// their time is reading the big operand A once (the t_gemm bandwidth term
+// of "Crossing the single-GPU memory wall", section 1.6).  B is staged in
+// shared memory one k-chunk at a time; each row of A is read once, by
+// `lanes` threads that split its k range and then combine their partial
+// sums with warp shuffles.  Long k ranges are cut into ksplit chunks run by
+// different CTAs; their fp32 partial sums land in the workspace and
+// splitk_reduce adds them in split order (deterministic), then stores the
+// node's output through its separable offsets in the consumer's format.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_constant__ StreamArgs a) {
+    __shared__ float2 Bs[kStreamMaxN * kStreamKc];
+    const int s = blockIdx.y;
+    const int64_t k0 = (int64_t)s * a.kchunk;
+    const int64_t k1 = min(a.k, k0 + a.kchunk);
+    const int n = (int)a.n;
+    const int lanes = a.lanes;
+    const int g = threadIdx.x / lanes, l = threadIdx.x % lanes;
+    const int groups = kThreads / lanes;
+    const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_cta;
+    const int64_t r1 = min(a.m, r0 + a.rows_per_cta);
+
+    // accumulators per row, B staged chunk by chunk
+    for (int64_t rb = r0; rb < r1; rb += groups) {
+        const int64_t r = rb + g;
+        float2 acc[kStreamMaxN];
+#pragma unroll
+        for (int j = 0; j < kStreamMaxN; ++j) acc[j] = make_float2(0.f, 0.f);
+        for (int64_t c0 = k0; c0 < k1; c0 += kStreamKc) {
+            const int clen = (int)min((int64_t)kStreamKc, k1 - c0);
+            __syncthreads();
+            for (int e = threadIdx.x; e < n * clen; e += kThreads) {
+                const int j = e / clen, kk = e - j * clen;
+                Bs[j * kStreamKc + kk] = a.B[(int64_t)j * a.k + c0 + kk];
+            }
+            __syncthreads();
+            if (r < r1) {
+                const float2 *arow = a.A + r * a.k + c0;
+                for (int kk = l; kk < clen; kk += lanes) {
+                    const float2 av = arow[kk];
+#pragma unroll
+                    for (int j = 0; j < kStreamMaxN; ++j)
+                        if (j < n) cfma(acc[j], av, Bs[j * kStreamKc + kk]);
+                }
+            }
+        }
+        // combine the lanes of a row
+        for (int off = lanes >> 1; off > 0; off >>= 1) {
+#pragma unroll
+            for (int j = 0; j < kStreamMaxN; ++j) {
+                if (j < n) {
+                    acc[j].x += __shfl_down_sync(0xffffffffu, acc[j].x, off, lanes);
+                    acc[j].y += __shfl_down_sync(0xffffffffu, acc[j].y, off, lanes);
+                }
+            }
+        }
+        if (l == 0 && r < r1) {
+            if (a.ksplit > 1) {
+                float2 *dst = a.part + ((int64_t)s * a.m + r) * a.n;
+#pragma unroll
+                for (int j = 0; j < kStreamMaxN; ++j)
+                    if (j < n) dst[j] = acc[j];
+            } else {
+                const int64_t offm = sep_offset(a.lm, r);
+#pragma unroll
+                for (int j = 0; j < kStreamMaxN; ++j)
+                    if (j < n)
+                        store_entry(a.C, a.out_fmt, a.m * a.n, offm + sep_offset(a.ln, j), acc[j],
+                                    a.accumulate);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    const int64_t mn = a.m * a.n;
+    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < mn;
+         e += (int64_t)gridDim.x * kThreads) {
+        float2 v = make_float2(0.f, 0.f);
+        for (int s = 0; s < a.ksplit; ++s) {
+            const float2 p = a.part[(int64_t)s * mn + e];
+            v.x += p.x;
+            v.y += p.y;
+        }
+        const int64_t i = e / a.n, j = e - i * a.n;
+        store_entry(a.C, a.out_fmt, mn, sep_offset(a.lm, i) + sep_offset(a.ln, j), v, a.accumulate);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
+    const int64_t blocks = (args.m + args.rows_per_cta - 1) / args.rows_per_cta;
+    dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
+    stream_node_kernel<<<grid, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream) {
+    const int64_t mn = args.m * args.n;
+    int64_t blocks = (mn + kThreads - 1) / kThreads;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    splitk_reduce_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace tn

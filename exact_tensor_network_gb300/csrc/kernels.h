@@ -28,7 +28,45 @@ struct NodeArgs {
     int32_t accumulate;   // 1: add into C (later slices of the root)
     int32_t out_fmt;      // Fmt of C; planes are m*n entries apart
     DevStatus *status;
+    // split-K: with ksplit > 1, split s sums k in [s*kchunk, (s+1)*kchunk)
+    // and writes plain partials part[(s*m + i)*n + j]; splitk_reduce stores C
+    int32_t ksplit;
+    int64_t kchunk;
+    float2 *part;
 };
+
+// Bandwidth-bound node: B (n <= kStreamMaxN rows) is small and staged in
+// shared memory k-chunk by k-chunk; the rows of A stream through once.
+// Same output and split-K conventions as NodeArgs.
+constexpr int kStreamMaxN = 16;
+constexpr int kStreamKc = 256;     // k entries of B staged per chunk (<= 32 KiB)
+struct StreamArgs {
+    const float2 *A;
+    const float2 *B;
+    void *C;
+    float2 *part;
+    int64_t m, n, k, kchunk;
+    int32_t ksplit;
+    int32_t lanes;        // threads that share one row of A (power of two <= 32)
+    int32_t rows_per_cta;
+    SepLayout lm, ln;
+    int32_t accumulate;
+    int32_t out_fmt;
+};
+
+// Ordered sum of split-K partials into the node's output.
+struct ReduceArgs {
+    const float2 *part;
+    void *C;
+    int64_t m, n;
+    int32_t ksplit;
+    SepLayout lm, ln;
+    int32_t accumulate;
+    int32_t out_fmt;
+};
+
+cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream);
 
 // One tensor-core node.  A and B are planar (FMT_SPLIT4 or FMT_BF2) and
 // reached through 3-D TMA maps over (k, rows, plane).
@@ -42,6 +80,10 @@ struct DenseArgs {
     int32_t out_fmt;
     int32_t bf16;         // operands are FMT_BF2 (else FMT_SPLIT4)
     DevStatus *status;
+    // split-K as in NodeArgs (kchunk a multiple of 256)
+    int32_t ksplit;
+    int64_t kchunk;
+    float2 *part;
 };
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream);

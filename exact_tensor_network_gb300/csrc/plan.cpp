@@ -350,11 +350,15 @@ uint64_t place_buffers(std::vector<Interval> &iv) {
 
 int classify(const Plan &p, const NodePlan &nd);  // defined in exec.cu
 uint64_t launches_per_slice(const Plan &p);        // defined in exec.cu
+void choose_split(const Plan &p, NodePlan &nd);    // defined in exec.cu
 
 tn_status layout_plan(Plan *p) {
     const int n = p->n_tensors;
     const int S = (int)p->nodes.size();
-    for (auto &nd : p->nodes) nd.cls = classify(*p, nd);
+    for (auto &nd : p->nodes) {
+        nd.cls = classify(*p, nd);
+        choose_split(*p, nd);
+    }
 
     // Storage formats: operands of tensor-core nodes are written planar by
     // their producers; everything else is complex64.
@@ -382,9 +386,11 @@ tn_status layout_plan(Plan *p) {
         const NodePlan &nd = p->nodes[s];
         if (!nd.is_root)
             iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), s, p->consumer[nd.out], nd.out, 0});
+        if (nd.ksplit > 1)   // split-K partial sums live during the step only
+            iv.push_back({(uint64_t)nd.ksplit * nd.m * nd.n * 8, s, s, n + S + s, 0});
     }
     p->arena_bytes = place_buffers(iv);
-    std::vector<Place> where(n + S, Place{PLACE_WS, -1, 0});
+    std::vector<Place> where(n + 2 * S, Place{PLACE_WS, -1, 0});
     for (const auto &b : iv) where[b.id] = {PLACE_WS, -1, b.off};
     for (int t = 0; t < n; ++t) {
         LeafPlan &lp = p->leaves[t];
@@ -404,6 +410,7 @@ tn_status layout_plan(Plan *p) {
         nd.pa = where[nd.a];
         nd.pb = where[nd.b];
         nd.pc = where[nd.out];
+        nd.part = where[n + S + s];
     }
     p->table_off = kAlign;
     p->table_bytes = (p->perm_table.size() * sizeof(PermDesc) + kAlign - 1) / kAlign * kAlign;

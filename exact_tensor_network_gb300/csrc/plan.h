@@ -86,7 +86,18 @@ struct NodePlan {
     bool is_root;
     int32_t layout;         // 0: C = [M|N], 1: C = [N|M], 2: interleaved
     int32_t out_fmt;        // format the output is stored in (Fmt)
+    // split-K (CUDA-core classes): ksplit ranges of kchunk entries each write
+    // fp32 complex partial sums [split][i][j] into `part`, then an ordered
+    // reduction stores the node's output
+    int32_t ksplit;
+    int64_t kchunk;
+    Place part;
+    int32_t swap;           // stream class: operands swapped so B is the small side
 };
+
+// Aim of the split-K choice: at least this many CTAs per launch (two per
+// SM of a GB300).
+constexpr int kTargetCtas = 2 * 152;
 
 // Launch data of a tensor-core node, built when the workspace is bound:
 // 3-D TMA maps (k, rows, planes) over the planar operands.

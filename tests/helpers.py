@@ -20,6 +20,19 @@ def run_gpu(net, tree, slices=(), precision="tf32x3", policy=0, out_dtype=None, 
     return out.cpu().numpy().astype(np.complex128), plan
 
 
+def node_network(m, n, k, seed, name=None):
+    """Single step A[i, x] B[j, x] -> C[i, j] with one mode per side
+    (extents m, n, k; a side of extent 1 still gets its mode)."""
+    from workloads.network import Network
+    rng = np.random.default_rng(seed)
+
+    def rnd(shape):
+        return ((rng.standard_normal(shape) + 1j * rng.standard_normal(shape))
+                .astype(np.complex64))
+    return Network([[0, 2], [1, 2]], [m, n, k], [0, 1], [rnd((m, k)), rnd((n, k))],
+                   name or f"node_{m}x{n}x{k}")
+
+
 def max_rel_err(got, ref):
     scale = float(np.abs(ref).max()) if np.size(ref) else 0.0
     err = float(np.abs(np.asarray(got) - np.asarray(ref)).max()) if np.size(ref) else 0.0

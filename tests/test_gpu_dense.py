@@ -112,6 +112,34 @@ def test_dense_chain(precision, tol):
     assert_close(got, _ref(net, tree), tol, f"dense chain {precision}")
 
 
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("m,n,k", [(128, 256, 16384), (64, 4096, 2048), (300, 200, 3000)])
+def test_dense_split_k(precision, tol, m, n, k):
+    """Few output tiles and long k: the tensor-core kernel splits k across
+    CTAs (whole 256-entry chunks) and the partials are reduced in order."""
+    net = node_network(m, n, k, m + 2 * n + 3 * k)
+    p = tn.Plan.from_network(net, [(0, 1)], (), precision)
+    assert p.node_class(0) == tn.TN_NODE_DENSE
+    assert p.launches == 3            # leaf conversion, dense, reduction
+    got, _ = run_gpu(net, [(0, 1)], precision=precision)
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"split dense {m}x{n}x{k} {precision}")
+
+
+def test_dense_split_k_feeding_dense():
+    # A[a,x] B[b,x] -> C[a,b] (64 x 2048 output, k = 4096: split), then
+    # C[a,b] D[c,b] -> root (dense over b = 2048)
+    rng = np.random.default_rng(21)
+    ext = [64, 4096, 2048, 256]          # a x b c
+    tensors = [[0, 1], [2, 1], [3, 2]]
+    data = [_rand(rng, [ext[x] for x in t], 0.25) for t in tensors]
+    net = Network(tensors, ext, [0, 3], data)
+    tree = [(0, 1), (3, 2)]
+    p = tn.Plan.from_network(net, tree)
+    assert [p.node_class(s) for s in range(2)] == [tn.TN_NODE_DENSE, tn.TN_NODE_DENSE]
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), TOL_C64, "split dense feeding dense")
+
+
 def test_sliced_dense_root_accumulates():
     net = gemm_network(8, 8, 9, 3)
     sl = [net.tensors[0][-1], net.tensors[0][-2]]     # two K modes -> 4 slices

@@ -1,0 +1,69 @@
+"""Bandwidth-bound (stream) kernel and split-K vs the fp64 oracle (GB300).
+
+Stream nodes have a side of at most 16 entries: gate-like (huge m, tiny n
+and k), dot products (m = n = 1), outer products (k = 1), and the swapped
+case where m is the small side.  Split-K cuts long k ranges across CTAs and
+sums the partials in order; it is used by the stream kernel and the
+general CUDA-core kernel when a node alone would not fill the GPU.
+"""
+import numpy as np
+import pytest
+
+import exact_tensor_network_gb300 as tn
+import oracle
+from workloads import greedy_tree, grid_circuit_network
+from workloads.network import Network
+
+from helpers import TOL_C64, assert_close, node_network, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _ref(net, tree):
+    return oracle.contract(net.tensors, net.extents, net.open_modes, net.data, tree)
+
+
+@pytest.mark.parametrize("m,n,k,cls", [
+    (32, 4, 65536, tn.TN_NODE_STREAM),      # split-K dot-like
+    (4, 32, 65536, tn.TN_NODE_STREAM),      # swapped
+    (1, 1, 262144, tn.TN_NODE_STREAM),      # dot product
+    (1 << 20, 2, 2, tn.TN_NODE_STREAM),     # gate-like
+    (1 << 16, 16, 16, tn.TN_NODE_STREAM),
+    (3, 100000, 1, tn.TN_NODE_STREAM),      # outer product, swapped
+    (1000, 7, 300, tn.TN_NODE_STREAM),
+    (100, 90, 5000, tn.TN_NODE_SIMT),       # split SIMT tiles
+    (70, 300, 1001, tn.TN_NODE_SIMT),       # k odd: not tensor-core eligible
+    (17, 17, 17, tn.TN_NODE_SIMT),
+])
+def test_stream_and_split_nodes(m, n, k, cls):
+    net = node_network(m, n, k, m * 7 + n * 3 + k)
+    p = tn.Plan.from_network(net, [(0, 1)])
+    assert p.node_class(0) == cls
+    got, _ = run_gpu(net, [(0, 1)])
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, f"node {m}x{n}x{k}")
+
+
+def test_split_root_with_slices_accumulates():
+    net = node_network(32, 4, 4096, 5)
+    # slice the contracted mode by replacing it with two modes of 64 each
+    rng = np.random.default_rng(2)
+    a = net.data[0].reshape(32, 64, 64)
+    b = net.data[1].reshape(4, 64, 64)
+    net2 = Network([[0, 2, 3], [1, 2, 3]], [32, 4, 64, 64], [0, 1], [a, b])
+    got, plan = run_gpu(net2, [(0, 1)], slices=[2])
+    assert plan.num_slices == 64
+    assert_close(got, _ref(net2, [(0, 1)]), TOL_C64, "sliced split-K root")
+
+
+@pytest.mark.parametrize("rows,cols,cycles,n_open", [(4, 4, 8, 0), (4, 5, 10, 4), (5, 5, 8, 2)])
+def test_circuits(rows, cols, cycles, n_open):
+    net, _ = grid_circuit_network(rows, cols, cycles, rows * cols + cycles, n_open=n_open)
+    tree = greedy_tree(net, 0)
+    got, _ = run_gpu(net, tree)
+    assert_close(got, _ref(net, tree), TOL_C64, f"circuit {rows}x{cols} d{cycles}")
