@@ -12,13 +12,26 @@ namespace tn {
 
 // Offset of index i under a separable output layout: split i mixed-radix
 // over the runs (run 0 most significant) and sum digit * stride.
+// Power-of-two extents use shifts and masks; other extents divide (32-bit
+// when the index fits, which avoids the slow 64-bit division).
 __device__ __forceinline__ int64_t sep_offset(const SepLayout &L, int64_t i) {
     int64_t off = 0;
     for (int r = L.nrun - 1; r >= 0; --r) {
         const int64_t e = L.ext[r];
-        const int64_t q = i / e;
-        off += (i - q * e) * L.stride[r];
-        i = q;
+        int64_t d;
+        if (L.shift[r] >= 0) {
+            d = i & (e - 1);
+            i >>= L.shift[r];
+        } else if (i < 0x7fffffff && e < 0x7fffffff) {
+            const uint32_t q = static_cast<uint32_t>(i) / static_cast<uint32_t>(e);
+            d = i - static_cast<int64_t>(q) * e;
+            i = q;
+        } else {
+            const int64_t q = i / e;
+            d = i - q * e;
+            i = q;
+        }
+        off += d * L.stride[r];
     }
     return off;
 }

@@ -23,11 +23,14 @@ namespace tn {
 // 4 per bf16 entry, 8 per output entry) is high enough to be
 // compute-bound rather than bandwidth-bound.
 int classify(const Plan &p, const NodePlan &nd) {
-    if (p.policy == TN_POLICY_SIMT || p.precision == TN_PREC_FP32) return TN_NODE_SIMT;
+    if (p.policy == TN_POLICY_SIMT) return TN_NODE_SIMT;
     const bool bf16 = p.precision == TN_PREC_BF16;
+    const bool fp32 = p.precision == TN_PREC_FP32;
     const uint64_t kq = bf16 ? 8 : 4;
-    if (p.policy == TN_POLICY_DENSE) return nd.k % kq == 0 ? TN_NODE_DENSE : TN_NODE_SIMT;
-    if (nd.k % kq == 0 && nd.k >= 16 && nd.m >= 64 && nd.n >= 64) {
+    if (p.policy == TN_POLICY_DENSE)
+        return (!fp32 && nd.k % kq == 0) ? TN_NODE_DENSE : TN_NODE_SIMT;
+    if (p.policy == TN_POLICY_AUTO && nd.m * nd.n * nd.k <= kTinyMacs) return TN_NODE_TINY;
+    if (!fp32 && nd.k % kq == 0 && nd.k >= 16 && nd.m >= 64 && nd.n >= 64) {
         const double in_b = bf16 ? 4.0 : 16.0;
         const double m = (double)nd.m, n = (double)nd.n, k = (double)nd.k;
         const double intensity = 8.0 * m * n * k / (in_b * (m * k + n * k) + 8.0 * m * n);
@@ -107,9 +110,11 @@ void choose_split(const Plan &p, NodePlan &nd) {
 }
 
 uint64_t launches_per_slice(const Plan &p) {
-    uint64_t n = (p.perm_table.size() + kPermBatch - 1) / kPermBatch + p.nodes.size();
-    for (const auto &nd : p.nodes)
-        if (nd.ksplit > 1) ++n;   // the split-K reduction
+    uint64_t n = (p.perm_table.size() + kPermBatch - 1) / kPermBatch;
+    for (const auto &L : p.sched) {
+        if (L.kind == LAUNCH_TINY) ++n;
+        if (L.kind == LAUNCH_NODE) n += p.nodes[L.node].ksplit > 1 ? 2 : 1;   // + reduction
+    }
     return n;
 }
 
@@ -189,10 +194,10 @@ tn_status build_dense_maps(Plan *p) {
 tn_status upload_tables(Plan *p) {
     cudaError_t e = cudaMemset(p->ws, 0, p->table_off);
     if (e != cudaSuccess) return cuda_fail(p, e, "clearing the status word");
-    if (!p->perm_table.empty()) {
-        e = cudaMemcpy(static_cast<char *>(p->ws) + p->table_off, p->perm_table.data(),
-                       p->perm_table.size() * sizeof(PermDesc), cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) return cuda_fail(p, e, "uploading the permutation table");
+    if (!p->table_blob.empty()) {
+        e = cudaMemcpy(static_cast<char *>(p->ws) + p->table_off, p->table_blob.data(),
+                       p->table_blob.size(), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(p, e, "uploading the descriptor tables");
     }
     int dev = 0;
     e = cudaGetDevice(&dev);
@@ -269,7 +274,26 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
             }
         }
         if (st != TN_OK) break;
-        for (const NodePlan &nd : p->nodes) {
+        for (const Launch &L : p->sched) {
+            if (L.kind == LAUNCH_PERMUTE) continue;   // issued above
+            if (L.kind == LAUNCH_TINY) {
+                TinyLaunch tl;
+                tl.table = reinterpret_cast<const TinyDesc *>(ws + p->tiny_off);
+                tl.first = L.first;
+                tl.count = L.count;
+                tl.arena = arena;
+                tl.out = out;
+                tl.accumulate_root = sigma > 0 ? 1 : 0;
+                rec.begin(TN_KERNEL_TINY, -1, L.flops, L.bytes);
+                cudaError_t e = launch_tiny_batch(tl, L.ctas, stream);
+                rec.end();
+                if (e != cudaSuccess) {
+                    st = cuda_fail(p, e, "launching a tiny-node batch");
+                    break;
+                }
+                continue;
+            }
+            const NodePlan &nd = p->nodes[L.node];
             auto resolve = [&](const Place &pl_) -> float2 * {
                 switch (pl_.kind) {
                     case PLACE_WS: return reinterpret_cast<float2 *>(arena + pl_.off);
@@ -300,6 +324,7 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                 d->ksplit = nd.ksplit;
                 d->kchunk = nd.kchunk;
                 d->part = reinterpret_cast<float2 *>(arena + nd.part.off);
+                d->ep = nd.ep_off >= 0 ? reinterpret_cast<const EpTable *>(ws + nd.ep_off) : nullptr;
                 const uint64_t in_b = d->bf16 ? 4 : 16;
                 rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +

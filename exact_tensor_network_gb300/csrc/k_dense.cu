@@ -71,7 +71,8 @@ struct Cfg {
     // stages, alignment slack, barriers, then one 32 x 16 complex staging
     // tile per drain warp for coalesced stores
     static constexpr int STAGING = DRAIN_WARPS * 32 * 16 * 8;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + STAGING;
+    static constexpr int EP_BYTES = (int)((sizeof(EpTable) + 127) / 128 * 128);
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + STAGING + EP_BYTES;
     // instruction descriptor: D f32, A/B tf32 (2) or bf16 (1), both K-major,
     // N = 256, M = 128
     static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
@@ -393,6 +394,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const int32_t accum = plain ? 0 : a.accumulate;
         float2 *stage_tile = reinterpret_cast<float2 *>(
             smem + C::STAGES * C::STAGE_BYTES + 256 + (warp - 4) * 32 * 16 * 8);
+        EpTable *ep_s = nullptr;
+        if (a.ep && !plain) {
+            ep_s = reinterpret_cast<EpTable *>(smem + C::STAGES * C::STAGE_BYTES + 256 + C::STAGING);
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(a.ep);
+            uint32_t *dstw = reinterpret_cast<uint32_t *>(ep_s);
+            for (int x = threadIdx.x - 128; x < (int)(sizeof(EpTable) / 4); x += DRAIN_WARPS * 32)
+                dstw[x] = src[x];
+            asm volatile("bar.sync 1, %0;" ::"n"(DRAIN_WARPS * 32) : "memory");
+        }
         uint32_t tphase = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
@@ -439,7 +449,31 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             const int64_t i0 = mt * BM + q * 32;
             const int64_t i = i0 + lane;
             const int64_t offm = i < a.m ? (plain ? i * a.n : sep_offset(a.lm, i)) : 0;
-            if (rows_adjacent) {
+            if (ep_s) {
+                // walk each 32 x 16 block in address order
+                const int64_t bm = sep_offset(a.lm, i0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int64_t j0 = nt * BN + h * 64 + cc * 16;
+                    if (j0 >= a.n) break;   // warp-uniform
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        stage_tile[lane * 16 + (x ^ (lane & 15))] =
+                            make_float2(sr[cc * 16 + x], si[cc * 16 + x]);
+                    __syncwarp();
+                    const int64_t base = bm + sep_offset(a.ln, j0);
+#pragma unroll 4
+                    for (int it = 0; it < 16; ++it) {
+                        const int e = ep_s->perm[it * 32 + lane];
+                        const int r = e >> 4, c = e & 15;
+                        const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
+                        if (i0 + r < a.m && j0 + c < a.n)
+                            store_entry(dst, fmt, plane, base + ep_s->lo_m[r] + ep_s->lo_n[c], v,
+                                        accum);
+                    }
+                    __syncwarp();
+                }
+            } else if (rows_adjacent) {
                 if (i < a.m) {
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {

@@ -44,9 +44,14 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
             int64_t rem = e, so = 0;
             for (int r = rank - 1; r >= 0; --r) {
                 const int64_t dim = d.dims[r];
-                const int64_t q = rem / dim;
-                so += (rem - q * dim) * d.sstride[r];
-                rem = q;
+                if (d.dshift[r] >= 0) {
+                    so += (rem & (dim - 1)) * d.sstride[r];
+                    rem >>= d.dshift[r];
+                } else {
+                    const int64_t q = rem / dim;
+                    so += (rem - q * dim) * d.sstride[r];
+                    rem = q;
+                }
             }
             store_entry(dst, fmt, size, e, src[so], a.accumulate);
         }

@@ -1,0 +1,74 @@
+// Batched kernel for tiny nodes.
+//
+// Most nodes near the leaves of a tree are tiny (a few hundred to a few
+// hundred thousand complex multiply-adds: single-qubit gates absorbed into
+// wires, small random tensors meeting).  One launch per node would cost
+// several microseconds of launch and memory latency each, far more than
+// their arithmetic.  All tiny nodes of one schedule stage are independent,
+// so one launch runs them all: each node owns a few CTAs (its cta_base
+// range in the descriptor table); each CTA takes a share of the node's
+// outputs; `lanes` threads cooperate on one output's k range and combine
+// with warp shuffles.  Operands are complex64 in the workspace arena; the
+// output goes through the node's separable offsets in its consumer's format
+// (the root adds into the caller's output on later slices).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_constant__ TinyLaunch a) {
+    // this CTA's node: last descriptor whose cta_base <= blockIdx.x
+    int lo = a.first, hi = a.first + a.count - 1;
+    const int b = blockIdx.x;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.table[mid].cta_base <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    const TinyDesc &d = a.table[lo];
+    const int local = b - d.cta_base;
+    const float2 *A = reinterpret_cast<const float2 *>(a.arena + d.a_off);
+    const float2 *B = reinterpret_cast<const float2 *>(a.arena + d.b_off);
+    void *C = d.c_off < 0 ? static_cast<void *>(a.out) : static_cast<void *>(a.arena + d.c_off);
+    const int64_t mn = (int64_t)d.m * d.n;
+    const int64_t per = (mn + d.ctas - 1) / d.ctas;
+    const int64_t o0 = (int64_t)local * per;
+    const int64_t o1 = min(mn, o0 + per);
+    const int lanes = d.lanes;
+    const int g = threadIdx.x / lanes, l = threadIdx.x % lanes;
+    const int groups = kThreads / lanes;
+    const int accumulate = d.is_root ? a.accumulate_root : 0;
+    const int k = d.k;
+    for (int64_t ob = o0; ob < o1; ob += groups) {
+        const int64_t o = ob + g;
+        float2 acc = make_float2(0.f, 0.f);
+        // m n <= 2^18 here, so 32-bit index arithmetic is exact
+        const int o32 = static_cast<int>(o);
+        const int i = o32 / d.n, j = o32 - i * d.n;
+        if (o < o1) {
+            const float2 *ar = A + (int64_t)i * k, *br = B + (int64_t)j * k;
+            for (int kk = l; kk < k; kk += lanes) cfma(acc, ar[kk], br[kk]);
+        }
+        for (int off = lanes >> 1; off > 0; off >>= 1) {
+            acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, lanes);
+            acc.y += __shfl_down_sync(0xffffffffu, acc.y, off, lanes);
+        }
+        if (l == 0 && o < o1) {
+            store_entry(C, d.out_fmt, mn, sep_offset(d.lm, i) + sep_offset(d.ln, j), acc, accumulate);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tiny_batch(const TinyLaunch &args, int ctas, cudaStream_t stream) {
+    if (ctas <= 0) return cudaSuccess;
+    tiny_batch_kernel<<<ctas, kThreads, 0, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace tn

@@ -65,6 +65,17 @@ struct ReduceArgs {
     int32_t out_fmt;
 };
 
+// One batched launch of tiny nodes: descriptors [first, first + count) of
+// the workspace table.
+struct TinyLaunch {
+    const TinyDesc *table;
+    int32_t first, count;
+    char *arena;
+    float2 *out;
+    int32_t accumulate_root;   // later slices: the root adds into out
+};
+
+cudaError_t launch_tiny_batch(const TinyLaunch &args, int ctas, cudaStream_t stream);
 cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream);
 
@@ -84,6 +95,7 @@ struct DenseArgs {
     int32_t ksplit;
     int64_t kchunk;
     float2 *part;
+    const EpTable *ep;    // address-order store table, or null
 };
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream);

@@ -107,9 +107,9 @@ extern "C" TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Status word back to zero, then this plan's descriptor table.
     cudaError_t e = cudaMemsetAsync(scratch, 0, p.table_off, s);
-    if (e == cudaSuccess && !p.perm_table.empty())
-        e = cudaMemcpyAsync(static_cast<char *>(scratch) + p.table_off, p.perm_table.data(),
-                            p.perm_table.size() * sizeof(tn::PermDesc), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && !p.table_blob.empty())
+        e = cudaMemcpyAsync(static_cast<char *>(scratch) + p.table_off, p.table_blob.data(),
+                            p.table_blob.size(), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) {
         p.last_error = std::string("preparing the static scratch array: ") + cudaGetErrorString(e);
         return TN_ECUDA;

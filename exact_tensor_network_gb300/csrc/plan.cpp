@@ -59,6 +59,7 @@ bool make_runs(const std::vector<int32_t> &oc, const std::vector<int32_t> &side,
         }
     }
     lay->nrun = nrun;
+    for (int i = 0; i < kMaxRuns; ++i) lay->shift[i] = i < nrun ? log2_exact(lay->ext[i]) : -1;
     return true;
 }
 
@@ -302,125 +303,9 @@ tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices
         for (size_t i = 0; i < dims.size(); ++i) {
             lp.perm.dims[i] = dims[i];
             lp.perm.sstride[i] = sst[i];
+            lp.perm.dshift[i] = log2_exact(dims[i]);
         }
     }
-    return TN_OK;
-}
-
-namespace {
-
-struct Interval {
-    uint64_t bytes;
-    int start, end;   // steps; leaves start at -1
-    int id;           // SSA id
-    uint64_t off;
-};
-
-// Offline placement: largest buffers first, each at the lowest offset that
-// does not overlap any placed buffer alive at the same time.  A step's
-// output is alive at its step, as are its operands, so they never alias.
-uint64_t place_buffers(std::vector<Interval> &iv) {
-    std::vector<int> order(iv.size());
-    for (size_t i = 0; i < iv.size(); ++i) order[i] = (int)i;
-    std::sort(order.begin(), order.end(), [&](int x, int y) {
-        if (iv[x].bytes != iv[y].bytes) return iv[x].bytes > iv[y].bytes;
-        return iv[x].start < iv[y].start;
-    });
-    std::vector<int> placed;
-    uint64_t peak = 0;
-    for (int i : order) {
-        std::vector<std::pair<uint64_t, uint64_t>> busy;
-        for (int j : placed)
-            if (!(iv[j].end < iv[i].start || iv[i].end < iv[j].start))
-                busy.push_back({iv[j].off, iv[j].off + iv[j].bytes});
-        std::sort(busy.begin(), busy.end());
-        uint64_t off = 0;
-        for (auto &b : busy) {
-            if (off + iv[i].bytes <= b.first) break;
-            off = std::max(off, (b.second + kAlign - 1) / kAlign * kAlign);
-        }
-        iv[i].off = off;
-        peak = std::max(peak, off + iv[i].bytes);
-        placed.push_back(i);
-    }
-    return (peak + kAlign - 1) / kAlign * kAlign;
-}
-
-}  // namespace
-
-int classify(const Plan &p, const NodePlan &nd);  // defined in exec.cu
-uint64_t launches_per_slice(const Plan &p);        // defined in exec.cu
-void choose_split(const Plan &p, NodePlan &nd);    // defined in exec.cu
-
-tn_status layout_plan(Plan *p) {
-    const int n = p->n_tensors;
-    const int S = (int)p->nodes.size();
-    for (auto &nd : p->nodes) {
-        nd.cls = classify(*p, nd);
-        choose_split(*p, nd);
-    }
-
-    // Storage formats: operands of tensor-core nodes are written planar by
-    // their producers; everything else is complex64.
-    p->fmt.assign(n + S, FMT_C64);
-    const int32_t dense_fmt = p->precision == TN_PREC_BF16 ? FMT_BF2 : FMT_SPLIT4;
-    for (const auto &nd : p->nodes)
-        if (nd.cls == TN_NODE_DENSE) p->fmt[nd.a] = p->fmt[nd.b] = dense_fmt;
-    for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
-
-    std::vector<Interval> iv;
-    p->perm_table.clear();
-    p->perm_leaves.clear();
-    for (int t = 0; t < n; ++t) {
-        LeafPlan &lp = p->leaves[t];
-        lp.in_place = S > 0 && lp.identity && p->fmt[t] == FMT_C64;
-        if (S == 0) {
-            lp.place = {PLACE_OUT, t, 0};
-        } else if (lp.in_place) {
-            lp.place = {PLACE_LEAF, t, 0};
-        } else {
-            iv.push_back({(uint64_t)lp.size * fmt_bytes(p->fmt[t]), -1, p->consumer[t], t, 0});
-        }
-    }
-    for (int s = 0; s < S; ++s) {
-        const NodePlan &nd = p->nodes[s];
-        if (!nd.is_root)
-            iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), s, p->consumer[nd.out], nd.out, 0});
-        if (nd.ksplit > 1)   // split-K partial sums live during the step only
-            iv.push_back({(uint64_t)nd.ksplit * nd.m * nd.n * 8, s, s, n + S + s, 0});
-    }
-    p->arena_bytes = place_buffers(iv);
-    std::vector<Place> where(n + 2 * S, Place{PLACE_WS, -1, 0});
-    for (const auto &b : iv) where[b.id] = {PLACE_WS, -1, b.off};
-    for (int t = 0; t < n; ++t) {
-        LeafPlan &lp = p->leaves[t];
-        if (S > 0 && !lp.in_place) lp.place = where[t];
-        where[t] = lp.place;
-        if (S == 0 || !lp.in_place) {
-            PermDesc d = lp.perm;
-            d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
-            d.fmt = (S == 0) ? FMT_C64 : p->fmt[t];
-            p->perm_table.push_back(d);
-            p->perm_leaves.push_back(t);
-        }
-    }
-    for (int s = 0; s < S; ++s) {
-        NodePlan &nd = p->nodes[s];
-        if (nd.is_root) where[nd.out] = {PLACE_OUT, -1, 0};
-        nd.pa = where[nd.a];
-        nd.pb = where[nd.b];
-        nd.pc = where[nd.out];
-        nd.part = where[n + S + s];
-    }
-    p->table_off = kAlign;
-    p->table_bytes = (p->perm_table.size() * sizeof(PermDesc) + kAlign - 1) / kAlign * kAlign;
-    p->arena_off = p->table_off + p->table_bytes;
-    p->ws_bytes = p->arena_off + p->arena_bytes;
-    p->launches_per_exec = launches_per_slice(*p) * p->n_slices;
-    p->dense_maps.clear();
-    p->maps_ws = nullptr;
-    p->ws = nullptr;
-    p->ws_size = 0;
     return TN_OK;
 }
 

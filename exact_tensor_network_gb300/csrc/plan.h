@@ -32,7 +32,15 @@ struct SepLayout {
     int32_t pad;
     int64_t ext[kMaxRuns];
     int64_t stride[kMaxRuns];
+    int32_t shift[kMaxRuns];   // log2(ext) when ext is a power of two, else -1
 };
+
+inline int32_t log2_exact(int64_t e) {
+    if (e <= 0 || (e & (e - 1)) != 0) return -1;
+    int32_t s = 0;
+    while ((int64_t(1) << s) < e) ++s;
+    return s;
+}
 
 // Storage format of a tensor in HBM.  Every tensor is C64 except the
 // operands of tensor-core (dense) nodes, which their producer writes in the
@@ -63,6 +71,7 @@ struct PermDesc {
     int32_t fmt;            // destination format (Fmt); planes are `size` apart
     int64_t dims[kMaxPermRank];
     int64_t sstride[kMaxPermRank];
+    int32_t dshift[kMaxPermRank];   // log2(dims) for powers of two, else -1
 };
 
 struct LeafPlan {
@@ -93,7 +102,76 @@ struct NodePlan {
     int64_t kchunk;
     Place part;
     int32_t swap;           // stream class: operands swapped so B is the small side
+    // dense class: byte offset (from the workspace start) of the node's
+    // address-order store table (EpTable), or -1 when it has none
+    int64_t ep_off;
 };
+
+// Address-order store table of a tensor-core node.  Every warp of the
+// kernel's epilogue owns 32 output rows x 16 columns at a time; when the
+// output layout repeats identically from one such block to the next, the
+// entry (r, c) of a block lies at block_base + lo_m[r] + lo_n[c], and
+// perm lists the 512 entries (r * 16 + c) by increasing address so that the
+// warp's stores walk memory in order.
+struct EpTable {
+    int64_t lo_m[32];
+    int64_t lo_n[16];
+    uint16_t perm[512];
+};
+
+// One tiny node inside a batched launch (device table).  Its operands and
+// output live in the workspace arena (c_off < 0: the caller's output).
+struct TinyDesc {
+    int64_t a_off, b_off, c_off;
+    int32_t m, n, k;
+    int32_t out_fmt;
+    int32_t is_root;
+    int32_t cta_base;      // first CTA of this node within its launch
+    int32_t ctas;
+    int32_t lanes;         // threads that share one output's k range (1, 4 or 32)
+    SepLayout lm, ln;
+};
+
+// Launch schedule: every node gets a stage one past its operands' stages;
+// stage by stage, the tiny nodes of the stage run as one batched launch and
+// the other nodes one launch each.
+enum LaunchKind : int32_t { LAUNCH_PERMUTE = 0, LAUNCH_NODE = 1, LAUNCH_TINY = 2 };
+struct Launch {
+    int32_t kind;
+    int32_t node;          // LAUNCH_NODE: step
+    int32_t first, count;  // LAUNCH_TINY: range in the tiny table
+    int32_t ctas;          // LAUNCH_TINY: CTAs of the launch
+    uint64_t flops, bytes; // algorithmic work of the launch (measurement)
+};
+
+// Tiny nodes: at most this many complex multiply-adds (m n k).
+constexpr uint64_t kTinyMacs = 1ull << 18;
+
+inline int64_t sep_offset_host(const SepLayout &L, int64_t i) {
+    int64_t off = 0;
+    for (int r = L.nrun - 1; r >= 0; --r) {
+        off += (i % L.ext[r]) * L.stride[r];
+        i /= L.ext[r];
+    }
+    return off;
+}
+
+// True when offsets of index i0 + r (i0 a multiple of B, r < B) split as
+// off(i0) + off(r): B is a product of whole innermost runs times a divisor
+// of the next run.
+inline bool block_invariant(const SepLayout &L, int64_t B) {
+    int64_t c = 1;
+    for (int r = L.nrun - 1; r >= 0; --r) {
+        const int64_t e = L.ext[r];
+        if (B % (c * e) == 0) {
+            c *= e;
+            if (c == B) return true;
+            continue;
+        }
+        return (c * e) % B == 0 && B % c == 0;
+    }
+    return true;
+}
 
 // Aim of the split-K choice: at least this many CTAs per launch (two per
 // SM of a GB300).
@@ -131,6 +209,9 @@ struct Plan {
     uint64_t ws_bytes = 0;
     std::vector<PermDesc> perm_table;
     std::vector<int32_t> perm_leaves;           // leaf of each table entry
+    std::vector<unsigned char> table_blob;      // device tables: PermDesc[], EpTable[], TinyDesc[]
+    std::vector<Launch> sched;                  // launches of one slice, in order
+    uint64_t tiny_off = 0;                      // workspace offset of the TinyDesc table
     std::vector<int32_t> fmt;                   // per SSA id (Fmt)
     std::vector<DenseMaps> dense_maps;          // per dense node, set at bind
     void *maps_ws = nullptr;                    // workspace the maps point into

@@ -1,0 +1,264 @@
+// Node classes, launch schedule, workspace layout and device tables.
+//
+// Runs after build_plan (and again whenever the policy changes); host only.
+//   1. classify every node (tensor-core, streaming, general, tiny) and
+//      choose its split-K;
+//   2. storage formats: operands of tensor-core nodes are written planar by
+//      their producers, everything else is complex64;
+//   3. schedule: a node's stage is one past the stages of its operands; stage
+//      by stage, all tiny nodes of the stage form one batched launch and
+//      every other node gets its own launch (the root, which depends on
+//      everything, comes last);
+//   4. buffer lifetimes on that launch order and an offline placement into
+//      one arena (largest first, lowest free offset);
+//   5. device tables: leaf permutation jobs, address-order store tables of
+//      tensor-core nodes, tiny-node descriptors.
+#include <algorithm>
+#include <cstring>
+
+#include "plan.h"
+
+namespace tn {
+
+int classify(const Plan &p, const NodePlan &nd);   // exec.cu
+void choose_split(const Plan &p, NodePlan &nd);    // exec.cu
+uint64_t launches_per_slice(const Plan &p);        // exec.cu
+
+namespace {
+
+struct Interval {
+    uint64_t bytes;
+    int start, end;   // launch indices; leaf copies start at -1
+    int id;
+    uint64_t off;
+};
+
+// Largest buffers first, each at the lowest offset that overlaps no placed
+// buffer alive at the same time.  Operands end at the launch that reads
+// them and outputs start there, so a launch never aliases its own buffers.
+uint64_t place_buffers(std::vector<Interval> &iv) {
+    std::vector<int> order(iv.size());
+    for (size_t i = 0; i < iv.size(); ++i) order[i] = (int)i;
+    std::sort(order.begin(), order.end(), [&](int x, int y) {
+        if (iv[x].bytes != iv[y].bytes) return iv[x].bytes > iv[y].bytes;
+        return iv[x].start < iv[y].start;
+    });
+    std::vector<int> placed;
+    uint64_t peak = 0;
+    for (int i : order) {
+        std::vector<std::pair<uint64_t, uint64_t>> busy;
+        for (int j : placed)
+            if (!(iv[j].end < iv[i].start || iv[i].end < iv[j].start))
+                busy.push_back({iv[j].off, iv[j].off + iv[j].bytes});
+        std::sort(busy.begin(), busy.end());
+        uint64_t off = 0;
+        for (auto &b : busy) {
+            if (off + iv[i].bytes <= b.first) break;
+            off = std::max(off, (b.second + kAlign - 1) / kAlign * kAlign);
+        }
+        iv[i].off = off;
+        peak = std::max(peak, off + iv[i].bytes);
+        placed.push_back(i);
+    }
+    return (peak + kAlign - 1) / kAlign * kAlign;
+}
+
+uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool make_ep_table(const NodePlan &nd, EpTable *t) {
+    if (!block_invariant(nd.lm, 32) || !block_invariant(nd.ln, 16)) return false;
+    std::memset(t, 0, sizeof(*t));
+    for (int r = 0; r < 32; ++r) t->lo_m[r] = r < (int64_t)nd.m ? sep_offset_host(nd.lm, r) : 0;
+    for (int c = 0; c < 16; ++c) t->lo_n[c] = c < (int64_t)nd.n ? sep_offset_host(nd.ln, c) : 0;
+    std::vector<uint16_t> idx(512);
+    for (int e = 0; e < 512; ++e) idx[e] = (uint16_t)e;
+    auto key = [&](uint16_t e) -> int64_t {
+        const int r = e >> 4, c = e & 15;
+        if (r >= (int64_t)nd.m || c >= (int64_t)nd.n) return INT64_MAX;
+        return t->lo_m[r] + t->lo_n[c];
+    };
+    std::stable_sort(idx.begin(), idx.end(), [&](uint16_t x, uint16_t y) { return key(x) < key(y); });
+    for (int e = 0; e < 512; ++e) t->perm[e] = idx[e];
+    return true;
+}
+
+}  // namespace
+
+tn_status layout_plan(Plan *p) {
+    const int n = p->n_tensors;
+    const int S = (int)p->nodes.size();
+    for (auto &nd : p->nodes) {
+        nd.cls = classify(*p, nd);
+        choose_split(*p, nd);
+    }
+
+    // 2. formats
+    p->fmt.assign(n + S, FMT_C64);
+    const int32_t dense_fmt = p->precision == TN_PREC_BF16 ? FMT_BF2 : FMT_SPLIT4;
+    for (const auto &nd : p->nodes)
+        if (nd.cls == TN_NODE_DENSE) p->fmt[nd.a] = p->fmt[nd.b] = dense_fmt;
+    for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
+
+    // 3. schedule
+    std::vector<int> stage(n + S, 0);
+    int max_stage = 0;
+    for (const auto &nd : p->nodes) {
+        stage[nd.out] = 1 + std::max(stage[nd.a], stage[nd.b]);
+        max_stage = std::max(max_stage, stage[nd.out]);
+    }
+    std::vector<std::vector<int>> by_stage(max_stage + 1);
+    for (int s = 0; s < S; ++s) by_stage[stage[n + s]].push_back(s);
+    p->sched.clear();
+    std::vector<int> t_of(n + S, -1);   // launch index producing each id
+    std::vector<std::vector<int>> tiny_batches;
+    for (int st = 1; st <= max_stage; ++st) {
+        std::vector<int> tiny;
+        for (int s : by_stage[st])
+            if (p->nodes[s].cls == TN_NODE_TINY) tiny.push_back(s);
+        if (!tiny.empty()) {
+            Launch L{};
+            L.kind = LAUNCH_TINY;
+            L.node = -1;
+            for (int s : tiny) t_of[n + s] = (int)p->sched.size();
+            tiny_batches.push_back(tiny);
+            p->sched.push_back(L);
+        }
+        for (int s : by_stage[st]) {
+            if (p->nodes[s].cls == TN_NODE_TINY) continue;
+            Launch L{};
+            L.kind = LAUNCH_NODE;
+            L.node = s;
+            t_of[n + s] = (int)p->sched.size();
+            p->sched.push_back(L);
+        }
+    }
+    auto consume_t = [&](int id) { return p->consumer[id] < 0 ? (int)p->sched.size()
+                                                               : t_of[n + p->consumer[id]]; };
+
+    // 4. lifetimes and placement
+    std::vector<Interval> iv;
+    for (int t = 0; t < n; ++t) {
+        LeafPlan &lp = p->leaves[t];
+        const bool tiny_consumer = S > 0 && p->nodes[p->consumer[t]].cls == TN_NODE_TINY;
+        lp.in_place = S > 0 && lp.identity && p->fmt[t] == FMT_C64 && !tiny_consumer;
+        if (S == 0) {
+            lp.place = {PLACE_OUT, t, 0};
+        } else if (lp.in_place) {
+            lp.place = {PLACE_LEAF, t, 0};
+        } else {
+            iv.push_back({(uint64_t)lp.size * fmt_bytes(p->fmt[t]), -1, consume_t(t), t, 0});
+        }
+    }
+    for (int s = 0; s < S; ++s) {
+        const NodePlan &nd = p->nodes[s];
+        const int ts = t_of[n + s];
+        if (!nd.is_root)
+            iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), ts, consume_t(nd.out), nd.out, 0});
+        if (nd.ksplit > 1)
+            iv.push_back({(uint64_t)nd.ksplit * nd.m * nd.n * 8, ts, ts, n + S + s, 0});
+    }
+    p->arena_bytes = place_buffers(iv);
+    std::vector<Place> where(n + 2 * S, Place{PLACE_WS, -1, 0});
+    for (const auto &b : iv) where[b.id] = {PLACE_WS, -1, b.off};
+    p->perm_table.clear();
+    p->perm_leaves.clear();
+    for (int t = 0; t < n; ++t) {
+        LeafPlan &lp = p->leaves[t];
+        if (S > 0 && !lp.in_place) lp.place = where[t];
+        where[t] = lp.place;
+        if (S == 0 || !lp.in_place) {
+            PermDesc d = lp.perm;
+            d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
+            d.fmt = (S == 0) ? FMT_C64 : p->fmt[t];
+            p->perm_table.push_back(d);
+            p->perm_leaves.push_back(t);
+        }
+    }
+    if (!p->perm_table.empty()) {
+        Launch L{};
+        L.kind = LAUNCH_PERMUTE;
+        L.node = -1;
+        for (const auto &d : p->perm_table) L.bytes += 16 * (uint64_t)d.size;
+        p->sched.insert(p->sched.begin(), L);
+    }
+    for (int s = 0; s < S; ++s) {
+        NodePlan &nd = p->nodes[s];
+        if (nd.is_root) where[nd.out] = {PLACE_OUT, -1, 0};
+        nd.pa = where[nd.a];
+        nd.pb = where[nd.b];
+        nd.pc = where[nd.out];
+        nd.part = where[n + S + s];
+    }
+
+    // 5. device tables
+    p->table_off = kAlign;
+    const uint64_t perm_bytes = p->perm_table.size() * sizeof(PermDesc);
+    const uint64_t ep_start = align_up(perm_bytes);
+    std::vector<EpTable> eps;
+    for (auto &nd : p->nodes) {
+        nd.ep_off = -1;
+        if (nd.cls != TN_NODE_DENSE || nd.ksplit > 1) continue;
+        EpTable t;
+        if (!make_ep_table(nd, &t)) continue;
+        nd.ep_off = (int64_t)(p->table_off + ep_start + eps.size() * sizeof(EpTable));
+        eps.push_back(t);
+    }
+    std::vector<TinyDesc> tiny;
+    size_t batch = 0;
+    for (auto &L : p->sched) {
+        if (L.kind != LAUNCH_TINY) continue;
+        L.first = (int32_t)tiny.size();
+        L.count = (int32_t)tiny_batches[batch].size();
+        int ctas = 0;
+        for (int s : tiny_batches[batch]) {
+            const NodePlan &nd = p->nodes[s];
+            TinyDesc d;
+            std::memset(&d, 0, sizeof(d));
+            d.a_off = (int64_t)nd.pa.off;
+            d.b_off = (int64_t)nd.pb.off;
+            d.c_off = nd.pc.kind == PLACE_OUT ? -1 : (int64_t)nd.pc.off;
+            d.m = (int32_t)nd.m;
+            d.n = (int32_t)nd.n;
+            d.k = (int32_t)nd.k;
+            d.out_fmt = nd.out_fmt;
+            d.is_root = nd.is_root ? 1 : 0;
+            const uint64_t macs = nd.m * nd.n * nd.k;
+            d.ctas = (int32_t)std::max<uint64_t>(1, std::min<uint64_t>((macs + 8191) / 8192,
+                                                                       (nd.m * nd.n + 7) / 8));
+            d.lanes = nd.k >= 64 ? 32 : nd.k >= 8 ? 4 : 1;
+            d.cta_base = ctas;
+            d.lm = nd.lm;
+            d.ln = nd.ln;
+            ctas += d.ctas;
+            L.flops += 8 * macs;
+            L.bytes += 8 * (nd.m * nd.k + nd.n * nd.k + nd.m * nd.n);
+            tiny.push_back(d);
+        }
+        L.ctas = ctas;
+        ++batch;
+    }
+    for (auto &L : p->sched) {
+        if (L.kind != LAUNCH_NODE) continue;
+        const NodePlan &nd = p->nodes[L.node];
+        L.flops = 8 * nd.m * nd.n * nd.k;
+    }
+    const uint64_t tiny_start = align_up(ep_start + eps.size() * sizeof(EpTable));
+    p->tiny_off = p->table_off + tiny_start;
+    p->table_blob.assign(tiny_start + tiny.size() * sizeof(TinyDesc), 0);
+    if (perm_bytes) std::memcpy(p->table_blob.data(), p->perm_table.data(), perm_bytes);
+    if (!eps.empty())
+        std::memcpy(p->table_blob.data() + ep_start, eps.data(), eps.size() * sizeof(EpTable));
+    if (!tiny.empty())
+        std::memcpy(p->table_blob.data() + tiny_start, tiny.data(), tiny.size() * sizeof(TinyDesc));
+    p->table_bytes = align_up(p->table_blob.size());
+    p->arena_off = p->table_off + p->table_bytes;
+    p->ws_bytes = p->arena_off + p->arena_bytes;
+    p->launches_per_exec = launches_per_slice(*p) * p->n_slices;
+    p->dense_maps.clear();
+    p->maps_ws = nullptr;
+    p->ws = nullptr;
+    p->ws_size = 0;
+    return TN_OK;
+}
+
+}  // namespace tn

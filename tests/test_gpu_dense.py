@@ -98,6 +98,20 @@ def test_interleaved_output_layout():
     assert_close(got, _ref(net, tree), TOL_C64, "interleaved dense output")
 
 
+@pytest.mark.parametrize("ext", [[6, 12, 100, 64, 5], [16, 2, 64, 32, 4], [3, 64, 48, 16, 6]])
+def test_interleaved_output_general_extents(ext):
+    """Interleaved output whose blocks do not repeat (extents 3, 6, 12):
+    the epilogue cannot use an address-order table and falls back."""
+    rng = np.random.default_rng(sum(ext))
+    tensors = [[0, 1, 3], [2, 3], [1, 4]]
+    data = [_rand(rng, [ext[x] for x in t]) for t in tensors]
+    net = Network(tensors, ext, [0, 2, 4], data)
+    tree = [(0, 1), (3, 2)]
+    got, plan = run_gpu(net, tree, policy=tn.TN_POLICY_DENSE)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE
+    assert_close(got, _ref(net, tree), TOL_C64, f"interleaved {ext}")
+
+
 @pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
 def test_dense_chain(precision, tol):
     # A[a,x] B[x,b] -> C[a,b] (dense, planar output), C[a,b] D[b,c] -> root (dense)

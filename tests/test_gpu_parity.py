@@ -141,6 +141,20 @@ def test_simt_policy_matches_auto():
     assert_close(b, ref, what="simt policy vs oracle")
 
 
+@pytest.mark.parametrize("name", ["circuit_3x3_d4", "random_60"])
+def test_tiny_batching_matches_unbatched(name):
+    """Tiny nodes batched per schedule stage (auto) and launched one by one
+    (no-tiny policy) both match the oracle."""
+    import exact_tensor_network_gb300 as tn
+    net, tree, _ = configs.by_name(name)
+    ref = _ref(net, tree)
+    a, pa = run_gpu(net, tree, policy=tn.TN_POLICY_AUTO)
+    b, pb = run_gpu(net, tree, policy=tn.TN_POLICY_NO_TINY)
+    assert pa.launches < pb.launches
+    assert_close(a, ref, what=f"{name} batched tiny nodes")
+    assert_close(b, ref, what=f"{name} one launch per node")
+
+
 def test_profiling_records_every_launch():
     import torch
     import exact_tensor_network_gb300 as tn

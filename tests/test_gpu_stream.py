@@ -42,11 +42,16 @@ def _ref(net, tree):
     (17, 17, 17, tn.TN_NODE_SIMT),
 ])
 def test_stream_and_split_nodes(m, n, k, cls):
+    """Class expected with tiny batching off; then the same node under the
+    default policy (where small ones go to the tiny-node kernel)."""
     net = node_network(m, n, k, m * 7 + n * 3 + k)
-    p = tn.Plan.from_network(net, [(0, 1)])
+    p = tn.Plan.from_network(net, [(0, 1)], (), "tf32x3", tn.TN_POLICY_NO_TINY)
     assert p.node_class(0) == cls
-    got, _ = run_gpu(net, [(0, 1)])
-    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, f"node {m}x{n}x{k}")
+    ref = _ref(net, [(0, 1)])
+    got, _ = run_gpu(net, [(0, 1)], policy=tn.TN_POLICY_NO_TINY)
+    assert_close(got, ref, TOL_C64, f"node {m}x{n}x{k}")
+    got2, _ = run_gpu(net, [(0, 1)])
+    assert_close(got2, ref, TOL_C64, f"node {m}x{n}x{k} default policy")
 
 
 def test_split_root_with_slices_accumulates():
