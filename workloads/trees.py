@@ -23,10 +23,10 @@ def _prod(extents: Sequence[int], modes) -> int:
 
 
 def greedy_tree(net: Network, seed: int, noise: float = 0.0,
-                exclude: Sequence[int] = ()) -> Tree:
+                exclude: Sequence[int] = (), alpha: float = 1.0) -> Tree:
     """Repeatedly contract the pair of live tensors sharing a mode that
-    minimises |out| - |a| - |b| (ties broken by a seeded random key; with
-    ``noise`` > 0 the score is also multiplied by a random factor in
+    minimises |out| - alpha (|a| + |b|) (ties broken by a seeded random key;
+    with ``noise`` > 0 the score is also multiplied by a random factor in
     [1-noise, 1+noise] for positive scores).  Tensors with nothing in common
     are joined at the end, smallest first.  Modes in ``exclude`` are
     treated as absent (extent 1), as when they are sliced."""
@@ -45,7 +45,7 @@ def greedy_tree(net: Network, seed: int, noise: float = 0.0,
 
     def push(a: int, b: int) -> None:
         out = live[a] ^ live[b]
-        score = float(_prod(ext, out) - size[a] - size[b])
+        score = float(_prod(ext, out)) - alpha * float(size[a] + size[b])
         if noise > 0.0:
             f = 1.0 + noise * (2.0 * rng.random() - 1.0)
             score = score * f if score > 0 else score / f
