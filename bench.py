@@ -172,6 +172,20 @@ def oracle_subtree_sample(net, tree, slices, budget: float):
     modes = planner.tensor_modes(net.tensors, tree, slices)
     leaves_t, leaves_d = oracle.slice_leaves(net.tensors, net.data, slices, [0] * len(slices))
     flops, secs = 0, 0.0
+    if not chosen:
+        # not even one subtree fits: contract one block of the output
+        # instead, fixing leading open modes at index 0
+        from workloads.trees import step_volume
+        fixed = []
+        for x in net.open_modes:
+            if 8 * step_volume(net, tree, exclude=list(slices) + fixed) <= budget:
+                break
+            fixed.append(x)
+        cost_b = 8 * step_volume(net, tree, exclude=list(slices) + fixed)
+        t2, d2 = oracle.slice_leaves(leaves_t, leaves_d, fixed, [0] * len(fixed))
+        t0 = time.perf_counter()
+        oracle.contract(t2, net.extents, [x for x in net.open_modes if x not in fixed], d2, tree)
+        return cost_b, time.perf_counter() - t0, 1, oracle.num_threads()
     for x in chosen:
         sub_leaves, steps = [], []
 
