@@ -61,6 +61,33 @@ def kernel_peak(kernel: str, pk):
     return "hbm", pk["hbm_gbs"], "GB/s", f"copy bandwidth, {pk['source']}"
 
 
+KERNEL_SOURCES = {
+    "dense_tf32x3": ["k_dense.cu", "common.cuh"],
+    "dense_bf16": ["k_dense.cu", "common.cuh"],
+}
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture in
+    profiles/dram_traffic.md, if the kernel's source still matches."""
+    import hashlib
+    srcs = KERNEL_SOURCES.get(kernel)
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not srcs or not os.path.exists(path):
+        return None
+    h = hashlib.sha1()
+    for f in srcs:
+        with open(os.path.join(ROOT, "exact_tensor_network_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()[:16]
+    with open(path) as fh:
+        for line in fh:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) == 5 and cells[0] == kernel and cells[1] == workload and cells[2] == sha:
+                return float(cells[4])
+    return None
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during a region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -350,7 +377,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
     per_launch = d["flops" if unit == "TFLOP/s" else "bytes"] / d["launches"]
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None, "peak_note": note + " (of " + pk["source"] + ")",
+                "frac": achieved / peak, "traffic": measured_traffic(dom, net.name),
+                "traffic_unit": "bytes per launch (ncu dram read + write)",
+                "peak_note": note + " (of " + pk["source"] + ")",
                 "algorithmic_per_launch": per_launch,
                 "avg_launch_ms": d["ms"] / d["launches"]}
     kernels = {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps,

@@ -54,7 +54,8 @@ class tn_launch_record(ctypes.Structure):
                 ("flops", ctypes.c_uint64), ("bytes", ctypes.c_uint64)]
 
 
-KERNEL_NAMES = {0: "permute", 1: "simt", 2: "dense_tf32x3", 3: "dense_bf16", 4: "stream", 5: "tiny"}
+KERNEL_NAMES = {0: "permute", 1: "simt", 2: "dense_tf32x3", 3: "dense_bf16", 4: "stream", 5: "tiny",
+                6: "reduce"}
 
 
 class tn_slices(ctypes.Structure):

@@ -390,12 +390,9 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                 r.ln = sw ? nd.lm : nd.ln;
                 r.accumulate = accumulate;
                 r.out_fmt = nd.out_fmt;
-                const int32_t kid = nd.cls == TN_NODE_STREAM ? TN_KERNEL_STREAM
-                                    : nd.cls == TN_NODE_DENSE
-                                        ? (p->precision == TN_PREC_BF16 ? TN_KERNEL_DENSE_BF16
-                                                                        : TN_KERNEL_DENSE_TF32X3)
-                                        : TN_KERNEL_SIMT;
-                rec.begin(kid, nd.step, 0, 0);
+                // bytes: every partial read once, the output written once
+                rec.begin(TN_KERNEL_REDUCE, nd.step, 0,
+                          8 * (uint64_t)nd.ksplit * nd.m * nd.n + fmt_bytes(nd.out_fmt) * nd.m * nd.n);
                 e = launch_splitk_reduce(r, stream);
                 rec.end();
             }

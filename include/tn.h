@@ -244,7 +244,8 @@ enum {
     TN_KERNEL_DENSE_TF32X3 = 2, /* tcgen05 node kernel, split tf32 */
     TN_KERNEL_DENSE_BF16 = 3,   /* tcgen05 node kernel, bf16 operands */
     TN_KERNEL_STREAM = 4,       /* bandwidth-bound node kernel */
-    TN_KERNEL_TINY = 5          /* batched tiny-node kernel */
+    TN_KERNEL_TINY = 5,         /* batched tiny-node kernel */
+    TN_KERNEL_REDUCE = 6        /* ordered sum of split-K partials */
 };
 
 /* One kernel launch of a profiled tn_execute.  flops = 8 m n k of the
