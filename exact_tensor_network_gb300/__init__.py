@@ -84,6 +84,7 @@ SIGNATURES = {
     "tn_plan_set_workspace": (ctypes.c_int, [_P, _P, ctypes.c_uint64]),
     "tn_execute": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_execute_static": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
+    "tn_plan_set_replay": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_plan_check": (ctypes.c_int, [_P]),
     "tn_plan_launches": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_profiling": (ctypes.c_int, [_P, ctypes.c_int32]),
@@ -213,6 +214,10 @@ def tn_execute_static(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream:
     that cannot allocate device memory (no workspace needed; see tn.h)."""
     arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
     _check(lib().tn_execute_static(plan, arr, out_ptr, stream), plan)
+
+
+def tn_plan_set_replay(plan: int, enable: bool) -> None:
+    _check(lib().tn_plan_set_replay(plan, 1 if enable else 0), plan)
 
 
 def tn_plan_check(plan: int) -> None:

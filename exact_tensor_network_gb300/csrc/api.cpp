@@ -12,6 +12,8 @@ namespace tn {
 tn_status upload_tables(Plan *p);
 tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream);
 tn_status check_plan(Plan *p);
+tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
+                           cudaStream_t stream);
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len);
 }  // namespace tn
 
@@ -148,13 +150,20 @@ tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_pt
         p.last_error = "no workspace bound (tn_plan_set_workspace)";
         return TN_ENOMEM;
     }
-    return tn::execute_plan(&p, leaf_ptrs, out_ptr, reinterpret_cast<cudaStream_t>(stream));
+    return tn::execute_replayed(&p, leaf_ptrs, out_ptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tn_status tn_plan_check(tn_plan_t *plan) {
     if (!plan) return TN_EINVAL;
     if (!plan->p.ws) return TN_OK;
     return tn::check_plan(&plan->p);
+}
+
+tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable) {
+    if (!plan) return TN_EINVAL;
+    tn::drop_graph(&plan->p);
+    plan->p.use_graph = enable != 0;
+    return TN_OK;
 }
 
 tn_status tn_plan_launches(const tn_plan_t *plan, uint64_t *n) {

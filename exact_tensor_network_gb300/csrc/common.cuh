@@ -43,8 +43,35 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(r);
 }
 
-// Store entry `off` of a tensor in format `fmt` (see Fmt in plan.h); planes
-// are `plane` entries apart.  `accumulate` adds into a C64 destination.
+// Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
+// plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
+// destination.  Kernels instantiated per format keep one store path.
+template <int FMT>
+__device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t off, float2 v,
+                                              int32_t accumulate) {
+    if constexpr (FMT == FMT_C64) {
+        float2 *p = static_cast<float2 *>(dst) + off;
+        if (accumulate) {
+            const float2 o = *p;
+            v.x += o.x;
+            v.y += o.y;
+        }
+        *p = v;
+    } else if constexpr (FMT == FMT_SPLIT4) {
+        float *p = static_cast<float *>(dst) + off;
+        const float rh = to_tf32(v.x), ih = to_tf32(v.y);
+        p[0] = rh;
+        p[plane] = ih;
+        p[2 * plane] = to_tf32(v.x - rh);
+        p[3 * plane] = to_tf32(v.y - ih);
+    } else {
+        __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
+        p[0] = __float2bfloat16_rn(v.x);
+        p[plane] = __float2bfloat16_rn(v.y);
+    }
+}
+
+// Same with the format chosen at run time.
 __device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plane, int64_t off,
                                             float2 v, int32_t accumulate) {
     if (fmt == FMT_C64) {

@@ -71,7 +71,8 @@ void choose_split(const Plan &p, NodePlan &nd) {
         const uint64_t tiles = ((nd.m + 127) / 128) * ((nd.n + 127) / 128);
         const uint64_t sms = kTargetCtas / 2;
         if (tiles >= sms || nd.k < 512) return;
-        uint64_t s = std::min<uint64_t>((sms + tiles - 1) / tiles, nd.k / 256);
+        // whole waves only: tiles x splits <= SMs
+        uint64_t s = std::min<uint64_t>(sms / tiles, nd.k / 256);
         s = std::min<uint64_t>(s, kPartialBudget / (8 * outs));
         if (s < 2) return;
         uint64_t chunk = (nd.k + s - 1) / s;
@@ -118,10 +119,21 @@ uint64_t launches_per_slice(const Plan &p) {
     return n;
 }
 
+void drop_graph(Plan *p) {
+    if (p->graph_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->graph_exec));
+    p->graph_exec = nullptr;
+    p->graph_leaves.clear();
+    p->graph_out = nullptr;
+    p->graph_ws = nullptr;
+}
+
 void release_events(Plan *p) {
     for (void *e : p->events)
         if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
     p->events.clear();
+    drop_graph(p);
+    if (p->capture_stream) cudaStreamDestroy(static_cast<cudaStream_t>(p->capture_stream));
+    p->capture_stream = nullptr;
 }
 
 namespace {
@@ -404,6 +416,68 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     }
     delete pl;
     return st;
+}
+
+// tn_execute: the first call with a given (leaves, output, workspace) runs
+// the launch sequence directly and then records it, captured on the plan's
+// own stream, into a CUDA graph; later calls with the same buffers replay
+// the graph on the caller's stream, which removes the host-side launch
+// work and most of the gaps between dependent launches.  Profiling runs
+// always launch directly.  If capture is unavailable the plan simply keeps
+// launching directly.
+tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
+                           cudaStream_t stream) {
+    if (!p->use_graph || p->profiling) return execute_plan(p, leaf_ptrs, out_ptr, stream);
+    // a caller that is capturing its own stream gets the launches recorded
+    // into its capture
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return execute_plan(p, leaf_ptrs, out_ptr, stream);
+    }
+    const int n = p->n_tensors;
+    bool hit = p->graph_exec && p->graph_out == out_ptr && p->graph_ws == p->ws &&
+               (int)p->graph_leaves.size() == n;
+    for (int t = 0; hit && t < n; ++t) hit = p->graph_leaves[t] == leaf_ptrs[t];
+    if (hit) {
+        cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(p->graph_exec), stream);
+        if (e != cudaSuccess) return cuda_fail(p, e, "launching the recorded graph");
+        return TN_OK;
+    }
+    drop_graph(p);
+    tn_status st = execute_plan(p, leaf_ptrs, out_ptr, stream);
+    if (st != TN_OK) return st;
+    if (!p->capture_stream) {
+        cudaStream_t s;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            p->use_graph = false;
+            return TN_OK;
+        }
+        p->capture_stream = s;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(p->capture_stream);
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        p->use_graph = false;
+        return TN_OK;
+    }
+    const tn_status cst = execute_plan(p, leaf_ptrs, out_ptr, cs);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cs, &g);
+    cudaGraphExec_t ex = nullptr;
+    if (cst == TN_OK && e == cudaSuccess && g) e = cudaGraphInstantiate(&ex, g, 0);
+    if (g) cudaGraphDestroy(g);
+    if (cst != TN_OK || e != cudaSuccess || !ex) {
+        cudaGetLastError();
+        p->use_graph = false;   // keep launching directly
+        return TN_OK;
+    }
+    p->graph_exec = ex;
+    p->graph_leaves.assign(leaf_ptrs, leaf_ptrs + n);
+    p->graph_out = out_ptr;
+    p->graph_ws = p->ws;
+    return TN_OK;
 }
 
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len) {

@@ -541,8 +541,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream) {
-    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
-    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    const int64_t work = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN) *
+                         (args.ksplit > 1 ? args.ksplit : 1);
+    const int grid = static_cast<int>(work < num_sms ? work : num_sms);
     if (grid <= 0) return cudaSuccess;
     if (args.bf16) {
         static bool attr = false;

@@ -7,8 +7,9 @@
 // offM(i) + offN(j), which covers outputs whose order interleaves M and N
 // modes without any transpose pass.
 //
-// 64 x 64 output tile per CTA, 256 threads each owning a 4 x 4 block of
-// complex accumulators; K staged through shared memory 16 entries at a
+// 64 x 64 output tile per CTA, 256 threads each owning 4 x 4 complex
+// accumulators (rows ty + 16r, columns tx + 16c, so that 16 lanes store 16
+// consecutive columns); K staged through shared memory 16 entries at a
 // time.  Any shape works (ragged edges are masked); the tensor-core and
 // streaming kernels take the shapes they are faster on.
 #include "common.cuh"
@@ -21,6 +22,7 @@ namespace {
 constexpr int BM = 64, BN = 64, BK = 16, TM = 4, TN = 4;
 constexpr int kThreads = (BM / TM) * (BN / TN);
 
+template <int FMT>
 __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_constant__ NodeArgs a) {
     __shared__ float2 As[BK][BM + 1];
     __shared__ float2 Bs[BK][BN + 1];
@@ -53,13 +55,13 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
                 Bs[c][r] = (j < a.n && kk < kend) ? a.B[j * a.k + kk] : make_float2(0.f, 0.f);
             }
             __syncthreads();
-#pragma unroll
+#pragma unroll 2
             for (int kk = 0; kk < BK; ++kk) {
                 float2 av[TM], bv[TN];
 #pragma unroll
-                for (int r = 0; r < TM; ++r) av[r] = As[kk][ty * TM + r];
+                for (int r = 0; r < TM; ++r) av[r] = As[kk][ty + r * (BM / TM)];
 #pragma unroll
-                for (int c = 0; c < TN; ++c) bv[c] = Bs[kk][tx * TN + c];
+                for (int c = 0; c < TN; ++c) bv[c] = Bs[kk][tx + c * (BN / TN)];
 #pragma unroll
                 for (int r = 0; r < TM; ++r)
 #pragma unroll
@@ -71,12 +73,12 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             // plain partial sums of this k range
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
-                const int64_t i = i0 + ty * TM + r;
+                const int64_t i = i0 + ty + r * (BM / TM);
                 if (i >= a.m) continue;
                 float2 *dst = a.part + ((int64_t)split * a.m + i) * a.n;
 #pragma unroll
                 for (int c = 0; c < TN; ++c) {
-                    const int64_t j = j0 + tx * TN + c;
+                    const int64_t j = j0 + tx + c * (BN / TN);
                     if (j < a.n) dst[j] = acc[r][c];
                 }
             }
@@ -85,19 +87,19 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
         int64_t offn[TN];
 #pragma unroll
         for (int c = 0; c < TN; ++c) {
-            const int64_t j = j0 + tx * TN + c;
+            const int64_t j = j0 + tx + c * (BN / TN);
             offn[c] = j < a.n ? sep_offset(a.ln, j) : 0;
         }
 #pragma unroll
         for (int r = 0; r < TM; ++r) {
-            const int64_t i = i0 + ty * TM + r;
+            const int64_t i = i0 + ty + r * (BM / TM);
             if (i >= a.m) continue;
             const int64_t offm = sep_offset(a.lm, i);
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
-                const int64_t j = j0 + tx * TN + c;
+                const int64_t j = j0 + tx + c * (BN / TN);
                 if (j >= a.n) continue;
-                store_entry(a.C, a.out_fmt, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate);
+                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate);
             }
         }
     }
@@ -108,7 +110,12 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
 cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
     const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN) * args.ksplit;
     const int64_t grid = tiles < 152 * 16 ? tiles : 152 * 16;
-    simt_node_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(args);
+    if (args.out_fmt == FMT_SPLIT4)
+        simt_node_kernel<FMT_SPLIT4><<<(unsigned)grid, kThreads, 0, stream>>>(args);
+    else if (args.out_fmt == FMT_BF2)
+        simt_node_kernel<FMT_BF2><<<(unsigned)grid, kThreads, 0, stream>>>(args);
+    else
+        simt_node_kernel<FMT_C64><<<(unsigned)grid, kThreads, 0, stream>>>(args);
     return cudaGetLastError();
 }
 

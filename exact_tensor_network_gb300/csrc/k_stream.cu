@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
+template <int FMT>
 __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_constant__ StreamArgs a) {
     __shared__ float2 Bs[kStreamMaxN * kStreamKc];
     const int s = blockIdx.y;
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
 #pragma unroll
                 for (int j = 0; j < kStreamMaxN; ++j)
                     if (j < n)
-                        store_entry(a.C, a.out_fmt, a.m * a.n, offm + sep_offset(a.ln, j), acc[j],
+                        store_entry_t<FMT>(a.C, a.m * a.n, offm + sep_offset(a.ln, j), acc[j],
                                     a.accumulate);
             }
         }
@@ -103,7 +104,12 @@ __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_co
 cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
     const int64_t blocks = (args.m + args.rows_per_cta - 1) / args.rows_per_cta;
     dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
-    stream_node_kernel<<<grid, kThreads, 0, stream>>>(args);
+    if (args.out_fmt == FMT_SPLIT4)
+        stream_node_kernel<FMT_SPLIT4><<<grid, kThreads, 0, stream>>>(args);
+    else if (args.out_fmt == FMT_BF2)
+        stream_node_kernel<FMT_BF2><<<grid, kThreads, 0, stream>>>(args);
+    else
+        stream_node_kernel<FMT_C64><<<grid, kThreads, 0, stream>>>(args);
     return cudaGetLastError();
 }
 

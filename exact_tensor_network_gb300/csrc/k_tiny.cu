@@ -51,7 +51,18 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
         const int i = o32 / d.n, j = o32 - i * d.n;
         if (o < o1) {
             const float2 *ar = A + (int64_t)i * k, *br = B + (int64_t)j * k;
-            for (int kk = l; kk < k; kk += lanes) cfma(acc, ar[kk], br[kk]);
+            // eight independent load pairs in flight per round
+            for (int kk = l; kk < k; kk += 8 * lanes) {
+                float2 av[8], bv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int idx = kk + u * lanes;
+                    av[u] = idx < k ? ar[idx] : make_float2(0.f, 0.f);
+                    bv[u] = idx < k ? br[idx] : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) cfma(acc, av[u], bv[u]);
+            }
         }
         for (int off = lanes >> 1; off > 0; off >>= 1) {
             acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, lanes);

@@ -223,6 +223,16 @@ struct Plan {
     std::vector<tn_launch_record> records;
     uint64_t launches_per_exec = 0;
 
+    // replay: the launch sequence of the last (leaves, output, workspace)
+    // captured as a CUDA graph (graph exec and capture stream as opaque
+    // handles; exec.cu)
+    bool use_graph = true;
+    void *graph_exec = nullptr;
+    void *capture_stream = nullptr;
+    std::vector<const void *> graph_leaves;
+    void *graph_out = nullptr;
+    void *graph_ws = nullptr;
+
     // binding
     void *ws = nullptr;
     uint64_t ws_size = 0;
@@ -239,8 +249,11 @@ tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices
 // Classify nodes under plan->policy and lay out the workspace.
 tn_status layout_plan(Plan *plan);
 
-// Destroy the plan's CUDA events (exec.cu).
+// Destroy the plan's CUDA events, recorded graph and capture stream (exec.cu).
 void release_events(Plan *plan);
+
+// Forget the recorded launch graph (exec.cu).
+void drop_graph(Plan *plan);
 
 }  // namespace tn
 

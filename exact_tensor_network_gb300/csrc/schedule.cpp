@@ -87,6 +87,7 @@ bool make_ep_table(const NodePlan &nd, EpTable *t) {
 tn_status layout_plan(Plan *p) {
     const int n = p->n_tensors;
     const int S = (int)p->nodes.size();
+    drop_graph(p);
     for (auto &nd : p->nodes) {
         nd.cls = classify(*p, nd);
         choose_split(*p, nd);

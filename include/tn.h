@@ -200,6 +200,11 @@ TN_API tn_status tn_plan_set_workspace(tn_plan_t *plan, void *dev_ptr, uint64_t 
  *                 Overwritten with the sum over all slices.
  * Asynchronous: returns after enqueueing.  Launch-time failures give
  * TN_ECUDA; device-side problems surface through tn_plan_check().
+ * Replay: the first call with a given set of leaf, output and workspace
+ * pointers launches directly and also records the launch sequence into a
+ * CUDA graph (on a stream the plan creates); later calls with the same
+ * pointers replay that graph on `stream`.  Different pointers re-record.
+ * Turn this off with tn_plan_set_replay(plan, 0).
  * Errors: TN_EINVAL (NULL pointers), TN_ENOMEM (no workspace bound).
  */
 TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
@@ -229,6 +234,10 @@ TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void 
  */
 TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
                                    tn_stream_t stream);
+
+/* Enable (1, the default) or disable (0) graph replay in tn_execute; any
+ * recorded graph is released either way. */
+TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);
 
 /* After the stream has been synchronised: read and clear the device status
  * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or

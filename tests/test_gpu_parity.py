@@ -141,6 +141,53 @@ def test_simt_policy_matches_auto():
     assert_close(b, ref, what="simt policy vs oracle")
 
 
+@pytest.mark.parametrize("replay", [True, False])
+def test_graph_replay_with_changing_buffers(replay):
+    """Same buffers replay the recorded graph; new output or leaf buffers
+    re-record; results match the oracle every time (and with replay off)."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    net, tree, _ = configs.random_60()
+    ref = _ref(net, tree)
+    plan = tn.Plan.from_network(net, tree)
+    tn.tn_plan_set_replay(plan.handle, replay)
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    outs = [torch.zeros(plan.out_shape, dtype=torch.complex64, device=dev) for _ in range(2)]
+    for it in range(6):
+        o = outs[it // 3]
+        o.fill_(complex(9.0, 9.0))
+        if it == 4:
+            leaves = [x.clone() for x in leaves]       # new leaf buffers
+        plan.execute(leaves, o)
+        torch.cuda.synchronize()
+        assert_close(o.cpu().numpy().astype(np.complex128), ref, what=f"call {it}")
+    plan.check()
+
+
+def test_execute_inside_callers_graph_capture():
+    """A caller capturing its stream records our launches in its graph."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    net, tree, _ = configs.random_60()
+    ref = _ref(net, tree)
+    plan = tn.Plan.from_network(net, tree)
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    out = torch.zeros(plan.out_shape, dtype=torch.complex64, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.execute(leaves, out, s)          # binds the workspace outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.execute(leaves, out, s)
+    out.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy().astype(np.complex128), ref, what="caller graph replay")
+
+
 @pytest.mark.parametrize("name", ["circuit_3x3_d4", "random_60"])
 def test_tiny_batching_matches_unbatched(name):
     """Tiny nodes batched per schedule stage (auto) and launched one by one
