@@ -85,6 +85,8 @@ SIGNATURES = {
     "tn_execute": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_execute_static": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_set_replay": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_execute_slices": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P, ctypes.c_uint64,
+                                         ctypes.c_uint64]),
     "tn_plan_check": (ctypes.c_int, [_P]),
     "tn_plan_launches": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_profiling": (ctypes.c_int, [_P, ctypes.c_int32]),
@@ -216,6 +218,22 @@ def tn_execute_static(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream:
     _check(lib().tn_execute_static(plan, arr, out_ptr, stream), plan)
 
 
+def tn_execute_slices(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream: int,
+                      first: int, step: int) -> None:
+    arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
+    _check(lib().tn_execute_slices(plan, arr, out_ptr, stream, first, step), plan)
+
+
+def shard_slices(n_slices: int, rank: int, world: int) -> Tuple[int, int, int]:
+    """Slices of rank `rank` among `world` processes: (first, step, count)
+    with slices first, first + step, ... below n_slices (round robin).  The
+    ranks' outputs add up to the full result."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    count = 0 if rank >= n_slices else (n_slices - 1 - rank) // world + 1
+    return rank, world, count
+
+
 def tn_plan_set_replay(plan: int, enable: bool) -> None:
     _check(lib().tn_plan_set_replay(plan, 1 if enable else 0), plan)
 
@@ -320,6 +338,19 @@ class Plan:
             stream = torch.cuda.current_stream(out.device)
         sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         tn_execute(self.handle, [t.data_ptr() for t in leaves], out.data_ptr(), sp)
+
+    def execute_slices(self, leaves, out, first: int, step: int, stream=None) -> None:
+        """Sum of slices first, first + step, ... into ``out`` (see
+        tn_execute_slices); with shard_slices this splits a sliced
+        contraction over processes."""
+        import torch
+        if self._ws is None:
+            self.bind_workspace(out.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(out.device)
+        sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        tn_execute_slices(self.handle, [t.data_ptr() for t in leaves], out.data_ptr(), sp,
+                          first, step)
 
     def execute_host(self, host_leaves, host_out, dev_leaves, dev_out, stream=None) -> None:
         """End-to-end call with host buffers: copy the (pinned) host leaves

@@ -14,6 +14,8 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cud
 tn_status check_plan(Plan *p);
 tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                            cudaStream_t stream);
+tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
+                        uint64_t first, uint64_t step);
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len);
 }  // namespace tn
 
@@ -157,6 +159,27 @@ tn_status tn_plan_check(tn_plan_t *plan) {
     if (!plan) return TN_EINVAL;
     if (!plan->p.ws) return TN_OK;
     return tn::check_plan(&plan->p);
+}
+
+tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                            tn_stream_t stream, uint64_t first, uint64_t step) {
+    if (!plan) return TN_EINVAL;
+    tn::Plan &p = plan->p;
+    if (!leaf_ptrs || !out_ptr || step < 1) {
+        p.last_error = "leaf_ptrs and out_ptr are required and step must be >= 1";
+        return TN_EINVAL;
+    }
+    for (int t = 0; t < p.n_tensors; ++t)
+        if (!leaf_ptrs[t]) {
+            p.last_error = "leaf pointer " + std::to_string(t) + " is NULL";
+            return TN_EINVAL;
+        }
+    if (!p.ws) {
+        p.last_error = "no workspace bound (tn_plan_set_workspace)";
+        return TN_ENOMEM;
+    }
+    return tn::execute_range(&p, leaf_ptrs, out_ptr, reinterpret_cast<cudaStream_t>(stream), first,
+                             step);
 }
 
 tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable) {

@@ -218,8 +218,14 @@ tn_status upload_tables(Plan *p) {
     return build_dense_maps(p);
 }
 
-tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
-                       cudaStream_t stream) {
+// Slices first, first + step, ... of the plan; the first of them writes the
+// output and the others add into it; an empty range zeroes the output.
+tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
+                        uint64_t first, uint64_t step) {
+    if (first >= p->n_slices) {
+        cudaError_t e = cudaMemsetAsync(out_ptr, 0, p->out_elems * sizeof(float2), stream);
+        return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "zeroing the output");
+    }
     char *ws = static_cast<char *>(p->ws);
     char *arena = ws + p->arena_off;
     DevStatus *status = reinterpret_cast<DevStatus *>(ws);
@@ -246,7 +252,8 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     Recorder rec{p, stream};
     p->records.clear();
 
-    for (uint64_t sigma = 0; sigma < p->n_slices && st == TN_OK; ++sigma) {
+    for (uint64_t sigma = first; sigma < p->n_slices && st == TN_OK; sigma += step) {
+        const bool later = sigma != first;   // add into the output
         // slice digits, first slice mode most significant
         uint64_t rem = sigma;
         for (int i = nsl - 1; i >= 0; --i) {
@@ -295,7 +302,7 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                 tl.count = L.count;
                 tl.arena = arena;
                 tl.out = out;
-                tl.accumulate_root = sigma > 0 ? 1 : 0;
+                tl.accumulate_root = later ? 1 : 0;
                 rec.begin(TN_KERNEL_TINY, -1, L.flops, L.bytes);
                 cudaError_t e = launch_tiny_batch(tl, L.ctas, stream);
                 rec.end();
@@ -313,7 +320,7 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                     default: return out;
                 }
             };
-            const int32_t accumulate = (nd.is_root && sigma > 0) ? 1 : 0;
+            const int32_t accumulate = (nd.is_root && later) ? 1 : 0;
             const uint64_t flops = 8 * nd.m * nd.n * nd.k;
             cudaError_t e;
             if (nd.cls == TN_NODE_DENSE) {
@@ -416,6 +423,11 @@ tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     }
     delete pl;
     return st;
+}
+
+// All slices.
+tn_status execute_plan(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream) {
+    return execute_range(p, leaf_ptrs, out_ptr, stream, 0, 1);
 }
 
 // tn_execute: the first call with a given (leaves, output, workspace) runs

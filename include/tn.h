@@ -235,6 +235,18 @@ TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void 
 TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
                                    tn_stream_t stream);
 
+/*
+ * tn_execute restricted to the slices first, first + step, first + 2 step,
+ * ... below tn_plan_num_slices: out_ptr receives their sum (zero when the
+ * range is empty).  Slices are independent sub-contractions whose results
+ * add up (section 1.1 slicing), so R processes that take first = r,
+ * step = R and add their outputs obtain the full result; that sum is the
+ * only exchange between them.  step >= 1, first >= 0.  Launches directly
+ * (no graph replay); otherwise as tn_execute.
+ */
+TN_API tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                                   tn_stream_t stream, uint64_t first, uint64_t step);
+
 /* Enable (1, the default) or disable (0) graph replay in tn_execute; any
  * recorded graph is released either way. */
 TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);

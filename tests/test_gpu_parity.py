@@ -92,6 +92,32 @@ def test_sliced_circuit_scalar():
     assert_close(got, _ref(net, tree), what="sliced 4x4 circuit")
 
 
+def test_slice_shards_add_up():
+    """tn_execute_slices: round-robin shards of the slices sum to the full
+    result (the multi-GPU partition); an empty shard yields zeros."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    net = random_network(40, 2)
+    tree = greedy_tree(net, 0)
+    sl = choose_slices(net, tree, largest_intermediate(net, tree) // 8)[:3]
+    plan = tn.Plan.from_network(net, tree, sl)
+    ns = plan.num_slices
+    assert ns >= 4
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    total = torch.zeros(plan.out_shape, dtype=torch.complex128, device=dev)
+    for r in range(3):
+        first, step, count = tn.shard_slices(ns, r, 3)
+        o = torch.full(plan.out_shape, complex(5.0, 1.0), dtype=torch.complex64, device=dev)
+        plan.execute_slices(leaves, o, first, step)
+        total += o.to(torch.complex128)
+    empty = torch.full(plan.out_shape, complex(5.0, 1.0), dtype=torch.complex64, device=dev)
+    plan.execute_slices(leaves, empty, ns, 1)
+    torch.cuda.synchronize()
+    assert float(empty.abs().max()) == 0.0
+    assert_close(total.cpu().numpy(), _ref(net, tree), what="sum of 3 slice shards")
+
+
 def test_repeated_execute_overwrites():
     net, tree, _ = configs.circuit_3x3_d4()
     got, _ = run_gpu(net, tree, repeat=3)
