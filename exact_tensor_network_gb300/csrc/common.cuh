@@ -46,9 +46,26 @@ __device__ __forceinline__ float to_tf32(float x) {
 // Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
 // plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
 // destination.  Kernels instantiated per format keep one store path.
+// Physical index of row-major index `off` in a K-tiled planar operand (see
+// PlanarTile in plan.h).
+__device__ __forceinline__ int64_t tiled_offset(const PlanarTile &t, int64_t off) {
+    if (t.kt == 0) return off;
+    int64_t r, c;
+    if (t.kshift >= 0) {
+        r = off >> t.kshift;
+        c = off & (t.k - 1);
+    } else {
+        r = off / t.k;
+        c = off - r * t.k;
+    }
+    const int sh = t.kt == 32 ? 5 : 4;
+    return (((c >> sh) * t.rows + r) << sh) + (c & (t.kt - 1));
+}
+
 template <int FMT>
 __device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t off, float2 v,
-                                              int32_t accumulate) {
+                                              int32_t accumulate, const PlanarTile &tile) {
+    if constexpr (FMT != FMT_C64) off = tiled_offset(tile, off);
     if constexpr (FMT == FMT_C64) {
         float2 *p = static_cast<float2 *>(dst) + off;
         if (accumulate) {
@@ -73,7 +90,8 @@ __device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t 
 
 // Same with the format chosen at run time.
 __device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plane, int64_t off,
-                                            float2 v, int32_t accumulate) {
+                                            float2 v, int32_t accumulate, const PlanarTile &tile) {
+    if (fmt != FMT_C64) off = tiled_offset(tile, off);
     if (fmt == FMT_C64) {
         float2 *p = static_cast<float2 *>(dst) + off;
         if (accumulate) {

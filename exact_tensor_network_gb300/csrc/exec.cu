@@ -190,8 +190,8 @@ tn_status build_dense_maps(Plan *p) {
         std::memset(&dm, 0, sizeof(dm));
         dm.node = (int32_t)s;
         std::string err;
-        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, bf16, &err) ||
-            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, bf16, &err)) {
+        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, bf16, nd.ktiled != 0, &err) ||
+            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, bf16, nd.ktiled != 0, &err)) {
             p->last_error = "step " + std::to_string(s) + ": " + err;
             return TN_ECUDA;
         }
@@ -338,6 +338,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 d->ln = nd.ln;
                 d->accumulate = accumulate;
                 d->out_fmt = nd.out_fmt;
+                d->out_tile = nd.out_tile;
+                d->ktiled = nd.ktiled;
                 d->bf16 = p->precision == TN_PREC_BF16;
                 d->status = status;
                 d->ksplit = nd.ksplit;
@@ -367,6 +369,7 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 a.ln = nd.swap ? nd.lm : nd.ln;
                 a.accumulate = accumulate;
                 a.out_fmt = nd.out_fmt;
+                a.out_tile = nd.out_tile;
                 int lanes;
                 int64_t rpc;
                 stream_shape((uint64_t)a.m, nd.k, &lanes, &rpc);
@@ -388,6 +391,7 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 a.ln = nd.ln;
                 a.accumulate = accumulate;
                 a.out_fmt = nd.out_fmt;
+                a.out_tile = nd.out_tile;
                 a.status = status;
                 a.ksplit = nd.ksplit;
                 a.kchunk = nd.kchunk;
@@ -409,6 +413,7 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 r.ln = sw ? nd.lm : nd.ln;
                 r.accumulate = accumulate;
                 r.out_fmt = nd.out_fmt;
+                r.out_tile = nd.out_tile;
                 // bytes: every partial read once, the output written once
                 rec.begin(TN_KERNEL_REDUCE, nd.step, 0,
                           8 * (uint64_t)nd.ksplit * nd.m * nd.n + fmt_bytes(nd.out_fmt) * nd.m * nd.n);

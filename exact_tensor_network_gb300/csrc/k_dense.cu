@@ -147,6 +147,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// K-tiled operands: one box = one contiguous [128 rows][64 bytes] block.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
 // 64 bytes, 8-row core groups 512 bytes apart.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
@@ -284,15 +294,22 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     mbar_expect_tx(bar, C::STAGE_BYTES);
                     const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
                     const int32_t kx = kb * C::KB;
-#pragma unroll
-                    for (int p = 0; p < C::A_PLANES; ++p)
-                        tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
                     // B planes in the same order land as the stacks [re; im]
                     // of each split part (hi stack, then lo stack)
                     const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
+                    if (a.ktiled) {
 #pragma unroll
-                    for (int p = 0; p < C::A_PLANES; ++p)
-                        tma_load_3d(bbase + p * PLANE_TILE, &a.tmB, bar, kx, yn, p);
+                        for (int p = 0; p < C::A_PLANES; ++p) {
+                            tma_load_4d(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
+                            tma_load_4d(bbase + p * PLANE_TILE, &a.tmB, bar, 0, yn, kb, p);
+                        }
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < C::A_PLANES; ++p) {
+                            tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
+                            tma_load_3d(bbase + p * PLANE_TILE, &a.tmB, bar, kx, yn, p);
+                        }
+                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -403,6 +420,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 dstw[x] = src[x];
             asm volatile("bar.sync 1, %0;" ::"n"(DRAIN_WARPS * 32) : "memory");
         }
+        // pretiled tables hold tiled offsets: tile the block base only
+        const bool pretiled = ep_s && ep_s->pretiled;
+        const PlanarTile ep_tile = pretiled ? PlanarTile{0, 0, -1, 0} : a.out_tile;
         uint32_t tphase = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
@@ -461,7 +481,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         stage_tile[lane * 16 + (x ^ (lane & 15))] =
                             make_float2(sr[cc * 16 + x], si[cc * 16 + x]);
                     __syncwarp();
-                    const int64_t base = bm + sep_offset(a.ln, j0);
+                    int64_t base = bm + sep_offset(a.ln, j0);
+                    if (pretiled) base = tiled_offset(a.out_tile, base);
 #pragma unroll 4
                     for (int it = 0; it < 16; ++it) {
                         const int e = ep_s->perm[it * 32 + lane];
@@ -469,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
                         if (i0 + r < a.m && j0 + c < a.n)
                             store_entry(dst, fmt, plane, base + ep_s->lo_m[r] + ep_s->lo_n[c], v,
-                                        accum);
+                                        accum, ep_tile);
                     }
                     __syncwarp();
                 }
@@ -487,7 +508,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                             const int64_t offn =
                                 fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
                             store_entry(dst, fmt, plane, offm + offn,
-                                        make_float2(sr[cc * 16 + c], si[cc * 16 + c]), accum);
+                                        make_float2(sr[cc * 16 + c], si[cc * 16 + c]), accum,
+                                        a.out_tile);
                         }
                     }
                 }
@@ -518,7 +540,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         const int r = 2 * it + (lane >> 4);
                         const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
                         const int64_t om = __shfl_sync(0xffffffffu, offm, r);
-                        if (i0 + r < a.m && j < a.n) store_entry(dst, fmt, plane, om + offn, v, accum);
+                        if (i0 + r < a.m && j < a.n)
+                            store_entry(dst, fmt, plane, om + offn, v, accum, a.out_tile);
                     }
                     __syncwarp();
                 }
@@ -570,7 +593,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
 }
 
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
-                        std::string *err) {
+                        bool tiled, std::string *err) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
         void *fn = nullptr;
@@ -584,6 +607,25 @@ bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     const cuuint64_t esz = bf16 ? 2 : 4;
+    if (tiled) {
+        // planes of [k / kt][rows][kt]: dims (kt, rows, k / kt, planes)
+        const cuuint64_t kt = ROW_BYTES / esz;
+        const cuuint64_t d4[4] = {kt, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k) / kt,
+                                  static_cast<cuuint64_t>(bf16 ? 2 : 4)};
+        const cuuint64_t s4[3] = {kt * esz, static_cast<cuuint64_t>(rows) * kt * esz,
+                                  static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
+        const cuuint32_t b4[4] = {static_cast<cuuint32_t>(kt), BM, 1, 1};
+        const cuuint32_t e4[4] = {1, 1, 1, 1};
+        CUresult r4 = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                             4, const_cast<void *>(base), d4, s4, b4, e4,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r4 != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled (4-D) failed with " + std::to_string(static_cast<int>(r4));
+            return false;
+        }
+        return true;
+    }
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(bf16 ? 2 : 4)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * esz,

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
                     rem = q;
                 }
             }
-            store_entry(dst, fmt, size, e, src[so], a.accumulate);
+            store_entry(dst, fmt, size, e, src[so], a.accumulate, d.tile);
         }
     }
 }

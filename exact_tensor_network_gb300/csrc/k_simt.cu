@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             for (int c = 0; c < TN; ++c) {
                 const int64_t j = j0 + tx + c * (BN / TN);
                 if (j >= a.n) continue;
-                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate);
+                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate,
+                                   a.out_tile);
             }
         }
     }

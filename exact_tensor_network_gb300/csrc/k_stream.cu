@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
                 for (int j = 0; j < kStreamMaxN; ++j)
                     if (j < n)
                         store_entry_t<FMT>(a.C, a.m * a.n, offm + sep_offset(a.ln, j), acc[j],
-                                    a.accumulate);
+                                           a.accumulate, a.out_tile);
             }
         }
     }
@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_co
             v.y += p.y;
         }
         const int64_t i = e / a.n, j = e - i * a.n;
-        store_entry(a.C, a.out_fmt, mn, sep_offset(a.lm, i) + sep_offset(a.ln, j), v, a.accumulate);
+        store_entry(a.C, a.out_fmt, mn, sep_offset(a.lm, i) + sep_offset(a.ln, j), v, a.accumulate,
+                    a.out_tile);
     }
 }
 

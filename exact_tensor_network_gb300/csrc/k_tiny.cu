@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
             acc.y += __shfl_down_sync(0xffffffffu, acc.y, off, lanes);
         }
         if (l == 0 && o < o1) {
-            store_entry(C, d.out_fmt, mn, sep_offset(d.lm, i) + sep_offset(d.ln, j), acc, accumulate);
+            store_entry(C, d.out_fmt, mn, sep_offset(d.lm, i) + sep_offset(d.ln, j), acc, accumulate,
+                        d.out_tile);
         }
     }
 }

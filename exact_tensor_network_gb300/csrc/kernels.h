@@ -27,6 +27,7 @@ struct NodeArgs {
     SepLayout lm, ln;
     int32_t accumulate;   // 1: add into C (later slices of the root)
     int32_t out_fmt;      // Fmt of C; planes are m*n entries apart
+    PlanarTile out_tile;  // K-tiling of a planar C
     DevStatus *status;
     // split-K: with ksplit > 1, split s sums k in [s*kchunk, (s+1)*kchunk)
     // and writes plain partials part[(s*m + i)*n + j]; splitk_reduce stores C
@@ -52,6 +53,7 @@ struct StreamArgs {
     SepLayout lm, ln;
     int32_t accumulate;
     int32_t out_fmt;
+    PlanarTile out_tile;
 };
 
 // Ordered sum of split-K partials into the node's output.
@@ -63,6 +65,7 @@ struct ReduceArgs {
     SepLayout lm, ln;
     int32_t accumulate;
     int32_t out_fmt;
+    PlanarTile out_tile;
 };
 
 // One batched launch of tiny nodes: descriptors [first, first + count) of
@@ -89,7 +92,9 @@ struct DenseArgs {
     SepLayout lm, ln;
     int32_t accumulate;
     int32_t out_fmt;
+    PlanarTile out_tile;
     int32_t bf16;         // operands are FMT_BF2 (else FMT_SPLIT4)
+    int32_t ktiled;       // operands K-tiled (4-D maps) rather than row-major (3-D)
     DevStatus *status;
     // split-K as in NodeArgs (kchunk a multiple of 256)
     int32_t ksplit;
@@ -104,7 +109,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
 // Returns false (with a message) when the driver call is unavailable or
 // rejects the shape.
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
-                        std::string *err);
+                        bool tiled, std::string *err);
 
 constexpr int kPermBatch = 512;   // permutation jobs per launch
 

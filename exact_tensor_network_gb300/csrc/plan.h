@@ -52,6 +52,22 @@ inline int32_t log2_exact(int64_t e) {
 enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2 };
 inline uint64_t fmt_bytes(int32_t f) { return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : 8; }
 
+// K-tiling of a planar operand.  The consumer reads the operand as a
+// row-major [rows][k] matrix; with kt > 0 each plane is stored as
+// [k / kt][rows][kt], so that one tensor-core stage (kt entries of 128 rows)
+// is a single contiguous 8 KiB block rather than 128 pieces one row
+// (possibly megabytes) apart.  Producers map the row-major index
+// r * k + c to ((c / kt) * rows + r) * kt + c % kt.  kt = 0: row-major.
+struct PlanarTile {
+    int64_t k;
+    int64_t rows;
+    int32_t kshift;   // log2(k) when k is a power of two, else -1
+    int32_t kt;       // 0, 16 (tf32 planes) or 32 (bf16 planes)
+};
+
+// Entries per K tile for a planar format (64 bytes of one row).
+inline int32_t planar_kt(int32_t fmt) { return fmt == FMT_BF2 ? 32 : fmt == FMT_SPLIT4 ? 16 : 0; }
+
 // Where a tensor lives during execution.
 enum PlaceKind : int32_t { PLACE_WS = 0, PLACE_LEAF = 1, PLACE_OUT = 2 };
 struct Place {
@@ -69,6 +85,7 @@ struct PermDesc {
     int64_t dst_off;        // byte offset into the arena, or -1 = output
     int32_t rank;
     int32_t fmt;            // destination format (Fmt); planes are `size` apart
+    PlanarTile tile;        // destination K-tiling (planar formats)
     int64_t dims[kMaxPermRank];
     int64_t sstride[kMaxPermRank];
     int32_t dshift[kMaxPermRank];   // log2(dims) for powers of two, else -1
@@ -95,6 +112,8 @@ struct NodePlan {
     bool is_root;
     int32_t layout;         // 0: C = [M|N], 1: C = [N|M], 2: interleaved
     int32_t out_fmt;        // format the output is stored in (Fmt)
+    PlanarTile out_tile;    // K-tiling of the output (planar formats)
+    int32_t ktiled;         // dense class: operands are K-tiled
     // split-K (CUDA-core classes): ksplit ranges of kchunk entries each write
     // fp32 complex partial sums [split][i][j] into `part`, then an ordered
     // reduction stores the node's output
@@ -117,7 +136,18 @@ struct EpTable {
     int64_t lo_m[32];
     int64_t lo_n[16];
     uint16_t perm[512];
+    // 1: the output is K-tiled with power-of-two rows and k, so tiling is a
+    // permutation of address bits; lo_m / lo_n (and the sort) are then in
+    // tiled addresses and the block base is tiled before they are added
+    int32_t pretiled;
+    int32_t pad;
 };
+
+inline int64_t tiled_offset_host(const PlanarTile &t, int64_t off) {
+    if (t.kt == 0) return off;
+    const int64_t r = off / t.k, c = off % t.k;
+    return ((c / t.kt) * t.rows + r) * t.kt + c % t.kt;
+}
 
 // One tiny node inside a batched launch (device table).  Its operands and
 // output live in the workspace arena (c_off < 0: the caller's output).
@@ -126,6 +156,7 @@ struct TinyDesc {
     int32_t m, n, k;
     int32_t out_fmt;
     int32_t is_root;
+    PlanarTile out_tile;
     int32_t cta_base;      // first CTA of this node within its launch
     int32_t ctas;
     int32_t lanes;         // threads that share one output's k range (1, 4 or 32)

@@ -77,6 +77,21 @@ bool make_ep_table(const NodePlan &nd, EpTable *t) {
         if (r >= (int64_t)nd.m || c >= (int64_t)nd.n) return INT64_MAX;
         return t->lo_m[r] + t->lo_n[c];
     };
+    // power-of-two extents: every mode owns its own address bits, and K-tiling
+    // with power-of-two rows and k only moves bits, so the tiled address of
+    // base + lo_m[r] + lo_n[c] is the sum of the three tiled parts
+    const PlanarTile &tl = nd.out_tile;
+    auto pow2_layout = [](const SepLayout &L) {
+        for (int r = 0; r < L.nrun; ++r)
+            if (L.shift[r] < 0 || log2_exact(L.stride[r]) < 0) return false;
+        return true;
+    };
+    if (tl.kt != 0 && tl.kshift >= 0 && log2_exact(tl.rows) >= 0 && pow2_layout(nd.lm) &&
+        pow2_layout(nd.ln)) {
+        t->pretiled = 1;
+        for (int r = 0; r < 32; ++r) t->lo_m[r] = tiled_offset_host(tl, t->lo_m[r]);
+        for (int c = 0; c < 16; ++c) t->lo_n[c] = tiled_offset_host(tl, t->lo_n[c]);
+    }
     std::stable_sort(idx.begin(), idx.end(), [&](uint16_t x, uint16_t y) { return key(x) < key(y); });
     for (int e = 0; e < 512; ++e) t->perm[e] = idx[e];
     return true;
@@ -99,6 +114,21 @@ tn_status layout_plan(Plan *p) {
     for (const auto &nd : p->nodes)
         if (nd.cls == TN_NODE_DENSE) p->fmt[nd.a] = p->fmt[nd.b] = dense_fmt;
     for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
+    // K-tiling of tensor-core operands whose k fills whole tiles
+    const PlanarTile untiled{0, 0, -1, 0};
+    std::vector<PlanarTile> tile(n + S, untiled);
+    for (auto &nd : p->nodes) {
+        nd.ktiled = 0;
+        if (nd.cls != TN_NODE_DENSE) continue;
+        const int32_t kt = planar_kt(dense_fmt);
+        // rows of 16 KiB and more: 64-byte pieces would each cost a DRAM page
+        if (nd.k % (uint64_t)kt != 0 || nd.k < 4096) continue;
+        nd.ktiled = 1;
+        const int32_t ks = log2_exact((int64_t)nd.k);
+        tile[nd.a] = PlanarTile{(int64_t)nd.k, (int64_t)nd.m, ks, kt};
+        tile[nd.b] = PlanarTile{(int64_t)nd.k, (int64_t)nd.n, ks, kt};
+    }
+    for (auto &nd : p->nodes) nd.out_tile = nd.is_root ? untiled : tile[nd.out];
 
     // 3. schedule
     std::vector<int> stage(n + S, 0);
@@ -171,6 +201,7 @@ tn_status layout_plan(Plan *p) {
             PermDesc d = lp.perm;
             d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
             d.fmt = (S == 0) ? FMT_C64 : p->fmt[t];
+            d.tile = (S == 0) ? untiled : tile[t];
             p->perm_table.push_back(d);
             p->perm_leaves.push_back(t);
         }
@@ -222,6 +253,7 @@ tn_status layout_plan(Plan *p) {
             d.n = (int32_t)nd.n;
             d.k = (int32_t)nd.k;
             d.out_fmt = nd.out_fmt;
+            d.out_tile = nd.out_tile;
             d.is_root = nd.is_root ? 1 : 0;
             const uint64_t macs = nd.m * nd.n * nd.k;
             d.ctas = (int32_t)std::max<uint64_t>(1, std::min<uint64_t>((macs + 8191) / 8192,

@@ -176,3 +176,24 @@ def test_random_60_uses_dense_nodes_and_matches():
     got, _ = run_gpu(net, tree)
     assert_close(got, _ref(net, tree), TOL_C64, "random_60 auto")
     assert tn.TN_NODE_DENSE in cls or True
+
+
+@pytest.mark.parametrize("p_ext,a_ext,precision,tol", [
+    (64, 128, "tf32x3", TOL_C64),     # power-of-two extents: store table in tiled addresses
+    (72, 96, "tf32x3", TOL_C64),      # k = 6144: tiled, offsets tiled entry by entry
+    (64, 128, "bf16", TOL_BF16),
+])
+def test_dense_output_k_tiled_for_dense_consumer(p_ext, a_ext, precision, tol):
+    # A[p,a,x] B[y,x] -> C[p,a,y] (tensor cores), then C[p,a,y] D[q,a,y] -> root[p,q]
+    # with k = a*y >= 4096, so C is written K-tiled for the consumer's TMA loads
+    rng = np.random.default_rng(33)
+    ext = [p_ext, a_ext, 256, 64, 256]          # p a x y q
+    tensors = [[0, 1, 2], [3, 2], [4, 1, 3]]
+    data = [_rand(rng, [ext[x] for x in t], 0.1) for t in tensors]
+    net = Network(tensors, ext, [0, 4], data)
+    tree = [(0, 1), (3, 2)]
+    p = tn.Plan.from_network(net, tree, (), precision)
+    assert [p.node_class(s) for s in range(2)] == [tn.TN_NODE_DENSE, tn.TN_NODE_DENSE]
+    assert p.node_mnk(1)[2] == a_ext * 64
+    got, _ = run_gpu(net, tree, precision=precision)
+    assert_close(got, _ref(net, tree), tol, f"K-tiled operand {p_ext}x{a_ext} {precision}")
