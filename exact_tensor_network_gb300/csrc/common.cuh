@@ -16,6 +16,9 @@ namespace tn {
 // when the index fits, which avoids the slow 64-bit division).
 __device__ __forceinline__ int64_t sep_offset(const SepLayout &L, int64_t i) {
     int64_t off = 0;
+    // rolled: inlined at many call sites, an unrolled copy per site would
+    // swell the kernels' code (and their instruction-cache misses)
+#pragma unroll 1
     for (int r = L.nrun - 1; r >= 0; --r) {
         const int64_t e = L.ext[r];
         int64_t d;
@@ -43,9 +46,6 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(r);
 }
 
-// Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
-// plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
-// destination.  Kernels instantiated per format keep one store path.
 // Physical index of row-major index `off` in a K-tiled planar operand (see
 // PlanarTile in plan.h).
 __device__ __forceinline__ int64_t tiled_offset(const PlanarTile &t, int64_t off) {
@@ -62,6 +62,9 @@ __device__ __forceinline__ int64_t tiled_offset(const PlanarTile &t, int64_t off
     return (((c >> sh) * t.rows + r) << sh) + (c & (t.kt - 1));
 }
 
+// Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
+// plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
+// destination.  Kernels instantiated per format keep one store path.
 template <int FMT>
 __device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t off, float2 v,
                                               int32_t accumulate, const PlanarTile &tile) {
@@ -111,6 +114,55 @@ __device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plan
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         p[0] = __float2bfloat16_rn(v.x);
         p[plane] = __float2bfloat16_rn(v.y);
+    }
+}
+
+// Four entries at offsets off .. off + 3 (off a multiple of 4, planes a
+// multiple of 4 entries apart, dst 16-byte aligned): the conversions of
+// store_entry, then one 16-byte store per plane (8 bytes per bf16 plane).
+// K-tiling keeps such a run contiguous because tiles hold 16 or 32 entries.
+__device__ __forceinline__ void store_quad(void *dst, int32_t fmt, int64_t plane, int64_t off,
+                                           const float2 (&v)[4], int32_t accumulate,
+                                           const PlanarTile &tile) {
+    if (fmt != FMT_C64) off = tiled_offset(tile, off);
+    if (fmt == FMT_C64) {
+        float4 *p = reinterpret_cast<float4 *>(static_cast<float2 *>(dst) + off);
+        float4 x0 = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+        float4 x1 = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+        if (accumulate) {
+            const float4 o0 = p[0], o1 = p[1];
+            x0.x += o0.x; x0.y += o0.y; x0.z += o0.z; x0.w += o0.w;
+            x1.x += o1.x; x1.y += o1.y; x1.z += o1.z; x1.w += o1.w;
+        }
+        p[0] = x0;
+        p[1] = x1;
+    } else if (fmt == FMT_SPLIT4) {
+        float *p = static_cast<float *>(dst) + off;
+        float rh[4], ih[4], rl[4], il[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            rh[t] = to_tf32(v[t].x);
+            ih[t] = to_tf32(v[t].y);
+            rl[t] = to_tf32(v[t].x - rh[t]);
+            il[t] = to_tf32(v[t].y - ih[t]);
+        }
+        *reinterpret_cast<float4 *>(p) = make_float4(rh[0], rh[1], rh[2], rh[3]);
+        *reinterpret_cast<float4 *>(p + plane) = make_float4(ih[0], ih[1], ih[2], ih[3]);
+        *reinterpret_cast<float4 *>(p + 2 * plane) = make_float4(rl[0], rl[1], rl[2], rl[3]);
+        *reinterpret_cast<float4 *>(p + 3 * plane) = make_float4(il[0], il[1], il[2], il[3]);
+    } else {
+        __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
+        __nv_bfloat162 re0 = __halves2bfloat162(__float2bfloat16_rn(v[0].x), __float2bfloat16_rn(v[1].x));
+        __nv_bfloat162 re1 = __halves2bfloat162(__float2bfloat16_rn(v[2].x), __float2bfloat16_rn(v[3].x));
+        __nv_bfloat162 im0 = __halves2bfloat162(__float2bfloat16_rn(v[0].y), __float2bfloat16_rn(v[1].y));
+        __nv_bfloat162 im1 = __halves2bfloat162(__float2bfloat16_rn(v[2].y), __float2bfloat16_rn(v[3].y));
+        uint2 re, im;
+        re.x = *reinterpret_cast<uint32_t *>(&re0);
+        re.y = *reinterpret_cast<uint32_t *>(&re1);
+        im.x = *reinterpret_cast<uint32_t *>(&im0);
+        im.y = *reinterpret_cast<uint32_t *>(&im1);
+        *reinterpret_cast<uint2 *>(p) = re;
+        *reinterpret_cast<uint2 *>(p + plane) = im;
     }
 }
 

@@ -210,6 +210,22 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Staging-tile slot of entry e = r * 16 + c of a 32 x 16 block: row r,
+// column c xor-swizzled by the row (conflict-light for row and column walks).
+__device__ __forceinline__ int swz(int e) { return (e & ~15) | ((e ^ (e >> 4)) & 15); }
+
+// This lane's 16 values of column block cc (a run-time index: the selects
+// keep sr / si in registers) into the lane's row of the staging tile.
+__device__ __forceinline__ void stage_block(float2 *tile, int lane, const float (&sr)[64],
+                                            const float (&si)[64], int cc) {
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+        const float vr = cc == 0 ? sr[x] : cc == 1 ? sr[16 + x] : cc == 2 ? sr[32 + x] : sr[48 + x];
+        const float vi = cc == 0 ? si[x] : cc == 1 ? si[16 + x] : cc == 2 ? si[32 + x] : si[48 + x];
+        tile[swz(lane * 16 + x)] = make_float2(vr, vi);
+    }
+}
+
 // Output tile of linear tile index t: groups of 8 row tiles, columns inside.
 __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t ntiles, int64_t &mt,
                                             int64_t &nt) {
@@ -422,6 +438,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         }
         // pretiled tables hold tiled offsets: tile the block base only
         const bool pretiled = ep_s && ep_s->pretiled;
+        // runs of four need a 16-byte aligned destination (the caller's
+        // output may not be)
+        const bool quads =
+            ep_s && ep_s->vec && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
         const PlanarTile ep_tile = pretiled ? PlanarTile{0, 0, -1, 0} : a.out_tile;
         uint32_t tphase = 0;
         bool ok = true;
@@ -469,62 +489,61 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             const int64_t i0 = mt * BM + q * 32;
             const int64_t i = i0 + lane;
             const int64_t offm = i < a.m ? (plain ? i * a.n : sep_offset(a.lm, i)) : 0;
-            if (ep_s) {
-                // walk each 32 x 16 block in address order
-                const int64_t bm = sep_offset(a.lm, i0);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int64_t j0 = nt * BN + h * 64 + cc * 16;
-                    if (j0 >= a.n) break;   // warp-uniform
-#pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        stage_tile[lane * 16 + (x ^ (lane & 15))] =
-                            make_float2(sr[cc * 16 + x], si[cc * 16 + x]);
-                    __syncwarp();
+            const int64_t bm = ep_s ? sep_offset(a.lm, i0) : 0;
+            // One 32 x 16 block (this warp's rows, 16 columns) per pass.  The
+            // block goes through the staging tile (row = lane, columns
+            // xor-swizzled by row) and every store loop reads it from there,
+            // so the loops stay rolled and the kernel's code stays small.
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int64_t j0 = nt * BN + h * 64 + cc * 16;
+                if (j0 >= a.n) break;   // warp-uniform
+                stage_block(stage_tile, lane, sr, si, cc);
+                __syncwarp();
+                if (ep_s) {
+                    // the block in address order
                     int64_t base = bm + sep_offset(a.ln, j0);
                     if (pretiled) base = tiled_offset(a.out_tile, base);
-#pragma unroll 4
-                    for (int it = 0; it < 16; ++it) {
-                        const int e = ep_s->perm[it * 32 + lane];
-                        const int r = e >> 4, c = e & 15;
-                        const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
-                        if (i0 + r < a.m && j0 + c < a.n)
-                            store_entry(dst, fmt, plane, base + ep_s->lo_m[r] + ep_s->lo_n[c], v,
-                                        accum, ep_tile);
-                    }
-                    __syncwarp();
-                }
-            } else if (rows_adjacent) {
-                if (i < a.m) {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int64_t j0 = nt * BN + h * 64 + cc * 16;
-                        if (j0 >= a.n) break;
-                        const bool fast = (j0 % last_ext) + 16 <= last_ext;
-                        const int64_t offn0 = sep_offset(a.ln, j0);
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            if (j0 + c >= a.n) break;
-                            const int64_t offn =
-                                fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
-                            store_entry(dst, fmt, plane, offm + offn,
-                                        make_float2(sr[cc * 16 + c], si[cc * 16 + c]), accum,
-                                        a.out_tile);
+                    if (quads && i0 + 32 <= a.m && j0 + 16 <= a.n) {   // warp-uniform
+                        // each lane stores a run of four consecutive entries
+                        const uint2 *pk = reinterpret_cast<const uint2 *>(ep_s->perm);
+#pragma unroll 1
+                        for (int it = 0; it < 4; ++it) {
+                            const uint2 w4 = pk[it * 32 + lane];
+                            const int e0 = (int)(w4.x & 0xffffu), e1 = (int)(w4.x >> 16);
+                            const int e2 = (int)(w4.y & 0xffffu), e3 = (int)(w4.y >> 16);
+                            const float2 v[4] = {stage_tile[swz(e0)], stage_tile[swz(e1)],
+                                                 stage_tile[swz(e2)], stage_tile[swz(e3)]};
+                            store_quad(dst, fmt, plane,
+                                       base + ep_s->lo_m[e0 >> 4] + ep_s->lo_n[e0 & 15], v, accum,
+                                       ep_tile);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int it = 0; it < 16; ++it) {
+                            const int e = ep_s->perm[it * 32 + lane];
+                            const int r = e >> 4, c = e & 15;
+                            if (i0 + r < a.m && j0 + c < a.n)
+                                store_entry(dst, fmt, plane, base + ep_s->lo_m[r] + ep_s->lo_n[c],
+                                            stage_tile[swz(e)], accum, ep_tile);
                         }
                     }
-                }
-            } else {
-                const int c = lane & 15;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int64_t j0 = nt * BN + h * 64 + cc * 16;
-                    if (j0 >= a.n) break;   // warp-uniform
-                    // own row's 16 values, columns xor-swizzled by row
-#pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        stage_tile[lane * 16 + (x ^ (lane & 15))] =
-                            make_float2(sr[cc * 16 + x], si[cc * 16 + x]);
-                    __syncwarp();
+                } else if (rows_adjacent) {
+                    // thread per row: consecutive lanes are consecutive entries
+                    if (i < a.m) {
+                        const bool fast = (j0 % last_ext) + 16 <= last_ext;
+                        const int64_t offn0 = sep_offset(a.ln, j0);
+#pragma unroll 1
+                        for (int c = 0; c < 16 && j0 + c < a.n; ++c) {
+                            const int64_t offn =
+                                fast ? offn0 + c * last_stride : sep_offset(a.ln, j0 + c);
+                            store_entry(dst, fmt, plane, offm + offn, stage_tile[swz(lane * 16 + c)],
+                                        accum, a.out_tile);
+                        }
+                    }
+                } else {
+                    // 16 lanes store 16 consecutive columns of two rows
+                    const int c = lane & 15;
                     const int64_t j = j0 + c;
                     int64_t offn = 0;
                     if (j < a.n) {
@@ -535,16 +554,16 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                             offn = fast ? sep_offset(a.ln, j0) + c * last_stride : sep_offset(a.ln, j);
                         }
                     }
-#pragma unroll 4
+#pragma unroll 1
                     for (int it = 0; it < 16; ++it) {
                         const int r = 2 * it + (lane >> 4);
-                        const float2 v = stage_tile[r * 16 + (c ^ (r & 15))];
                         const int64_t om = __shfl_sync(0xffffffffu, offm, r);
                         if (i0 + r < a.m && j < a.n)
-                            store_entry(dst, fmt, plane, om + offn, v, accum, a.out_tile);
+                            store_entry(dst, fmt, plane, om + offn, stage_tile[swz(r * 16 + c)], accum,
+                                        a.out_tile);
                     }
-                    __syncwarp();
                 }
+                __syncwarp();
             }
         }
     }

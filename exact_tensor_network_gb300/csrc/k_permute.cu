@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
             const int64_t e = base + it * kThreads + threadIdx.x;
             if (e >= size) break;
             int64_t rem = e, so = 0;
+#pragma unroll 1
             for (int r = rank - 1; r >= 0; --r) {
                 const int64_t dim = d.dims[r];
                 if (d.dshift[r] >= 0) {

@@ -90,7 +90,9 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             const int64_t j = j0 + tx + c * (BN / TN);
             offn[c] = j < a.n ? sep_offset(a.ln, j) : 0;
         }
-#pragma unroll
+        // rows rolled (the selects keep acc in registers): one copy of the
+        // store code per column instead of one per entry
+#pragma unroll 1
         for (int r = 0; r < TM; ++r) {
             const int64_t i = i0 + ty + r * (BM / TM);
             if (i >= a.m) continue;
@@ -99,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             for (int c = 0; c < TN; ++c) {
                 const int64_t j = j0 + tx + c * (BN / TN);
                 if (j >= a.n) continue;
-                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], acc[r][c], a.accumulate,
-                                   a.out_tile);
+                const float2 v = r == 0 ? acc[0][c] : r == 1 ? acc[1][c] : r == 2 ? acc[2][c] : acc[3][c];
+                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], v, a.accumulate, a.out_tile);
             }
         }
     }

@@ -1,14 +1,15 @@
 // Batched kernel for tiny nodes.
 //
 // Most nodes near the leaves of a tree are tiny (a few hundred to a few
-// hundred thousand complex multiply-adds: single-qubit gates absorbed into
-// wires, small random tensors meeting).  One launch per node would cost
-// several microseconds of launch and memory latency each, far more than
-// their arithmetic.  All tiny nodes of one schedule stage are independent,
-// so one launch runs them all: each node owns a few CTAs (its cta_base
-// range in the descriptor table); each CTA takes a share of the node's
-// outputs; `lanes` threads cooperate on one output's k range and combine
-// with warp shuffles.  Operands are complex64 in the workspace arena; the
+// million complex multiply-adds: single-qubit gates absorbed into wires,
+// small random tensors meeting).  One launch per node would cost several
+// microseconds of launch and memory latency each, far more than their
+// arithmetic.  All tiny nodes of one schedule stage are independent, so one
+// launch runs them all: each node owns CTAs (its cta_base range in the
+// descriptor table), enough that every thread group computes at most two
+// outputs, since each output is a serial chain of memory waits; `lanes`
+// threads cooperate on one output's k range (k <= 512: at most two rounds of
+// loads) and combine with warp shuffles.  Operands are complex64 in the workspace arena; the
 // output goes through the node's separable offsets in its consumer's format
 // (the root adds into the caller's output on later slices).
 #include "common.cuh"
@@ -44,12 +45,26 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
     const int accumulate = d.is_root ? a.accumulate_root : 0;
     const int k = d.k;
     for (int64_t ob = o0; ob < o1; ob += groups) {
+        // outputs in address order: o is the address, (i, j) from the walk;
+        // m n <= 2^23 here, so 32-bit index arithmetic is exact
         const int64_t o = ob + g;
         float2 acc = make_float2(0.f, 0.f);
-        // m n <= 2^18 here, so 32-bit index arithmetic is exact
-        const int o32 = static_cast<int>(o);
-        const int i = o32 / d.n, j = o32 - i * d.n;
         if (o < o1) {
+            int rem = static_cast<int>(o), i = 0, j = 0;
+#pragma unroll 1
+            for (int t = 0; t < d.wn; ++t) {
+                int dg;
+                if (d.wshift[t] >= 0) {
+                    dg = rem & (d.wext[t] - 1);
+                    rem >>= d.wshift[t];
+                } else {
+                    const int q = rem / d.wext[t];
+                    dg = rem - q * d.wext[t];
+                    rem = q;
+                }
+                if ((d.wside >> t) & 1u) j += dg * d.wt[t];
+                else i += dg * d.wt[t];
+            }
             const float2 *ar = A + (int64_t)i * k, *br = B + (int64_t)j * k;
             // eight independent load pairs in flight per round
             for (int kk = l; kk < k; kk += 8 * lanes) {
@@ -68,10 +83,7 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
             acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, lanes);
             acc.y += __shfl_down_sync(0xffffffffu, acc.y, off, lanes);
         }
-        if (l == 0 && o < o1) {
-            store_entry(C, d.out_fmt, mn, sep_offset(d.lm, i) + sep_offset(d.ln, j), acc, accumulate,
-                        d.out_tile);
-        }
+        if (l == 0 && o < o1) store_entry(C, d.out_fmt, mn, o, acc, accumulate, d.out_tile);
     }
 }
 

@@ -140,7 +140,10 @@ struct EpTable {
     // permutation of address bits; lo_m / lo_n (and the sort) are then in
     // tiled addresses and the block base is tiled before they are added
     int32_t pretiled;
-    int32_t pad;
+    // 1: in every full block the sorted entries form runs of four at
+    // consecutive offsets, the first a multiple of 4 (block bases and the
+    // plane size too), so a lane stores four entries at once
+    int32_t vec;
 };
 
 inline int64_t tiled_offset_host(const PlanarTile &t, int64_t off) {
@@ -160,7 +163,15 @@ struct TinyDesc {
     int32_t cta_base;      // first CTA of this node within its launch
     int32_t ctas;
     int32_t lanes;         // threads that share one output's k range (1, 4 or 32)
-    SepLayout lm, ln;
+    // Output walk, so that consecutive threads store consecutive addresses:
+    // address p (< m n <= 2^23) splits mixed-radix over the wn runs of the
+    // output's modes, fastest first; digit d of run t adds d * wt[t] to i
+    // (bit t of wside clear) or to j (bit t set).
+    int32_t wn;
+    uint32_t wside;
+    int32_t wext[2 * kMaxRuns];
+    int32_t wshift[2 * kMaxRuns];   // log2(wext) or -1
+    int32_t wt[2 * kMaxRuns];
 };
 
 // Launch schedule: every node gets a stage one past its operands' stages;
@@ -175,8 +186,11 @@ struct Launch {
     uint64_t flops, bytes; // algorithmic work of the launch (measurement)
 };
 
-// Tiny nodes: at most this many complex multiply-adds (m n k).
-constexpr uint64_t kTinyMacs = 1ull << 18;
+// Tiny nodes: at most this many complex multiply-adds (m n k) and a k short
+// enough for one pass of a thread group over it.  Such a node costs the
+// batched dot-product kernel a few microseconds, less than a launch of its own.
+constexpr uint64_t kTinyMacs = 1ull << 23;
+constexpr uint64_t kTinyMaxK = 512;
 
 inline int64_t sep_offset_host(const SepLayout &L, int64_t i) {
     int64_t off = 0;

@@ -65,6 +65,64 @@ uint64_t place_buffers(std::vector<Interval> &iv) {
 
 uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Whether the sorted order of a full 32 x 16 block splits into runs of four
+// consecutive offsets starting at multiples of 4, with every block base and
+// the plane size multiples of 4 as well.  (K-tiling keeps such runs
+// contiguous: its tiles hold 16 or 32 entries and tiling keeps the low bits.)
+bool quad_stores_ok(const NodePlan &nd, const EpTable &t) {
+    if (nd.m < 32 || nd.n < 16) return false;
+    if (nd.out_fmt != FMT_C64 && (nd.m * nd.n) % 4 != 0) return false;
+    for (int g = 0; g < 128; ++g) {
+        const int e0 = t.perm[4 * g];
+        const int64_t o = t.lo_m[e0 >> 4] + t.lo_n[e0 & 15];
+        if (o % 4 != 0) return false;
+        for (int u = 1; u < 4; ++u) {
+            const int e = t.perm[4 * g + u];
+            if (t.lo_m[e >> 4] + t.lo_n[e & 15] != o + u) return false;
+        }
+    }
+    for (uint64_t i0 = 0; i0 < nd.m; i0 += 32)
+        if (sep_offset_host(nd.lm, (int64_t)i0) % 4 != 0) return false;
+    for (uint64_t j0 = 0; j0 < nd.n; j0 += 16)
+        if (sep_offset_host(nd.ln, (int64_t)j0) % 4 != 0) return false;
+    return true;
+}
+
+// The output walk of a tiny node (see TinyDesc): the runs of M and N,
+// each with its digit's weight in i or j, sorted by their stride in the
+// output.  Those strides nest (1, e0, e0 e1, ...) because the output is a
+// dense row-major tensor over the M and N modes.
+bool make_walk(const NodePlan &nd, TinyDesc *d) {
+    struct Run {
+        int64_t ext, stride, weight;
+        int side;
+    };
+    std::vector<Run> runs;
+    auto add = [&](const SepLayout &L, int side) {
+        int64_t w = 1;
+        for (int r = L.nrun - 1; r >= 0; --r) {
+            if (L.ext[r] > 1) runs.push_back({L.ext[r], L.stride[r], w, side});
+            w *= L.ext[r];
+        }
+    };
+    add(nd.lm, 0);
+    add(nd.ln, 1);
+    std::sort(runs.begin(), runs.end(), [](const Run &x, const Run &y) { return x.stride < y.stride; });
+    if (runs.size() > 2 * (size_t)kMaxRuns) return false;
+    int64_t expect = 1;
+    d->wn = (int32_t)runs.size();
+    d->wside = 0;
+    for (size_t t = 0; t < runs.size(); ++t) {
+        if (runs[t].stride != expect) return false;
+        expect *= runs[t].ext;
+        d->wext[t] = (int32_t)runs[t].ext;
+        d->wshift[t] = log2_exact(runs[t].ext);
+        d->wt[t] = (int32_t)runs[t].weight;
+        if (runs[t].side) d->wside |= 1u << t;
+    }
+    return expect == (int64_t)(nd.m * nd.n);
+}
+
 bool make_ep_table(const NodePlan &nd, EpTable *t) {
     if (!block_invariant(nd.lm, 32) || !block_invariant(nd.ln, 16)) return false;
     std::memset(t, 0, sizeof(*t));
@@ -94,6 +152,7 @@ bool make_ep_table(const NodePlan &nd, EpTable *t) {
     }
     std::stable_sort(idx.begin(), idx.end(), [&](uint16_t x, uint16_t y) { return key(x) < key(y); });
     for (int e = 0; e < 512; ++e) t->perm[e] = idx[e];
+    t->vec = quad_stores_ok(nd, *t) ? 1 : 0;
     return true;
 }
 
@@ -256,12 +315,13 @@ tn_status layout_plan(Plan *p) {
             d.out_tile = nd.out_tile;
             d.is_root = nd.is_root ? 1 : 0;
             const uint64_t macs = nd.m * nd.n * nd.k;
-            d.ctas = (int32_t)std::max<uint64_t>(1, std::min<uint64_t>((macs + 8191) / 8192,
-                                                                       (nd.m * nd.n + 7) / 8));
+            // `lanes` threads per output; enough CTAs that each group of a CTA
+            // computes at most two outputs (the rounds are serial memory waits)
             d.lanes = nd.k >= 64 ? 32 : nd.k >= 8 ? 4 : 1;
+            const uint64_t per_cta = 2 * (256 / (uint64_t)d.lanes);
+            d.ctas = (int32_t)std::max<uint64_t>(1, (nd.m * nd.n + per_cta - 1) / per_cta);
             d.cta_base = ctas;
-            d.lm = nd.lm;
-            d.ln = nd.ln;
+            if (!make_walk(nd, &d)) return TN_ENOTIMPL;   // outputs are dense: not reached
             ctas += d.ctas;
             L.flops += 8 * macs;
             L.bytes += 8 * (nd.m * nd.k + nd.n * nd.k + nd.m * nd.n);

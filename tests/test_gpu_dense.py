@@ -44,8 +44,13 @@ def _ref(net, tree, slices=()):
     return oracle.contract(net.tensors, net.extents, net.open_modes, net.data, tree)
 
 
-def _classes(net, tree, slices=(), precision="tf32x3"):
-    p = tn.Plan.from_network(net, tree, slices, precision)
+# Tests of the tensor-core kernel turn the batched tiny-node class off, so
+# that their small shapes still reach it.
+NT = tn.TN_POLICY_NO_TINY
+
+
+def _classes(net, tree, slices=(), precision="tf32x3", policy=NT):
+    p = tn.Plan.from_network(net, tree, slices, precision, policy)
     return [p.node_class(s) for s in range(len(tree))]
 
 
@@ -55,7 +60,7 @@ def _classes(net, tree, slices=(), precision="tf32x3"):
 def test_gemm_networks(precision, tol, lm, ln, lk):
     net = gemm_network(lm, ln, lk, 11 * lm + 7 * ln + lk)
     assert _classes(net, [(0, 1)], precision=precision) == [tn.TN_NODE_DENSE]
-    got, _ = run_gpu(net, [(0, 1)], precision=precision)
+    got, _ = run_gpu(net, [(0, 1)], precision=precision, policy=NT)
     assert_close(got, _ref(net, [(0, 1)]), tol, f"gemm {lm},{ln},{lk} {precision}")
 
 
@@ -93,7 +98,7 @@ def test_interleaved_output_layout():
     net = Network(tensors, ext, [0, 2, 4], data)
     tree = [(0, 1), (3, 2)]
     assert _classes(net, tree)[0] == tn.TN_NODE_DENSE
-    got, plan = run_gpu(net, tree)
+    got, plan = run_gpu(net, tree, policy=NT)
     assert plan.mode_order(3) == [0, 2, 1]
     assert_close(got, _ref(net, tree), TOL_C64, "interleaved dense output")
 
@@ -122,7 +127,7 @@ def test_dense_chain(precision, tol):
     net = Network(tensors, ext, [0, 3], data)
     tree = [(0, 1), (3, 2)]
     assert _classes(net, tree, precision=precision) == [tn.TN_NODE_DENSE, tn.TN_NODE_DENSE]
-    got, _ = run_gpu(net, tree, precision=precision)
+    got, _ = run_gpu(net, tree, precision=precision, policy=NT)
     assert_close(got, _ref(net, tree), tol, f"dense chain {precision}")
 
 
@@ -158,7 +163,7 @@ def test_sliced_dense_root_accumulates():
     net = gemm_network(8, 8, 9, 3)
     sl = [net.tensors[0][-1], net.tensors[0][-2]]     # two K modes -> 4 slices
     assert _classes(net, [(0, 1)], sl) == [tn.TN_NODE_DENSE]
-    got, plan = run_gpu(net, [(0, 1)], sl)
+    got, plan = run_gpu(net, [(0, 1)], sl, policy=NT)
     assert plan.num_slices == 4
     assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced dense")
 
@@ -197,3 +202,35 @@ def test_dense_output_k_tiled_for_dense_consumer(p_ext, a_ext, precision, tol):
     assert p.node_mnk(1)[2] == a_ext * 64
     got, _ = run_gpu(net, tree, precision=precision)
     assert_close(got, _ref(net, tree), tol, f"K-tiled operand {p_ext}x{a_ext} {precision}")
+
+
+def test_sliced_dense_root_four_entry_stores():
+    # 128 x 256 root on tensor cores: the address-order stores go four
+    # entries per lane, and slices 1..3 add into the caller's output
+    net = gemm_network(7, 8, 10, 5)
+    sl = [net.tensors[0][-1], net.tensors[0][-3]]
+    assert _classes(net, [(0, 1)], sl) == [tn.TN_NODE_DENSE]
+    got, plan = run_gpu(net, [(0, 1)], sl, policy=NT)
+    assert plan.num_slices == 4
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced dense root, four-entry stores")
+
+
+def test_dense_root_output_not_16_byte_aligned():
+    # the caller's output 8 bytes past a 16-byte boundary: the tensor-core
+    # epilogue must fall back to single-entry stores
+    import torch
+    net = gemm_network(7, 8, 8, 6)            # k = 256: no split-K, the kernel stores the root
+    plan = tn.Plan.from_network(net, [(0, 1)], (), "tf32x3", NT)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE and plan.launches == 2
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    size = int(np.prod(plan.out_shape))
+    flat = torch.zeros(size + 1, dtype=torch.complex64, device=dev)
+    out = flat[1:].view(plan.out_shape)
+    assert out.data_ptr() % 16 == 8
+    plan.execute(leaves, out)
+    torch.cuda.synchronize(dev)
+    plan.check()
+    assert complex(flat[0].item()) == 0
+    assert_close(out.cpu().numpy().astype(np.complex128), _ref(net, [(0, 1)]), TOL_C64,
+                 "unaligned root output")
