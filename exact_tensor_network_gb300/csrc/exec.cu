@@ -29,7 +29,8 @@ int classify(const Plan &p, const NodePlan &nd) {
     const uint64_t kq = bf16 ? 8 : 4;
     if (p.policy == TN_POLICY_DENSE)
         return (!fp32 && nd.k % kq == 0) ? TN_NODE_DENSE : TN_NODE_SIMT;
-    if (p.policy == TN_POLICY_AUTO && nd.m * nd.n * nd.k <= kTinyMacs && nd.k <= kTinyMaxK)
+    if (p.policy == TN_POLICY_AUTO && nd.m * nd.n * nd.k <= kTinyMacs && nd.k <= kTinyMaxK &&
+        nd.m * nd.n <= kTinyMaxOut)
         return TN_NODE_TINY;
     if (!fp32 && nd.k % kq == 0 && nd.k >= 16 && nd.m >= 64 && nd.n >= 64) {
         const double in_b = bf16 ? 4.0 : 16.0;

@@ -40,19 +40,40 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
         for (int j = 0; j < kStreamMaxN; ++j) acc[j] = make_float2(0.f, 0.f);
         for (int64_t c0 = k0; c0 < k1; c0 += kStreamKc) {
             const int clen = (int)min((int64_t)kStreamKc, k1 - c0);
+            // this lane's first eight entries of the row are in flight while
+            // B is staged; later batches keep eight loads in flight as well
+            const float2 *arow = a.A + r * a.k + c0;
+            float2 av[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = l + u * lanes;
+                av[u] = (r < r1 && idx < clen) ? arow[idx] : make_float2(0.f, 0.f);
+            }
             __syncthreads();
+#pragma unroll 4
             for (int e = threadIdx.x; e < n * clen; e += kThreads) {
                 const int j = e / clen, kk = e - j * clen;
                 Bs[j * kStreamKc + kk] = a.B[(int64_t)j * a.k + c0 + kk];
             }
             __syncthreads();
             if (r < r1) {
-                const float2 *arow = a.A + r * a.k + c0;
-                for (int kk = l; kk < clen; kk += lanes) {
-                    const float2 av = arow[kk];
+                for (int kb = l; kb < clen; kb += 8 * lanes) {
+                    if (kb != l) {
 #pragma unroll
-                    for (int j = 0; j < kStreamMaxN; ++j)
-                        if (j < n) cfma(acc[j], av, Bs[j * kStreamKc + kk]);
+                        for (int u = 0; u < 8; ++u) {
+                            const int idx = kb + u * lanes;
+                            av[u] = idx < clen ? arow[idx] : make_float2(0.f, 0.f);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int idx = kb + u * lanes;
+                        if (idx < clen) {
+#pragma unroll
+                            for (int j = 0; j < kStreamMaxN; ++j)
+                                if (j < n) cfma(acc[j], av[u], Bs[j * kStreamKc + idx]);
+                        }
+                    }
                 }
             }
         }

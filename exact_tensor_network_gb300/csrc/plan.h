@@ -186,11 +186,14 @@ struct Launch {
     uint64_t flops, bytes; // algorithmic work of the launch (measurement)
 };
 
-// Tiny nodes: at most this many complex multiply-adds (m n k) and a k short
-// enough for one pass of a thread group over it.  Such a node costs the
-// batched dot-product kernel a few microseconds, less than a launch of its own.
+// Tiny nodes: at most this many complex multiply-adds (m n k), a k short
+// enough for one pass of a thread group over it, and few outputs (each
+// output reads its own A and B rows, which a tiled kernel would share).
+// Such a node costs the batched dot-product kernel a few microseconds, less
+// than a launch of its own.
 constexpr uint64_t kTinyMacs = 1ull << 23;
 constexpr uint64_t kTinyMaxK = 512;
+constexpr uint64_t kTinyMaxOut = 1ull << 17;
 
 inline int64_t sep_offset_host(const SepLayout &L, int64_t i) {
     int64_t off = 0;
