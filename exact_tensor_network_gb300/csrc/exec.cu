@@ -133,9 +133,15 @@ void release_events(Plan *p) {
     for (void *e : p->events)
         if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
     p->events.clear();
+    for (void *e : p->dag_events)
+        if (e) cudaEventDestroy(static_cast<cudaEvent_t>(e));
+    p->dag_events.clear();
     drop_graph(p);
     if (p->capture_stream) cudaStreamDestroy(static_cast<cudaStream_t>(p->capture_stream));
     p->capture_stream = nullptr;
+    for (void *s : p->lane_streams)
+        if (s) cudaStreamDestroy(static_cast<cudaStream_t>(s));
+    p->lane_streams.clear();
 }
 
 namespace {
@@ -165,6 +171,189 @@ struct Recorder {
         ++i;
     }
 };
+
+tn_status cuda_fail(Plan *p, cudaError_t e, const char *what);
+
+// ---- dependency graph of the launches, for recording ----
+//
+// What each launch reads and writes: byte ranges of the workspace arena, or
+// the caller's output (one token: lo < 0).  Leaves read in place are never
+// written and are left out.  Two launches conflict when one writes what the
+// other reads or writes; every order that keeps conflicting launches in
+// their issue order computes the same result as the issue order itself.
+struct Range {
+    int64_t lo, hi;
+};
+struct Access {
+    std::vector<Range> rd, wr;
+};
+
+void add_range(std::vector<Range> &v, const Place &pl, uint64_t bytes) {
+    if (pl.kind == PLACE_WS) v.push_back({(int64_t)pl.off, (int64_t)(pl.off + bytes)});
+    else if (pl.kind == PLACE_OUT) v.push_back({-1, -1});
+}
+
+bool overlap(const std::vector<Range> &x, const std::vector<Range> &y) {
+    for (const Range &a : x)
+        for (const Range &b : y) {
+            if (a.lo < 0 || b.lo < 0) {
+                if (a.lo < 0 && b.lo < 0) return true;
+                continue;
+            }
+            if (a.lo < b.hi && b.lo < a.hi) return true;
+        }
+    return false;
+}
+
+bool conflict(const Access &e, const Access &l) {
+    return overlap(e.wr, l.rd) || overlap(e.wr, l.wr) || overlap(e.rd, l.wr);
+}
+
+// Accesses of one slice's launches, in the order execute_range issues them.
+std::vector<Access> slice_accesses(const Plan &p) {
+    std::vector<Access> acc;
+    const int njobs = (int)p.perm_table.size();
+    for (int j0 = 0; j0 < njobs; j0 += kPermBatch) {
+        Access a;
+        for (int j = j0; j < std::min(njobs, j0 + kPermBatch); ++j) {
+            const PermDesc &d = p.perm_table[j];
+            if (d.dst_off < 0) a.wr.push_back({-1, -1});
+            else a.wr.push_back({d.dst_off, d.dst_off + d.size * (int64_t)fmt_bytes(d.fmt)});
+        }
+        acc.push_back(a);
+    }
+    const TinyDesc *tiny = reinterpret_cast<const TinyDesc *>(
+        p.table_blob.data() + (p.tiny_off - p.table_off));
+    for (const Launch &L : p.sched) {
+        if (L.kind == LAUNCH_PERMUTE) continue;
+        if (L.kind == LAUNCH_TINY) {
+            Access a;
+            for (int i = L.first; i < L.first + L.count; ++i) {
+                const TinyDesc &d = tiny[i];
+                const int64_t m = d.m, n = d.n, k = d.k;
+                a.rd.push_back({d.a_off, d.a_off + 8 * m * k});
+                a.rd.push_back({d.b_off, d.b_off + 8 * n * k});
+                if (d.c_off < 0) a.wr.push_back({-1, -1});
+                else a.wr.push_back({d.c_off, d.c_off + m * n * (int64_t)fmt_bytes(d.out_fmt)});
+            }
+            acc.push_back(a);
+            continue;
+        }
+        const NodePlan &nd = p.nodes[L.node];
+        Access a;
+        add_range(a.rd, nd.pa, nd.m * nd.k * fmt_bytes(p.fmt[nd.a]));
+        add_range(a.rd, nd.pb, nd.n * nd.k * fmt_bytes(p.fmt[nd.b]));
+        add_range(a.wr, nd.pc, nd.m * nd.n * fmt_bytes(nd.out_fmt));
+        if (nd.ksplit > 1) {
+            add_range(a.wr, nd.part, (uint64_t)nd.ksplit * nd.m * nd.n * 8);
+            acc.push_back(a);
+            Access r;
+            add_range(r.rd, nd.part, (uint64_t)nd.ksplit * nd.m * nd.n * 8);
+            add_range(r.wr, nd.pc, nd.m * nd.n * fmt_bytes(nd.out_fmt));
+            acc.push_back(r);
+        } else {
+            acc.push_back(a);
+        }
+    }
+    return acc;
+}
+
+constexpr int kLanes = 6;   // streams a recording spreads independent launches over
+
+// Issues the launches of a recording on several streams: launch i waits
+// (by event) for the launches it conflicts with on other streams and
+// follows the previous launch of its own stream.  Stream 0 is the capture
+// stream; the others join the capture through those waits and are joined
+// back into stream 0 at the end.
+struct Dag {
+    std::vector<cudaStream_t> lane_stream;
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> lane;                    // per launch
+    std::vector<std::vector<int>> wait;       // per launch: launches to wait for
+    std::vector<int> tail;                    // per stream: last launch
+    size_t next = 0;
+    bool ok = true;
+
+    cudaStream_t begin() {
+        const size_t i = next;
+        cudaStream_t s = lane_stream[lane[i]];
+        for (int e : wait[i])
+            if (cudaStreamWaitEvent(s, ev[e], 0) != cudaSuccess) ok = false;
+        return s;
+    }
+    void end() {
+        const size_t i = next++;
+        if (cudaEventRecord(ev[i], lane_stream[lane[i]]) != cudaSuccess) ok = false;
+    }
+    bool join() {
+        for (size_t l = 1; l < lane_stream.size(); ++l)
+            if (tail[l] >= 0 && cudaStreamWaitEvent(lane_stream[0], ev[tail[l]], 0) != cudaSuccess)
+                return false;
+        return ok;
+    }
+};
+
+// Dependencies and streams of all launches of slices first, first + step, ...
+tn_status build_dag(Plan *p, cudaStream_t origin, uint64_t first, uint64_t step, Dag *d) {
+    const std::vector<Access> one = slice_accesses(*p);
+    const size_t P = one.size();
+    uint64_t nsl = 0;
+    for (uint64_t s = first; s < p->n_slices; s += step) ++nsl;
+    const size_t N = P * nsl;
+    while (p->lane_streams.size() < (size_t)kLanes - 1) {
+        cudaStream_t s;
+        cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(p, e, "creating a stream");
+        p->lane_streams.push_back(s);
+    }
+    while (p->dag_events.size() < N) {
+        cudaEvent_t ev;
+        cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(p, e, "creating an event");
+        p->dag_events.push_back(ev);
+    }
+    d->lane_stream.assign(1, origin);
+    for (void *s : p->lane_streams) d->lane_stream.push_back(static_cast<cudaStream_t>(s));
+    d->ev.resize(N);
+    for (size_t i = 0; i < N; ++i) d->ev[i] = static_cast<cudaEvent_t>(p->dag_events[i]);
+    d->lane.assign(N, 0);
+    d->wait.assign(N, {});
+    d->tail.assign(kLanes, -1);
+    d->next = 0;
+    std::vector<int> last(kLanes);
+    for (size_t i = 0; i < N; ++i) {
+        // latest conflicting launch on each stream
+        std::fill(last.begin(), last.end(), -1);
+        bool any = false;
+        for (size_t e = 0; e < i; ++e)
+            if (conflict(one[e % P], one[i % P])) {
+                last[d->lane[e]] = std::max(last[d->lane[e]], (int)e);
+                any = true;
+            }
+        // a stream whose last launch is one of those adds no false order;
+        // else an unused stream; else the stream with the oldest last launch
+        int l = -1;
+        if (!any) {
+            l = 0;   // joins nothing: stays on the capture stream
+        } else {
+            for (int c = 0; c < kLanes; ++c)
+                if (d->tail[c] >= 0 && last[c] == d->tail[c] && (l < 0 || d->tail[c] > d->tail[l])) l = c;
+            if (l < 0)
+                for (int c = 1; c < kLanes && l < 0; ++c)
+                    if (d->tail[c] < 0) l = c;
+            if (l < 0) {
+                l = 0;
+                for (int c = 1; c < kLanes; ++c)
+                    if (d->tail[c] < d->tail[l]) l = c;
+            }
+        }
+        d->lane[i] = l;
+        for (int c = 0; c < kLanes; ++c)
+            if (c != l && last[c] >= 0) d->wait[i].push_back(last[c]);
+        d->tail[l] = (int)i;
+    }
+    return TN_OK;
+}
 
 uint64_t node_bytes(const NodePlan &nd, bool accumulate) {
     return 8 * (nd.m * nd.k + nd.n * nd.k + nd.m * nd.n * (accumulate ? 2 : 1));
@@ -222,8 +411,12 @@ tn_status upload_tables(Plan *p) {
 
 // Slices first, first + step, ... of the plan; the first of them writes the
 // output and the others add into it; an empty range zeroes the output.
-tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
-                        uint64_t first, uint64_t step) {
+namespace {
+
+// Slices first, first + step, ... issued on `stream`, or, with a graph
+// recorder, each launch on the stream the recorder picks for it.
+tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
+                      uint64_t first, uint64_t step, Dag *dag) {
     if (first >= p->n_slices) {
         cudaError_t e = cudaMemsetAsync(out_ptr, 0, p->out_elems * sizeof(float2), stream);
         return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "zeroing the output");
@@ -287,7 +480,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
             uint64_t bytes = 0;
             for (int j = 0; j < cnt; ++j) bytes += 16 * (uint64_t)p->perm_table[j0 + j].size;
             rec.begin(TN_KERNEL_PERMUTE, -1, 0, bytes);
-            cudaError_t e = launch_permute(*pl, ctas, stream);
+            cudaError_t e = launch_permute(*pl, ctas, dag ? dag->begin() : stream);
+            if (dag) dag->end();
             rec.end();
             if (e != cudaSuccess) {
                 st = cuda_fail(p, e, "launching the leaf permutation");
@@ -306,7 +500,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 tl.out = out;
                 tl.accumulate_root = later ? 1 : 0;
                 rec.begin(TN_KERNEL_TINY, -1, L.flops, L.bytes);
-                cudaError_t e = launch_tiny_batch(tl, L.ctas, stream);
+                cudaError_t e = launch_tiny_batch(tl, L.ctas, dag ? dag->begin() : stream);
+                if (dag) dag->end();
                 rec.end();
                 if (e != cudaSuccess) {
                     st = cuda_fail(p, e, "launching a tiny-node batch");
@@ -352,7 +547,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +
                               fmt_bytes(nd.out_fmt) * nd.m * nd.n * (accumulate ? 2 : 1));
-                e = launch_dense(*d, p->num_sms, stream);
+                e = launch_dense(*d, p->num_sms, dag ? dag->begin() : stream);
+                if (dag) dag->end();
                 rec.end();
             } else if (nd.cls == TN_NODE_STREAM) {
                 StreamArgs a;
@@ -378,7 +574,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 a.lanes = lanes;
                 a.rows_per_cta = (int32_t)rpc;
                 rec.begin(TN_KERNEL_STREAM, nd.step, flops, node_bytes(nd, accumulate));
-                e = launch_stream_node(a, stream);
+                e = launch_stream_node(a, dag ? dag->begin() : stream);
+                if (dag) dag->end();
                 rec.end();
             } else {
                 NodeArgs a;
@@ -399,7 +596,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 a.kchunk = nd.kchunk;
                 a.part = reinterpret_cast<float2 *>(arena + nd.part.off);
                 rec.begin(TN_KERNEL_SIMT, nd.step, flops, node_bytes(nd, accumulate));
-                e = launch_simt_node(a, stream);
+                e = launch_simt_node(a, dag ? dag->begin() : stream);
+                if (dag) dag->end();
                 rec.end();
             }
             if (e == cudaSuccess && nd.ksplit > 1) {
@@ -419,7 +617,8 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
                 // bytes: every partial read once, the output written once
                 rec.begin(TN_KERNEL_REDUCE, nd.step, 0,
                           8 * (uint64_t)nd.ksplit * nd.m * nd.n + fmt_bytes(nd.out_fmt) * nd.m * nd.n);
-                e = launch_splitk_reduce(r, stream);
+                e = launch_splitk_reduce(r, dag ? dag->begin() : stream);
+                if (dag) dag->end();
                 rec.end();
             }
             if (e != cudaSuccess) {
@@ -430,6 +629,13 @@ tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cu
     }
     delete pl;
     return st;
+}
+
+}  // namespace
+
+tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
+                        uint64_t first, uint64_t step) {
+    return issue_range(p, leaf_ptrs, out_ptr, stream, first, step, nullptr);
 }
 
 // All slices.
@@ -481,7 +687,12 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
         p->use_graph = false;
         return TN_OK;
     }
-    const tn_status cst = execute_plan(p, leaf_ptrs, out_ptr, cs);
+    // recorded as a dependency graph: launches that touch no common bytes
+    // (independent branches of the tree) may run at the same time
+    Dag dag;
+    tn_status cst = build_dag(p, cs, 0, 1, &dag);
+    if (cst == TN_OK) cst = issue_range(p, leaf_ptrs, out_ptr, cs, 0, 1, &dag);
+    if (cst == TN_OK && (dag.next != dag.lane.size() || !dag.join())) cst = TN_ECUDA;
     cudaGraph_t g = nullptr;
     cudaError_t e = cudaStreamEndCapture(cs, &g);
     cudaGraphExec_t ex = nullptr;

@@ -277,6 +277,8 @@ struct Plan {
     bool use_graph = true;
     void *graph_exec = nullptr;
     void *capture_stream = nullptr;
+    std::vector<void *> lane_streams;           // recording: extra streams for independent launches
+    std::vector<void *> dag_events;             // recording: one event per launch
     std::vector<const void *> graph_leaves;
     void *graph_out = nullptr;
     void *graph_ws = nullptr;

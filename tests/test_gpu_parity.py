@@ -243,3 +243,54 @@ def test_profiling_records_every_launch():
     assert len(recs) == plan.launches
     assert all(r["ms"] >= 0 for r in recs)
     assert sum(r["flops"] for r in recs) == plan.flops
+
+
+def _replay_case(case):
+    import exact_tensor_network_gb300 as tn
+    if case.startswith("random_60"):
+        net, tree, _ = configs.random_60()
+        pol = {"random_60_notiny": tn.TN_POLICY_NO_TINY, "random_60_simt": tn.TN_POLICY_SIMT}[case]
+        return net, tree, [], pol
+    if case == "circuit_3x3_sliced":
+        net, tree, _ = configs.circuit_3x3_d4()
+        return net, tree, net.closed_modes()[:3], tn.TN_POLICY_AUTO
+    if case.startswith("tiny_sliced"):
+        seed = int(case[-1])
+        net = random_tiny_network(500 + seed)
+        tree = greedy_tree(net, seed)
+        sl = [x for x in net.closed_modes()][:2]
+        return net, tree, sl, tn.TN_POLICY_NO_TINY if seed % 2 else tn.TN_POLICY_AUTO
+    # a split-K tensor-core node (64 x 128 x 2048) feeding a split-K
+    # streaming node (4 x 1 x 8192), two slices over the extra mode z
+    rng = np.random.default_rng(41)
+    ext = [64, 2048, 128, 4, 2]               # a x b e z
+    tensors = [[0, 1, 4], [2, 1, 4], [3, 2, 0]]
+    data = [((rng.standard_normal([ext[x] for x in t]) + 1j * rng.standard_normal([ext[x] for x in t]))
+             * 0.05).astype(np.complex64) for t in tensors]
+    net = Network(tensors, ext, [3], data)
+    return net, [(0, 1), (3, 2)], [4], tn.TN_POLICY_AUTO
+
+
+@pytest.mark.parametrize("case", ["random_60_notiny", "random_60_simt", "circuit_3x3_sliced",
+                                  "tiny_sliced_0", "tiny_sliced_1", "splitk_sliced"])
+def test_replayed_dependency_graph(case):
+    """The recorded graph runs independent launches concurrently (ordered only
+    where they touch common bytes); its replays match the oracle, including
+    across slices (leaf buffers reused, the root adding into the output) and
+    with split-K partials."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    net, tree, sl, pol = _replay_case(case)
+    ref = _ref(net, tree)
+    plan = tn.Plan.from_network(net, tree, sl, "tf32x3", pol)
+    if sl:
+        assert plan.num_slices > 1
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
+    for it in range(4):                        # direct, then three replays
+        out.fill_(complex(9.0, -9.0))
+        plan.execute(leaves, out)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy().astype(np.complex128), ref, what=f"{case} call {it}")
+    plan.check()
