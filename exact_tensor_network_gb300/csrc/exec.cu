@@ -66,13 +66,21 @@ void choose_split(const Plan &p, NodePlan &nd) {
     nd.ksplit = 1;
     nd.kchunk = (int64_t)nd.k;
     nd.swap = 0;
+    nd.tail_first = -1;
     uint64_t units = 0, outs = nd.m * nd.n;
     if (nd.cls == TN_NODE_DENSE) {
         // tensor-core tiles are 128 x 128 and one CTA runs per SM; splits are
         // whole multiples of the 256-entry accumulation chunk
-        const uint64_t tiles = ((nd.m + 127) / 128) * ((nd.n + 127) / 128);
+        const uint64_t tiles = dense_tiles(nd);
         const uint64_t sms = kTargetCtas / 2;
-        if (tiles >= sms || nd.k < 512) return;
+        if (tiles >= sms) {
+            // a last wave at most half full runs its tiles as two k halves:
+            // it then takes half a tile's time instead of a whole one
+            const uint64_t tail = tiles % sms;
+            if (tail > 0 && 2 * tail <= sms && nd.k >= 512) nd.tail_first = (int64_t)(tiles - tail);
+            return;
+        }
+        if (nd.k < 512) return;
         // whole waves only: tiles x splits <= SMs
         uint64_t s = std::min<uint64_t>(sms / tiles, nd.k / 256);
         s = std::min<uint64_t>(s, kPartialBudget / (8 * outs));
@@ -244,11 +252,12 @@ std::vector<Access> slice_accesses(const Plan &p) {
         add_range(a.rd, nd.pa, nd.m * nd.k * fmt_bytes(p.fmt[nd.a]));
         add_range(a.rd, nd.pb, nd.n * nd.k * fmt_bytes(p.fmt[nd.b]));
         add_range(a.wr, nd.pc, nd.m * nd.n * fmt_bytes(nd.out_fmt));
+        if (nd.tail_first >= 0) add_range(a.wr, nd.part, part_bytes(nd));
         if (nd.ksplit > 1) {
-            add_range(a.wr, nd.part, (uint64_t)nd.ksplit * nd.m * nd.n * 8);
+            add_range(a.wr, nd.part, part_bytes(nd));
             acc.push_back(a);
             Access r;
-            add_range(r.rd, nd.part, (uint64_t)nd.ksplit * nd.m * nd.n * 8);
+            add_range(r.rd, nd.part, part_bytes(nd));
             add_range(r.wr, nd.pc, nd.m * nd.n * fmt_bytes(nd.out_fmt));
             acc.push_back(r);
         } else {
@@ -543,6 +552,9 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->kchunk = nd.kchunk;
                 d->part = reinterpret_cast<float2 *>(arena + nd.part.off);
                 d->ep = nd.ep_off >= 0 ? reinterpret_cast<const EpTable *>(ws + nd.ep_off) : nullptr;
+                d->tail_first = nd.tail_first;
+                d->tail_cnt = nd.tail_first >= 0 ? reinterpret_cast<int32_t *>(ws + nd.tail_cnt_off)
+                                                 : nullptr;
                 const uint64_t in_b = d->bf16 ? 4 : 16;
                 rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +
@@ -731,6 +743,13 @@ tn_status check_plan(Plan *p) {
     if (h.code != ERR_NONE) {
         e = cudaMemset(p->ws, 0, sizeof(h));
         if (e != cudaSuccess) return cuda_fail(p, e, "clearing the status word");
+        // a kernel that gave up may have left tail-tile counters raised:
+        // restore the tables (counters included) before the next run
+        if (!p->table_blob.empty()) {
+            e = cudaMemcpy(static_cast<char *>(p->ws) + p->table_off, p->table_blob.data(),
+                           p->table_blob.size(), cudaMemcpyHostToDevice);
+            if (e != cudaSuccess) return cuda_fail(p, e, "restoring the descriptor tables");
+        }
         p->last_error = "device status " + std::to_string(h.code) + " at " + std::to_string(h.where);
         return h.code == ERR_TIMEOUT ? TN_ETIMEOUT : TN_EDEVICE;
     }

@@ -49,6 +49,7 @@ namespace {
 
 constexpr int BM = 128;                 // complex output rows per tile
 constexpr int BN = 128;                 // complex output columns per tile
+static_assert(BM == kDenseBM && BN == kDenseBN, "tile shape shared with the planner");
 constexpr int ROW_BYTES = 64;           // K bytes per smem row (64-byte swizzle)
 constexpr int PLANE_TILE = BM * ROW_BYTES;   // 8 KiB: 128 rows of one plane
 constexpr int THREADS = 384;            // 3 warpgroups
@@ -58,6 +59,8 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 // register split: launched with 168 per thread (384 x 168 = 64512)
 constexpr int REGS_LOW = 56, REGS_HIGH = 224;
+static_assert(4 * 32 * REGS_LOW + DRAIN_WARPS * 32 * REGS_HIGH <= THREADS * 168,
+              "register split exceeds the launch's registers");
 
 template <bool BF16>
 struct Cfg {
@@ -226,6 +229,41 @@ __device__ __forceinline__ void stage_block(float2 *tile, int lane, const float 
     }
 }
 
+// Work item w of a launch: its tile t, k-block range [kb0, kb1), k split sp
+// (split-K) and, for a tail tile's half, which half (else -1).  Work items
+// are whole tiles up to tail_first, then two halves per tail tile; with
+// split-K, ksplit items per tile.
+struct Item {
+    int64_t t;
+    int sp, kb0, kb1, half;
+};
+__device__ __forceinline__ Item work_item(int64_t w, int ksplit, int kbs, int nkb,
+                                          int64_t tail_first) {
+    Item it;
+    it.half = -1;
+    if (ksplit > 1) {
+        // work < 2^31 items with split-K (tiles x splits fill about one wave)
+        const uint32_t q = static_cast<uint32_t>(w) / static_cast<uint32_t>(ksplit);
+        it.t = q;
+        it.sp = static_cast<int>(static_cast<uint32_t>(w) - q * static_cast<uint32_t>(ksplit));
+        it.kb0 = it.sp * kbs;
+        it.kb1 = min(nkb, it.kb0 + kbs);
+    } else if (w < tail_first) {
+        it.t = w;
+        it.sp = 0;
+        it.kb0 = 0;
+        it.kb1 = nkb;
+    } else {
+        const int64_t u = w - tail_first;
+        it.t = tail_first + (u >> 1);
+        it.half = static_cast<int>(u & 1);
+        it.sp = 0;
+        it.kb0 = it.half ? nkb / 2 : 0;
+        it.kb1 = it.half ? nkb : nkb / 2;
+    }
+    return it;
+}
+
 // Output tile of linear tile index t: groups of 8 row tiles, columns inside.
 __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t ntiles, int64_t &mt,
                                             int64_t &nt) {
@@ -284,8 +322,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     // work item w = (tile w / ksplit, k split w % ksplit); a split covers kbs
     // k-blocks
     const int ksplit = a.ksplit > 1 ? a.ksplit : 1;
-    const int64_t work = tiles * ksplit;
     const int kbs = ksplit > 1 ? static_cast<int>(a.kchunk / C::KB) : nkb;
+    // first tail tile and work items: recomputed from the parameters where
+    // used, so they hold no registers across the role split
+#define TAIL_FIRST ((ksplit == 1 && a.tail_first >= 0) ? a.tail_first : tiles)
+#define WORK (ksplit > 1 ? tiles * ksplit : TAIL_FIRST + 2 * (tiles - TAIL_FIRST))
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
@@ -294,13 +335,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, last_par = 0;   // bit s: stage s has a load; its parity
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
-                const int64_t t = w / ksplit;
-                const int sp = static_cast<int>(w - t * ksplit);
+            for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
                 int64_t mt, nt;
-                tile_coords(t, mtiles, ntiles, mt, nt);
+                tile_coords(it.t, mtiles, ntiles, mt, nt);
                 const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * BN);
-                const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+                const int kb0 = it.kb0, kb1 = it.kb1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
                         ok = false;
@@ -343,10 +383,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             const uint32_t d1 = tmem, d2 = tmem + 256;
             uint32_t stage = 0, phase = 0, tphase = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
-                const int64_t t = w / ksplit;
-                const int sp = static_cast<int>(w - t * ksplit);
-                const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+            for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const int kb0 = it.kb0, kb1 = it.kb1;
                 const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
                 for (int ch = 0; ch < nch && ok; ++ch) {
                     if (!wait_bounded(tmem_empty, tphase ^ 1, abort_flag)) {
@@ -445,13 +484,13 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const PlanarTile ep_tile = pretiled ? PlanarTile{0, 0, -1, 0} : a.out_tile;
         uint32_t tphase = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < work && ok; w += gridDim.x) {
-            const int64_t t = w / ksplit;
-            const int sp = static_cast<int>(w - t * ksplit);
-            const int kb0 = sp * kbs, kb1 = min(nkb, kb0 + kbs);
+        for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+            const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+            const int sp = it.sp;
+            const int kb0 = it.kb0, kb1 = it.kb1;
             const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
             int64_t mt, nt;
-            tile_coords(t, mtiles, ntiles, mt, nt);
+            tile_coords(it.t, mtiles, ntiles, mt, nt);
             float sr[64], si[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) sr[c] = si[c] = 0.f;
@@ -485,6 +524,36 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 tphase ^= 1;
             }
             if (!ok) break;
+            // A tail tile's half.  Each drain warp pairs with the same warp
+            // (same 32 x 64 block) of the other half's CTA: it publishes its
+            // sums and counts in; the second to arrive adds the other's sums
+            // (below, block by block) and stores.  Two terms: the sum is the
+            // same whichever comes first.  Per warp: no wait on another warp
+            // or CTA.
+            const float2 *other = nullptr;
+            if (it.half >= 0) {
+                const int64_t slot = (it.t - TAIL_FIRST) * DRAIN_WARPS + (warp - 4);
+                float2 *mine = a.part + (slot * 2 + it.half) * (64 * 32);
+                // through the staging tile, block by block (rolled: unrolled
+                // stores of all 64 sums would spill registers)
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    stage_block(stage_tile, lane, sr, si, cc);
+#pragma unroll 4
+                    for (int x = 0; x < 16; ++x)
+                        mine[(cc * 16 + x) * 32 + lane] = stage_tile[swz(lane * 16 + x)];
+                    __syncwarp();
+                }
+                __threadfence();
+                __syncwarp();
+                int first = 0;
+                if (lane == 0) first = atomicAdd(a.tail_cnt + slot, 1) == 0;
+                first = __shfl_sync(0xffffffffu, first, 0);
+                if (first) continue;
+                __threadfence();
+                if (lane == 0) a.tail_cnt[slot] = 0;   // ready for the next run
+                other = a.part + (slot * 2 + (it.half ^ 1)) * (64 * 32);
+            }
             void *dst = plain ? static_cast<void *>(a.part + (int64_t)sp * plane) : a.C;
             const int64_t i0 = mt * BM + q * 32;
             const int64_t i = i0 + lane;
@@ -499,6 +568,16 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 const int64_t j0 = nt * BN + h * 64 + cc * 16;
                 if (j0 >= a.n) break;   // warp-uniform
                 stage_block(stage_tile, lane, sr, si, cc);
+                if (other) {
+                    // the other half's sums of this lane's 16 entries
+#pragma unroll 4
+                    for (int x = 0; x < 16; ++x) {
+                        const float2 v = __ldcg(other + (cc * 16 + x) * 32 + lane);
+                        float2 &d = stage_tile[swz(lane * 16 + x)];
+                        d.x += v.x;
+                        d.y += v.y;
+                    }
+                }
                 __syncwarp();
                 if (ep_s) {
                     // the block in address order
@@ -568,6 +647,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         }
     }
 
+#undef WORK
+#undef TAIL_FIRST
     fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -583,8 +664,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream) {
-    const int64_t work = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN) *
-                         (args.ksplit > 1 ? args.ksplit : 1);
+    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
+    const int64_t work = args.ksplit > 1          ? tiles * args.ksplit
+                         : args.tail_first >= 0 ? args.tail_first + 2 * (tiles - args.tail_first)
+                                                : tiles;
     const int grid = static_cast<int>(work < num_sms ? work : num_sms);
     if (grid <= 0) return cudaSuccess;
     if (args.bf16) {

@@ -101,6 +101,10 @@ struct DenseArgs {
     int64_t kchunk;
     float2 *part;
     const EpTable *ep;    // address-order store table, or null
+    // tail split (see NodePlan::tail_first): halves' sums in `part`, one
+    // counter per tail tile; tail_first < 0 when off
+    int64_t tail_first;
+    int32_t *tail_cnt;
 };
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream);

@@ -124,7 +124,29 @@ struct NodePlan {
     // dense class: byte offset (from the workspace start) of the node's
     // address-order store table (EpTable), or -1 when it has none
     int64_t ep_off;
+    // dense class, tail split: tiles from tail_first on (those past the last
+    // full wave) run as two k halves; each half writes its fp32 sums to
+    // `part` and counts itself in, per drain warp, in a counter (block of
+    // counters at tail_cnt_off: byte offset from the workspace start); the
+    // second to arrive adds the other half and stores.  -1: no tail split.
+    int64_t tail_first;
+    int64_t tail_cnt_off;
 };
+
+// Tensor-core tile (complex entries), its drain warps (one tail-tile
+// counter each) and the bytes of a node's fp32 partial sums: split-K
+// partials, or the two halves of every tail tile.
+constexpr int64_t kDenseBM = 128, kDenseBN = 128;
+constexpr uint64_t kDrainWarps = 8;
+inline uint64_t dense_tiles(const NodePlan &nd) {
+    return ((nd.m + kDenseBM - 1) / kDenseBM) * ((nd.n + kDenseBN - 1) / kDenseBN);
+}
+inline uint64_t part_bytes(const NodePlan &nd) {
+    if (nd.ksplit > 1) return (uint64_t)nd.ksplit * nd.m * nd.n * 8;
+    if (nd.tail_first >= 0)
+        return (dense_tiles(nd) - (uint64_t)nd.tail_first) * 2 * kDenseBM * kDenseBN * 8;
+    return 0;
+}
 
 // Address-order store table of a tensor-core node.  Every warp of the
 // kernel's epilogue owns 32 output rows x 16 columns at a time; when the

@@ -244,8 +244,7 @@ tn_status layout_plan(Plan *p) {
         const int ts = t_of[n + s];
         if (!nd.is_root)
             iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), ts, consume_t(nd.out), nd.out, 0});
-        if (nd.ksplit > 1)
-            iv.push_back({(uint64_t)nd.ksplit * nd.m * nd.n * 8, ts, ts, n + S + s, 0});
+        if (part_bytes(nd) > 0) iv.push_back({part_bytes(nd), ts, ts, n + S + s, 0});
     }
     p->arena_bytes = place_buffers(iv);
     std::vector<Place> where(n + 2 * S, Place{PLACE_WS, -1, 0});
@@ -337,7 +336,16 @@ tn_status layout_plan(Plan *p) {
     }
     const uint64_t tiny_start = align_up(ep_start + eps.size() * sizeof(EpTable));
     p->tiny_off = p->table_off + tiny_start;
-    p->table_blob.assign(tiny_start + tiny.size() * sizeof(TinyDesc), 0);
+    // tail-tile counters (zero; every run leaves them zero again)
+    const uint64_t cnt_start = align_up(tiny_start + tiny.size() * sizeof(TinyDesc));
+    uint64_t cnt = 0;
+    for (auto &nd : p->nodes) {
+        nd.tail_cnt_off = -1;
+        if (nd.tail_first < 0) continue;
+        nd.tail_cnt_off = (int64_t)(p->table_off + cnt_start + 4 * cnt);
+        cnt += (dense_tiles(nd) - (uint64_t)nd.tail_first) * kDrainWarps;
+    }
+    p->table_blob.assign(cnt_start + 4 * cnt, 0);
     if (perm_bytes) std::memcpy(p->table_blob.data(), p->perm_table.data(), perm_bytes);
     if (!eps.empty())
         std::memcpy(p->table_blob.data() + ep_start, eps.data(), eps.size() * sizeof(EpTable));

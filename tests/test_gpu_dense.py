@@ -234,3 +234,31 @@ def test_dense_root_output_not_16_byte_aligned():
     assert complex(flat[0].item()) == 0
     assert_close(out.cpu().numpy().astype(np.complex128), _ref(net, [(0, 1)]), TOL_C64,
                  "unaligned root output")
+
+
+@pytest.mark.parametrize("m,n,k,precision,tol", [
+    (2048, 1280, 512, "tf32x3", TOL_C64),     # 160 tiles: 8 past the last full wave
+    (2000, 1300, 528, "tf32x3", TOL_C64),     # ragged tiles, 33 k-blocks: halves of 16 and 17
+    (2048, 1280, 544, "bf16", TOL_BF16),      # bf16: 17 k-blocks
+])
+def test_dense_tail_tiles_split_in_k_halves(m, n, k, precision, tol):
+    """Tiles past the last full wave run as two k halves on two CTAs; the
+    second to finish adds the other's sums.  Matches the oracle, and two
+    runs give identical bits (a sum of two terms does not depend on which
+    half finished first)."""
+    import torch
+    net = node_network(m, n, k, m + n + k)
+    plan = tn.Plan.from_network(net, [(0, 1)], (), precision, NT)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE and plan.launches == 2
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    outs = []
+    for _ in range(3):
+        out = torch.full(plan.out_shape, complex(7.0, -3.0), dtype=torch.complex64, device=dev)
+        plan.execute(leaves, out)
+        torch.cuda.synchronize(dev)
+        outs.append(out.cpu().numpy())
+    plan.check()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    assert_close(outs[2].astype(np.complex128), _ref(net, [(0, 1)]), tol,
+                 f"tail halves {m}x{n}x{k} {precision}")
