@@ -105,6 +105,95 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
     }
 }
 
+// Streaming node with k <= 16 (gate-like, outer products): B (n x k) is
+// staged once per CTA; each thread takes 16 / K rows per pass (K = k rounded
+// up to a power of two), issues all their loads before any arithmetic
+// (16-byte loads when k = K is even) and then computes and stores the rows
+// one by one.  Consecutive threads own consecutive rows, so A is read and
+// (for outputs whose M side is innermost) C written in whole lines.
+template <int K>
+__global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_constant__ StreamArgs a) {
+    constexpr int RPT = 16 / K;   // rows per thread and pass
+    __shared__ float2 Bs[kStreamMaxN * K];
+    __shared__ int64_t offn_s[kStreamMaxN];
+    // row-major [m, n] outputs: each warp's 32 rows are one contiguous run,
+    // staged here and stored by consecutive lanes
+    __shared__ float2 Cs[kThreads / 32][32 * (kStreamMaxN + 1)];
+    const int n = (int)a.n, k = (int)a.k;
+    for (int e = threadIdx.x; e < n * K; e += kThreads) {
+        const int j = e / K, kk = e - j * K;
+        Bs[e] = kk < k ? a.B[(int64_t)j * k + kk] : make_float2(0.f, 0.f);
+    }
+    if (threadIdx.x < n) offn_s[threadIdx.x] = sep_offset(a.ln, threadIdx.x);
+    __syncthreads();
+    const bool vec = (k == K) && (K % 2 == 0);
+    const int64_t pass = (int64_t)kThreads * RPT;
+    for (int64_t base = (int64_t)blockIdx.x * pass; base < a.m; base += (int64_t)gridDim.x * pass) {
+        float2 av[RPT][K];
+#pragma unroll
+        for (int u = 0; u < RPT; ++u) {
+            const int64_t r = base + u * kThreads + threadIdx.x;
+            const float2 *row = a.A + r * k;
+            if (r < a.m && vec) {
+                const float4 *row4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+                for (int h = 0; h < K / 2; ++h) {
+                    const float4 v = row4[h];
+                    av[u][2 * h] = make_float2(v.x, v.y);
+                    av[u][2 * h + 1] = make_float2(v.z, v.w);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < K; ++kk)
+                    av[u][kk] = (r < a.m && kk < k) ? row[kk] : make_float2(0.f, 0.f);
+            }
+        }
+        if (a.rows_contig) {
+            const int lane = threadIdx.x & 31;
+            float2 *tile = Cs[threadIdx.x >> 5];
+            const int ts = n | 1;   // odd row stride: lanes' rows in distinct banks
+#pragma unroll
+            for (int u = 0; u < RPT; ++u) {
+                const int64_t r = base + u * kThreads + threadIdx.x;
+                if (r < a.m) {
+#pragma unroll 1
+                    for (int j = 0; j < n; ++j) {
+                        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int kk = 0; kk < K; ++kk) cfma(acc, av[u][kk], Bs[j * K + kk]);
+                        tile[lane * ts + j] = acc;
+                    }
+                }
+                __syncwarp();
+                const int64_t r0 = base + u * kThreads + (threadIdx.x & ~31);
+                const int64_t cnt = r0 < a.m ? min((int64_t)32, a.m - r0) * n : 0;
+#pragma unroll 1
+                for (int e = lane; e < (int)cnt; e += 32) {
+                    const int rr = e / n;
+                    store_entry(a.C, a.out_fmt, a.m * a.n, r0 * n + e, tile[rr * ts + (e - rr * n)],
+                                a.accumulate, a.out_tile);
+                }
+                __syncwarp();
+            }
+            continue;
+        }
+#pragma unroll
+        for (int u = 0; u < RPT; ++u) {
+            const int64_t r = base + u * kThreads + threadIdx.x;
+            if (r >= a.m) continue;
+            const int64_t offm = sep_offset(a.lm, r);
+#pragma unroll 1
+            for (int j = 0; j < n; ++j) {
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < K; ++kk) cfma(acc, av[u][kk], Bs[j * K + kk]);
+                store_entry(a.C, a.out_fmt, a.m * a.n, offm + offn_s[j], acc, a.accumulate,
+                            a.out_tile);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_constant__ ReduceArgs a) {
     const int64_t mn = a.m * a.n;
     for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < mn;
@@ -124,6 +213,27 @@ __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_co
 }  // namespace
 
 cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
+    if (args.k <= 16 && args.ksplit <= 1) {
+        // output entry (i, j) at i n + j (plain row-major [m, n]) with n >= 4:
+        // stage each warp's rows; with n < 4 a thread's own entries already
+        // fill most of a sector
+        StreamArgs a2 = args;
+        a2.rows_contig = args.n >= 4 &&
+                         (args.lm.nrun == 0 || (args.lm.nrun == 1 && args.lm.stride[0] == args.n)) &&
+                         (args.ln.nrun == 0 || (args.ln.nrun == 1 && args.ln.stride[0] == 1));
+        const int K = args.k <= 2 ? 2 : args.k <= 4 ? 4 : args.k <= 8 ? 8 : 16;
+        const int64_t pass = (int64_t)kThreads * (16 / K);
+        int64_t blocks = (args.m + pass - 1) / pass;
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        if (blocks < 1) blocks = 1;
+        switch (K) {
+            case 2: stream_rows_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
+            case 4: stream_rows_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
+            case 8: stream_rows_kernel<8><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
+            default: stream_rows_kernel<16><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
+        }
+        return cudaGetLastError();
+    }
     const int64_t blocks = (args.m + args.rows_per_cta - 1) / args.rows_per_cta;
     dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
     if (args.out_fmt == FMT_SPLIT4)

@@ -54,6 +54,7 @@ struct StreamArgs {
     int32_t accumulate;
     int32_t out_fmt;
     PlanarTile out_tile;
+    int32_t rows_contig;  // set by the launcher: entry (i, j) lies at i n + j
 };
 
 // Ordered sum of split-K partials into the node's output.

@@ -37,6 +37,11 @@ def _ref(net, tree):
     (1 << 16, 16, 16, tn.TN_NODE_STREAM),
     (3, 100000, 1, tn.TN_NODE_STREAM),      # outer product, swapped
     (1000, 7, 300, tn.TN_NODE_STREAM),
+    (100003, 5, 3, tn.TN_NODE_STREAM),      # k <= 16, odd: rows kernel, scalar loads
+    (70001, 13, 9, tn.TN_NODE_STREAM),      # k = 9 padded to 16
+    (65536, 3, 8, tn.TN_NODE_STREAM),       # k = 8: 16-byte loads
+    (1 << 18, 1, 4, tn.TN_NODE_STREAM),     # n = 1
+    (33, 2, 1, tn.TN_NODE_STREAM),          # fewer rows than one pass
     (100, 90, 5000, tn.TN_NODE_SIMT),       # split SIMT tiles
     (70, 300, 1001, tn.TN_NODE_SIMT),       # k odd: not tensor-core eligible
     (17, 17, 17, tn.TN_NODE_SIMT),
@@ -72,3 +77,17 @@ def test_circuits(rows, cols, cycles, n_open):
     tree = greedy_tree(net, 0)
     got, _ = run_gpu(net, tree)
     assert_close(got, _ref(net, tree), TOL_C64, f"circuit {rows}x{cols} d{cycles}")
+
+
+def test_gate_like_root_with_slices_accumulates():
+    # A[i, x, z] B[j, x, z] -> root[i, j], z sliced: k = 4 per slice, so the
+    # row-streaming kernel writes slice 0 and adds slices 1 and 2
+    rng = np.random.default_rng(12)
+    ext = [50001, 3, 4, 3]                 # i j x z
+    def rnd(shape):
+        return ((rng.standard_normal(shape) + 1j * rng.standard_normal(shape)) * 0.5).astype(np.complex64)
+    net = Network([[0, 2, 3], [1, 2, 3]], ext, [0, 1], [rnd((50001, 4, 3)), rnd((3, 4, 3))])
+    plan = tn.Plan.from_network(net, [(0, 1)], [3], "tf32x3", tn.TN_POLICY_NO_TINY)
+    assert plan.node_class(0) == tn.TN_NODE_STREAM and plan.num_slices == 3
+    got, _ = run_gpu(net, [(0, 1)], slices=[3], policy=tn.TN_POLICY_NO_TINY)
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced gate-like root")
