@@ -315,10 +315,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     tnbuild.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    net, tree, slices = load_workload(args.workload)
+    device_leaves = args.leaves == "device"
+    net, tree, slices = load_workload(args.workload, with_data=not device_leaves)
     plan = tn.Plan.from_network(net, tree, slices, args.precision)
     plan.bind_workspace(dev)
-    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    if device_leaves:
+        # seeded N(0, 1) complex entries drawn on the device (no host copy:
+        # single nodes of tens of GiB)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1234)
+        leaves = [torch.randn([net.extents[x] for x in t], dtype=torch.complex64, device=dev,
+                              generator=gen).mul_(2 ** 0.5) for t in net.tensors]
+    else:
+        leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
     out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
     stream = torch.cuda.current_stream(dev)
     ct = plan.flops
@@ -411,6 +420,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # End to end through the public API with host buffers: pinned host
     # leaves copied in, contraction, result copied out, every step.
+    if device_leaves:
+        e2e_none = {"value": None, "unit": "TFLOP/s", "note": "leaves drawn on the device"}
+        return finish(args, rank, world, net, plan, ct, units, value, ms, sharded, roofline, kernels,
+                      e2e_none, None, clk)
     host_leaves = [torch.from_numpy(np.ascontiguousarray(d)).pin_memory() for d in net.data]
     host_out = torch.empty(plan.out_shape, dtype=torch.complex64).pin_memory()
     dev_leaves = [torch.empty_like(h, device=dev) for h in host_leaves]
@@ -446,13 +459,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_leg(net, tree, slices, args.cpu_seconds)
+    finish(args, rank, world, net, plan, ct, units, value, ms, sharded, roofline, kernels, e2e, cpu,
+           clk)
 
+
+def finish(args, rank, world, net, plan, ct, units, value, ms, sharded, roofline, kernels, e2e, cpu,
+           clk):
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "strong" if sharded else "weak",
                 "vs_baseline": None, "dtype": "c64",
-                "data": "synthetic",
+                "data": "synthetic" + (" (leaves drawn on the device)" if args.leaves == "device" else ""),
                 "config": {"workload": net.name, "tensors": net.n_tensors, "C_t": ct,
                            "C_s": plan.peak, "slices": plan.num_slices, "precision": args.precision,
                            "l2": "flushed between timed steps (untimed 258 MiB fill)",
@@ -473,6 +491,8 @@ def main():
     ap.add_argument("--precision", default="tf32x3", choices=["tf32x3", "bf16", "fp32"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--leaves", choices=["host", "device"], default="host",
+                    help="device: draw the leaves on the GPU (no end-to-end or CPU leg)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
