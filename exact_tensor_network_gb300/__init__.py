@@ -55,7 +55,7 @@ class tn_launch_record(ctypes.Structure):
 
 
 KERNEL_NAMES = {0: "permute", 1: "simt", 2: "dense_tf32x3", 3: "dense_bf16", 4: "stream", 5: "tiny",
-                6: "reduce"}
+                6: "reduce", 7: "dense_tf32x3_3p"}
 
 
 class tn_slices(ctypes.Structure):
@@ -85,6 +85,7 @@ SIGNATURES = {
     "tn_execute": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_execute_static": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_set_replay": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_plan_set_three_products": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_execute_slices": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P, ctypes.c_uint64,
                                          ctypes.c_uint64]),
     "tn_plan_check": (ctypes.c_int, [_P]),
@@ -238,6 +239,10 @@ def tn_plan_set_replay(plan: int, enable: bool) -> None:
     _check(lib().tn_plan_set_replay(plan, 1 if enable else 0), plan)
 
 
+def tn_plan_set_three_products(plan: int, enable: bool) -> None:
+    _check(lib().tn_plan_set_three_products(plan, 1 if enable else 0), plan)
+
+
 def tn_plan_check(plan: int) -> None:
     _check(lib().tn_plan_check(plan), plan)
 
@@ -310,6 +315,10 @@ class Plan:
 
     def set_policy(self, policy: int) -> None:
         tn_plan_set_policy(self.handle, policy)
+        self._ws = None
+
+    def set_three_products(self, enable: bool) -> None:
+        tn_plan_set_three_products(self.handle, enable)
         self._ws = None
 
     def bind_workspace(self, device=None):

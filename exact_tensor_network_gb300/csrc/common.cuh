@@ -62,6 +62,19 @@ __device__ __forceinline__ int64_t tiled_offset(const PlanarTile &t, int64_t off
     return (((c >> sh) * t.rows + r) << sh) + (c & (t.kt - 1));
 }
 
+// One entry in FMT_GAUSS6 (see Fmt in plan.h): re, im and s = re + im, each
+// as tf32 hi and lo, planes `plane` entries apart.
+__device__ __forceinline__ void store_gauss6(float *p, int64_t plane, float2 v) {
+    const float sum = v.x + v.y;
+    const float rh = to_tf32(v.x), ih = to_tf32(v.y), sh = to_tf32(sum);
+    p[0] = rh;
+    p[plane] = ih;
+    p[2 * plane] = sh;
+    p[3 * plane] = to_tf32(v.x - rh);
+    p[4 * plane] = to_tf32(v.y - ih);
+    p[5 * plane] = to_tf32(sum - sh);
+}
+
 // Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
 // plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
 // destination.  Kernels instantiated per format keep one store path.
@@ -84,6 +97,8 @@ __device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t 
         p[plane] = ih;
         p[2 * plane] = to_tf32(v.x - rh);
         p[3 * plane] = to_tf32(v.y - ih);
+    } else if constexpr (FMT == FMT_GAUSS6) {
+        store_gauss6(static_cast<float *>(dst) + off, plane, v);
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         p[0] = __float2bfloat16_rn(v.x);
@@ -110,6 +125,8 @@ __device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plan
         p[plane] = ih;
         p[2 * plane] = to_tf32(v.x - rh);
         p[3 * plane] = to_tf32(v.y - ih);
+    } else if (fmt == FMT_GAUSS6) {
+        store_gauss6(static_cast<float *>(dst) + off, plane, v);
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         p[0] = __float2bfloat16_rn(v.x);
@@ -150,6 +167,22 @@ __device__ __forceinline__ void store_quad(void *dst, int32_t fmt, int64_t plane
         *reinterpret_cast<float4 *>(p + plane) = make_float4(ih[0], ih[1], ih[2], ih[3]);
         *reinterpret_cast<float4 *>(p + 2 * plane) = make_float4(rl[0], rl[1], rl[2], rl[3]);
         *reinterpret_cast<float4 *>(p + 3 * plane) = make_float4(il[0], il[1], il[2], il[3]);
+    } else if (fmt == FMT_GAUSS6) {
+        float *p = static_cast<float *>(dst) + off;
+        float q[6][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float sum = v[t].x + v[t].y;
+            q[0][t] = to_tf32(v[t].x);
+            q[1][t] = to_tf32(v[t].y);
+            q[2][t] = to_tf32(sum);
+            q[3][t] = to_tf32(v[t].x - q[0][t]);
+            q[4][t] = to_tf32(v[t].y - q[1][t]);
+            q[5][t] = to_tf32(sum - q[2][t]);
+        }
+#pragma unroll
+        for (int c = 0; c < 6; ++c)
+            *reinterpret_cast<float4 *>(p + c * plane) = make_float4(q[c][0], q[c][1], q[c][2], q[c][3]);
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         __nv_bfloat162 re0 = __halves2bfloat162(__float2bfloat16_rn(v[0].x), __float2bfloat16_rn(v[1].x));

@@ -378,7 +378,6 @@ tn_status cuda_fail(Plan *p, cudaError_t e, const char *what) {
 tn_status build_dense_maps(Plan *p) {
     p->dense_maps.clear();
     char *arena = static_cast<char *>(p->ws) + p->arena_off;
-    const bool bf16 = p->precision == TN_PREC_BF16;
     for (size_t s = 0; s < p->nodes.size(); ++s) {
         const NodePlan &nd = p->nodes[s];
         if (nd.cls != TN_NODE_DENSE) continue;
@@ -390,8 +389,9 @@ tn_status build_dense_maps(Plan *p) {
         std::memset(&dm, 0, sizeof(dm));
         dm.node = (int32_t)s;
         std::string err;
-        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, bf16, nd.ktiled != 0, &err) ||
-            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, bf16, nd.ktiled != 0, &err)) {
+        const int32_t fa = p->fmt[nd.a], fb = p->fmt[nd.b];
+        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, fa, nd.ktiled != 0, &err) ||
+            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, fb, nd.ktiled != 0, &err)) {
             p->last_error = "step " + std::to_string(s) + ": " + err;
             return TN_ECUDA;
         }
@@ -547,6 +547,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->out_tile = nd.out_tile;
                 d->ktiled = nd.ktiled;
                 d->bf16 = p->precision == TN_PREC_BF16;
+                d->three = nd.three_products;
                 d->status = status;
                 d->ksplit = nd.ksplit;
                 d->kchunk = nd.kchunk;
@@ -555,8 +556,10 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->tail_first = nd.tail_first;
                 d->tail_cnt = nd.tail_first >= 0 ? reinterpret_cast<int32_t *>(ws + nd.tail_cnt_off)
                                                  : nullptr;
-                const uint64_t in_b = d->bf16 ? 4 : 16;
-                rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16 : TN_KERNEL_DENSE_TF32X3, nd.step, flops,
+                const uint64_t in_b = fmt_bytes(p->fmt[nd.a]);
+                rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16
+                                  : d->three ? TN_KERNEL_DENSE_TF32X3_3P : TN_KERNEL_DENSE_TF32X3,
+                          nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +
                               fmt_bytes(nd.out_fmt) * nd.m * nd.n * (accumulate ? 2 : 1));
                 e = launch_dense(*d, p->num_sms, dag ? dag->begin() : stream);

@@ -16,6 +16,12 @@
 //     D1 = Ar * [Br; Bi]^T = [ArBr | ArBi],  D2 = Ai * [Br; Bi]^T = [AiBr | AiBi]
 // and the epilogue forms Cr = ArBr - AiBi, Ci = ArBi + AiBr.  In tf32x3
 // mode each product X*Y is hi*hi + hi*lo + lo*hi (lo*lo dropped).
+// Three-product mode (nodes bound by their arithmetic): operands also carry
+// the plane s = re + im, and three accumulators of 128 columns hold
+//     P1 = Ar Br,  P2 = Ai Bi,  P3 = (Ar + Ai)(Br + Bi)   (N = 128 each)
+// so that Cr = P1 - P2 and Ci = P3 - (P1 + P2): 9 instead of 12 tf32 MMAs
+// of 128 x 128 per k-step, in exchange for 24-byte operand entries and a
+// two-stage ring (96 KiB stages).
 //
 // Accuracy: the tensor core's fp32 accumulation loses a little on every
 // accumulation, and over thousands of k-steps that loss grows linearly with
@@ -62,26 +68,39 @@ constexpr int REGS_LOW = 56, REGS_HIGH = 224;
 static_assert(4 * 32 * REGS_LOW + DRAIN_WARPS * 32 * REGS_HIGH <= THREADS * 168,
               "register split exceeds the launch's registers");
 
-template <bool BF16>
+// Kernel modes: split tf32 with four real products per complex product,
+// bf16 operands (four products), split tf32 with three products.
+enum : int { MODE_TF32 = 0, MODE_BF16 = 1, MODE_TF32_3P = 2 };
+
+template <int MODE>
 struct Cfg {
-    static constexpr int A_PLANES = BF16 ? 2 : 4;
-    static constexpr int B_STACKS = BF16 ? 1 : 2;       // stacks of 256 rows
+    static constexpr bool BF16 = MODE == MODE_BF16;
+    static constexpr bool THREE = MODE == MODE_TF32_3P;
+    // planes per operand: [re, im] (bf16), [re_hi, im_hi, re_lo, im_lo],
+    // or [re_hi, im_hi, s_hi, re_lo, im_lo, s_lo] (s = re + im)
+    static constexpr int PLANES = BF16 ? 2 : THREE ? 6 : 4;
     static constexpr int KB = BF16 ? 32 : 16;           // complex k per stage
     static constexpr int K_INSTR = BF16 ? 16 : 8;       // k per MMA instruction
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
-    static constexpr int STAGE_BYTES = (A_PLANES + 2 * B_STACKS) * PLANE_TILE;
-    static constexpr int STAGES = BF16 ? 6 : 3;
+    static constexpr int STAGE_BYTES = 2 * PLANES * PLANE_TILE;
+    static constexpr int STAGES = BF16 ? 6 : THREE ? 2 : 3;
     // stages, alignment slack, barriers, then one 32 x 16 complex staging
     // tile per drain warp for coalesced stores
     static constexpr int STAGING = DRAIN_WARPS * 32 * 16 * 8;
     static constexpr int EP_BYTES = (int)((sizeof(EpTable) + 127) / 128 * 128);
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + STAGING + EP_BYTES;
+    // four products: B tiles stacked [Br; Bi] give N = 256 per MMA; three
+    // products: each real product is its own N = 128 MMA
+    static constexpr uint32_t MMA_N = THREE ? 128 : 256;
     // instruction descriptor: D f32, A/B tf32 (2) or bf16 (1), both K-major,
-    // N = 256, M = 128
+    // N = MMA_N, M = 128
     static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
-                                      ((BF16 ? 1u : 2u) << 10) | ((256u >> 3) << 17) |
+                                      ((BF16 ? 1u : 2u) << 10) | ((MMA_N >> 3) << 17) |
                                       ((128u >> 4) << 24);
 };
+static_assert(Cfg<MODE_TF32_3P>::SMEM <= 232448 && Cfg<MODE_TF32>::SMEM <= 232448 &&
+                  Cfg<MODE_BF16>::SMEM <= 232448,
+              "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -168,18 +187,18 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
            (static_cast<uint64_t>(4) << 61);
 }
 
-template <bool BF16>
+template <int MODE>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
-    if constexpr (BF16) {
+    if constexpr (MODE == MODE_BF16) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(a), "l"(b), "r"(Cfg<true>::IDESC), "r"(acc));
+            "l"(a), "l"(b), "r"(Cfg<MODE>::IDESC), "r"(acc));
     } else {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(a), "l"(b), "r"(Cfg<false>::IDESC), "r"(acc));
+            "l"(a), "l"(b), "r"(Cfg<MODE>::IDESC), "r"(acc));
     }
 }
 
@@ -277,9 +296,9 @@ __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t n
     nt = r / gm;
 }
 
-template <bool BF16>
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant__ DenseArgs a) {
-    using C = Cfg<BF16>;
+    using C = Cfg<MODE>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -352,16 +371,16 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     const int32_t kx = kb * C::KB;
                     // B planes in the same order land as the stacks [re; im]
                     // of each split part (hi stack, then lo stack)
-                    const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
+                    const uint32_t bbase = base + C::PLANES * PLANE_TILE;
                     if (a.ktiled) {
 #pragma unroll
-                        for (int p = 0; p < C::A_PLANES; ++p) {
+                        for (int p = 0; p < C::PLANES; ++p) {
                             tma_load_4d(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
                             tma_load_4d(bbase + p * PLANE_TILE, &a.tmB, bar, 0, yn, kb, p);
                         }
                     } else {
 #pragma unroll
-                        for (int p = 0; p < C::A_PLANES; ++p) {
+                        for (int p = 0; p < C::PLANES; ++p) {
                             tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
                             tma_load_3d(bbase + p * PLANE_TILE, &a.tmB, bar, kx, yn, p);
                         }
@@ -402,18 +421,32 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         }
                         fence_after();
                         const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
-                        const uint32_t bbase = base + C::A_PLANES * PLANE_TILE;
+                        const uint32_t bbase = base + C::PLANES * PLANE_TILE;
                         const bool first = kb == kb_beg;
 #pragma unroll
                         for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
                             const uint32_t off = kk * 32;   // 32 bytes of K per instruction
                             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                            if constexpr (BF16) {
+                            if constexpr (C::BF16) {
                                 const uint64_t ar = sdesc(base + off);
                                 const uint64_t ai = sdesc(base + PLANE_TILE + off);
                                 const uint64_t b = sdesc(bbase + off);
-                                mma<true>(d1, ar, b, acc);
-                                mma<true>(d2, ai, b, acc);
+                                mma<MODE>(d1, ar, b, acc);
+                                mma<MODE>(d2, ai, b, acc);
+                            } else if constexpr (C::THREE) {
+                                // D_c (128 columns at 128 c) = A_c B_c for the
+                                // components c = re, im, re + im
+#pragma unroll
+                                for (int c = 0; c < 3; ++c) {
+                                    const uint32_t dc = tmem + 128 * c;
+                                    const uint64_t ah = sdesc(base + c * PLANE_TILE + off);
+                                    const uint64_t al = sdesc(base + (c + 3) * PLANE_TILE + off);
+                                    const uint64_t bh = sdesc(bbase + c * PLANE_TILE + off);
+                                    const uint64_t bl = sdesc(bbase + (c + 3) * PLANE_TILE + off);
+                                    mma<MODE>(dc, al, bh, acc);
+                                    mma<MODE>(dc, ah, bl, 1);
+                                    mma<MODE>(dc, ah, bh, 1);
+                                }
                             } else {
                                 const uint64_t arh = sdesc(base + off);
                                 const uint64_t aih = sdesc(base + PLANE_TILE + off);
@@ -421,12 +454,12 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                 const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
                                 const uint64_t bh = sdesc(bbase + off);
                                 const uint64_t bl = sdesc(bbase + 2 * PLANE_TILE + off);
-                                mma<false>(d1, arl, bh, acc);
-                                mma<false>(d1, arh, bl, 1);
-                                mma<false>(d1, arh, bh, 1);
-                                mma<false>(d2, ail, bh, acc);
-                                mma<false>(d2, aih, bl, 1);
-                                mma<false>(d2, aih, bh, 1);
+                                mma<MODE>(d1, arl, bh, acc);
+                                mma<MODE>(d1, arh, bl, 1);
+                                mma<MODE>(d1, arh, bh, 1);
+                                mma<MODE>(d2, ail, bh, acc);
+                                mma<MODE>(d2, aih, bl, 1);
+                                mma<MODE>(d2, aih, bh, 1);
                             }
                         }
                         mma_commit(empty0 + 8 * stage);
@@ -506,16 +539,31 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const uint32_t col = h * 64 + cc * 16;
-                    float rr[16], ri[16], ir[16], ii[16];
-                    tmem_ld16(lane_base + col, rr);
-                    tmem_ld16(lane_base + 128 + col, ri);
-                    tmem_ld16(lane_base + 256 + col, ir);
-                    tmem_ld16(lane_base + 384 + col, ii);
-                    tmem_wait_ld();
+                    if constexpr (C::THREE) {
+                        // P1 = ArBr, P2 = AiBi, P3 = (Ar + Ai)(Br + Bi):
+                        // re = P1 - P2, im = P3 - (P1 + P2)
+                        float p1[16], p2[16], p3[16];
+                        tmem_ld16(lane_base + col, p1);
+                        tmem_ld16(lane_base + 128 + col, p2);
+                        tmem_ld16(lane_base + 256 + col, p3);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        sr[cc * 16 + c] += rr[c] - ii[c];
-                        si[cc * 16 + c] += ri[c] + ir[c];
+                        for (int c = 0; c < 16; ++c) {
+                            sr[cc * 16 + c] += p1[c] - p2[c];
+                            si[cc * 16 + c] += p3[c] - (p1[c] + p2[c]);
+                        }
+                    } else {
+                        float rr[16], ri[16], ir[16], ii[16];
+                        tmem_ld16(lane_base + col, rr);
+                        tmem_ld16(lane_base + 128 + col, ri);
+                        tmem_ld16(lane_base + 256 + col, ir);
+                        tmem_ld16(lane_base + 384 + col, ii);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            sr[cc * 16 + c] += rr[c] - ii[c];
+                            si[cc * 16 + c] += ri[c] + ir[c];
+                        }
                     }
                 }
                 fence_before();
@@ -670,32 +718,35 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
                                                 : tiles;
     const int grid = static_cast<int>(work < num_sms ? work : num_sms);
     if (grid <= 0) return cudaSuccess;
-    if (args.bf16) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(dense_kernel<true>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Cfg<true>::SMEM);
+    auto launch = [&](auto kernel, int smem, bool *attr) -> cudaError_t {
+        if (!*attr) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
-            attr = true;
+            *attr = true;
         }
-        dense_kernel<true><<<grid, THREADS, Cfg<true>::SMEM, stream>>>(args);
-    } else {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(dense_kernel<false>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 Cfg<false>::SMEM);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        dense_kernel<false><<<grid, THREADS, Cfg<false>::SMEM, stream>>>(args);
-    }
+        kernel<<<grid, THREADS, smem, stream>>>(args);
+        return cudaSuccess;
+    };
+    static bool attr_bf16 = false, attr_tf32 = false, attr_3p = false;
+    cudaError_t e;
+    if (args.bf16)
+        e = launch(dense_kernel<MODE_BF16>, Cfg<MODE_BF16>::SMEM, &attr_bf16);
+    else if (args.three)
+        e = launch(dense_kernel<MODE_TF32_3P>, Cfg<MODE_TF32_3P>::SMEM, &attr_3p);
+    else
+        e = launch(dense_kernel<MODE_TF32>, Cfg<MODE_TF32>::SMEM, &attr_tf32);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
+bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,
                         bool tiled, std::string *err) {
+    const bool bf16 = fmt == FMT_BF2;
+    const cuuint64_t planes = static_cast<cuuint64_t>(fmt_planes(fmt));
+    if (planes == 0) {
+        *err = "operand is not in a planar format";
+        return false;
+    }
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
         void *fn = nullptr;
@@ -713,7 +764,7 @@ bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_
         // planes of [k / kt][rows][kt]: dims (kt, rows, k / kt, planes)
         const cuuint64_t kt = ROW_BYTES / esz;
         const cuuint64_t d4[4] = {kt, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k) / kt,
-                                  static_cast<cuuint64_t>(bf16 ? 2 : 4)};
+                                  planes};
         const cuuint64_t s4[3] = {kt * esz, static_cast<cuuint64_t>(rows) * kt * esz,
                                   static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
         const cuuint32_t b4[4] = {static_cast<cuuint32_t>(kt), BM, 1, 1};
@@ -728,8 +779,7 @@ bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_
         }
         return true;
     }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(bf16 ? 2 : 4)};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows), planes};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * esz,
                                    static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(ROW_BYTES / esz), BM, 1};

@@ -115,6 +115,8 @@ cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
     const int64_t grid = tiles < 152 * 16 ? tiles : 152 * 16;
     if (args.out_fmt == FMT_SPLIT4)
         simt_node_kernel<FMT_SPLIT4><<<(unsigned)grid, kThreads, 0, stream>>>(args);
+    else if (args.out_fmt == FMT_GAUSS6)
+        simt_node_kernel<FMT_GAUSS6><<<(unsigned)grid, kThreads, 0, stream>>>(args);
     else if (args.out_fmt == FMT_BF2)
         simt_node_kernel<FMT_BF2><<<(unsigned)grid, kThreads, 0, stream>>>(args);
     else

@@ -238,6 +238,8 @@ cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
     dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
     if (args.out_fmt == FMT_SPLIT4)
         stream_node_kernel<FMT_SPLIT4><<<grid, kThreads, 0, stream>>>(args);
+    else if (args.out_fmt == FMT_GAUSS6)
+        stream_node_kernel<FMT_GAUSS6><<<grid, kThreads, 0, stream>>>(args);
     else if (args.out_fmt == FMT_BF2)
         stream_node_kernel<FMT_BF2><<<grid, kThreads, 0, stream>>>(args);
     else

@@ -83,8 +83,9 @@ cudaError_t launch_tiny_batch(const TinyLaunch &args, int ctas, cudaStream_t str
 cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream);
 
-// One tensor-core node.  A and B are planar (FMT_SPLIT4 or FMT_BF2) and
-// reached through 3-D TMA maps over (k, rows, plane).
+// One tensor-core node.  A and B are planar (FMT_SPLIT4, FMT_GAUSS6 or
+// FMT_BF2) and reached through 3-D TMA maps over (k, rows, plane), or 4-D
+// maps when K-tiled.
 struct DenseArgs {
     CUtensorMap tmA;
     CUtensorMap tmB;
@@ -94,7 +95,8 @@ struct DenseArgs {
     int32_t accumulate;
     int32_t out_fmt;
     PlanarTile out_tile;
-    int32_t bf16;         // operands are FMT_BF2 (else FMT_SPLIT4)
+    int32_t bf16;         // operands are FMT_BF2
+    int32_t three;        // operands are FMT_GAUSS6: three real products
     int32_t ktiled;       // operands K-tiled (4-D maps) rather than row-major (3-D)
     DevStatus *status;
     // split-K as in NodeArgs (kchunk a multiple of 256)
@@ -110,10 +112,10 @@ struct DenseArgs {
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream);
 
-// Build the TMA map of a planar operand: rows x k entries per plane.
-// Returns false (with a message) when the driver call is unavailable or
-// rejects the shape.
-bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, bool bf16,
+// Build the TMA map of a planar operand in format `fmt` (FMT_SPLIT4,
+// FMT_GAUSS6 or FMT_BF2): rows x k entries per plane.  Returns false (with a
+// message) when the driver call is unavailable or rejects the shape.
+bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,
                         bool tiled, std::string *err);
 
 constexpr int kPermBatch = 512;   // permutation jobs per launch

@@ -49,8 +49,18 @@ inline int32_t log2_exact(int64_t e) {
 //               tensor's row-major entries; hi = x rounded to tf32,
 //               lo = (x - hi) rounded to tf32 (16 bytes per entry)
 //   FMT_BF2:    two bf16 planes [re, im] (4 bytes per entry)
-enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2 };
-inline uint64_t fmt_bytes(int32_t f) { return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : 8; }
+//   FMT_GAUSS6: six fp32 planes [re_hi, im_hi, s_hi, re_lo, im_lo, s_lo]
+//               with s = re + im (rounded in fp32), split as in FMT_SPLIT4
+//               (24 bytes per entry): operands of nodes that form the
+//               complex product from three real products (see NodePlan)
+enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2, FMT_GAUSS6 = 3 };
+inline uint64_t fmt_bytes(int32_t f) {
+    return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : f == FMT_GAUSS6 ? 24 : 8;
+}
+// Planes of a planar format.
+inline int32_t fmt_planes(int32_t f) {
+    return f == FMT_SPLIT4 ? 4 : f == FMT_BF2 ? 2 : f == FMT_GAUSS6 ? 6 : 0;
+}
 
 // K-tiling of a planar operand.  The consumer reads the operand as a
 // row-major [rows][k] matrix; with kt > 0 each plane is stored as
@@ -66,7 +76,9 @@ struct PlanarTile {
 };
 
 // Entries per K tile for a planar format (64 bytes of one row).
-inline int32_t planar_kt(int32_t fmt) { return fmt == FMT_BF2 ? 32 : fmt == FMT_SPLIT4 ? 16 : 0; }
+inline int32_t planar_kt(int32_t fmt) {
+    return fmt == FMT_BF2 ? 32 : (fmt == FMT_SPLIT4 || fmt == FMT_GAUSS6) ? 16 : 0;
+}
 
 // Where a tensor lives during execution.
 enum PlaceKind : int32_t { PLACE_WS = 0, PLACE_LEAF = 1, PLACE_OUT = 2 };
@@ -131,6 +143,10 @@ struct NodePlan {
     // second to arrive adds the other half and stores.  -1: no tail split.
     int64_t tail_first;
     int64_t tail_cnt_off;
+    // dense class, tf32x3: the complex product from three real products
+    // (Ar Br, Ai Bi, (Ar + Ai)(Br + Bi)) instead of four; operands are
+    // FMT_GAUSS6
+    int32_t three_products;
 };
 
 // Tensor-core tile (complex entries), its drain warps (one tail-tile
@@ -274,6 +290,7 @@ struct Plan {
 
     // execution layout
     int32_t policy = TN_POLICY_AUTO;
+    int32_t three_products = 0;   // tn_plan_set_three_products
     uint64_t table_off = 0, table_bytes = 0;    // PermDesc table
     uint64_t arena_off = 0, arena_bytes = 0;
     uint64_t ws_bytes = 0;

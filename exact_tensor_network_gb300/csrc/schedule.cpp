@@ -65,6 +65,17 @@ uint64_t place_buffers(std::vector<Interval> &iv) {
 
 uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Three real products instead of four (FMT_GAUSS6 operands) where the node
+// stays bound by its arithmetic with 24-byte operand entries (flops per byte
+// well above the ratio of the tensor and HBM peaks, about 50) and its
+// operands stay below 64 GiB in that format.
+bool three_products_pay(const NodePlan &nd) {
+    const double m = (double)nd.m, n = (double)nd.n, k = (double)nd.k;
+    const double in_b = 24.0 * (m * k + n * k);
+    const double intensity = 8.0 * m * n * k / (in_b + 8.0 * m * n);
+    return nd.k >= 256 && intensity >= 64.0 && in_b <= 64.0 * (1ull << 30);
+}
+
 // Whether the sorted order of a full 32 x 16 block splits into runs of four
 // consecutive offsets starting at multiples of 4, with every block base and
 // the plane size multiples of 4 as well.  (K-tiling keeps such runs
@@ -170,8 +181,16 @@ tn_status layout_plan(Plan *p) {
     // 2. formats
     p->fmt.assign(n + S, FMT_C64);
     const int32_t dense_fmt = p->precision == TN_PREC_BF16 ? FMT_BF2 : FMT_SPLIT4;
-    for (const auto &nd : p->nodes)
-        if (nd.cls == TN_NODE_DENSE) p->fmt[nd.a] = p->fmt[nd.b] = dense_fmt;
+    for (auto &nd : p->nodes) {
+        nd.three_products = 0;
+        if (nd.cls != TN_NODE_DENSE) continue;
+        int32_t f = dense_fmt;
+        if (f == FMT_SPLIT4 && p->three_products && three_products_pay(nd)) {
+            f = FMT_GAUSS6;
+            nd.three_products = 1;
+        }
+        p->fmt[nd.a] = p->fmt[nd.b] = f;
+    }
     for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
     // K-tiling of tensor-core operands whose k fills whole tiles
     const PlanarTile untiled{0, 0, -1, 0};
@@ -179,7 +198,7 @@ tn_status layout_plan(Plan *p) {
     for (auto &nd : p->nodes) {
         nd.ktiled = 0;
         if (nd.cls != TN_NODE_DENSE) continue;
-        const int32_t kt = planar_kt(dense_fmt);
+        const int32_t kt = planar_kt(p->fmt[nd.a]);
         // rows of 16 KiB and more: 64-byte pieces would each cost a DRAM page
         if (nd.k % (uint64_t)kt != 0 || nd.k < 4096) continue;
         nd.ktiled = 1;

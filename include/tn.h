@@ -251,6 +251,23 @@ TN_API tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs
  * recorded graph is released either way. */
 TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);
 
+/*
+ * Complex products on the tensor cores in the split-tf32 precision: with
+ * `enable` = 1 a tensor-core node whose time is dominated by its arithmetic
+ * forms C = A B from three real products, Ar Br, Ai Bi and (Ar + Ai)(Br + Bi)
+ * (re = ArBr - AiBi, im = (Ar + Ai)(Br + Bi) - ArBr - AiBi), instead of four:
+ * 25 % fewer tensor-core operations, but operands of 24 instead of 16 bytes
+ * per entry, whose 96 KiB pipeline stages leave room for only two stages in
+ * shared memory; rounding errors of the imaginary part are about twice as
+ * large (still within the complex64 tolerance).  On a GB300 this is slower
+ * today (a 4096^3 node: 2.28 ms against 1.76 ms with four products), so the
+ * default is 0: always four products.  The pages do not describe this; it
+ * is the classic three-multiplication complex product.  Re-plans the layout
+ * (like tn_plan_set_policy): bind the workspace again afterwards.
+ * Errors: TN_EINVAL (NULL plan).
+ */
+TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
+
 /* After the stream has been synchronised: read and clear the device status
  * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or
  * TN_ETIMEOUT (a bounded wait inside a kernel gave up). */
@@ -266,7 +283,8 @@ enum {
     TN_KERNEL_DENSE_BF16 = 3,   /* tcgen05 node kernel, bf16 operands */
     TN_KERNEL_STREAM = 4,       /* bandwidth-bound node kernel */
     TN_KERNEL_TINY = 5,         /* batched tiny-node kernel */
-    TN_KERNEL_REDUCE = 6        /* ordered sum of split-K partials */
+    TN_KERNEL_REDUCE = 6,       /* ordered sum of split-K partials */
+    TN_KERNEL_DENSE_TF32X3_3P = 7 /* tcgen05 node kernel, split tf32, three real products */
 };
 
 /* One kernel launch of a profiled tn_execute.  flops = 8 m n k of the

@@ -262,3 +262,27 @@ def test_dense_tail_tiles_split_in_k_halves(m, n, k, precision, tol):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
     assert_close(outs[2].astype(np.complex128), _ref(net, [(0, 1)]), tol,
                  f"tail halves {m}x{n}x{k} {precision}")
+
+
+@pytest.mark.parametrize("m,n,k", [(512, 1024, 2048), (300, 700, 1040), (512, 512, 8192)])
+def test_three_product_nodes(m, n, k):
+    """Nodes bound by their arithmetic form the complex product from three
+    real products (Ar Br, Ai Bi, (Ar + Ai)(Br + Bi)); with that turned off,
+    from four.  Both match the oracle (k = 8192: K-tiled six-plane operands)."""
+    import torch
+    net = node_network(m, n, k, m + 3 * n + 7 * k)
+    ref = _ref(net, [(0, 1)])
+    dev = torch.device("cuda:0")
+    for three, kernel in ((True, "dense_tf32x3_3p"), (False, "dense_tf32x3")):
+        plan = tn.Plan.from_network(net, [(0, 1)], (), "tf32x3", NT)
+        plan.set_three_products(three)
+        assert plan.node_class(0) == tn.TN_NODE_DENSE
+        leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+        out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
+        plan.set_profiling(True)
+        plan.execute(leaves, out)
+        torch.cuda.synchronize(dev)
+        plan.check()
+        assert kernel in [r["kernel"] for r in plan.profile()]
+        assert_close(out.cpu().numpy().astype(np.complex128), ref, TOL_C64,
+                     f"{m}x{n}x{k} three products={three}")
