@@ -10,6 +10,34 @@
 
 namespace tn {
 
+// Programmatic dependent launch.  Every kernel is launched with programmatic
+// stream serialization (launch_pdl), signals at its start that the next
+// kernel on the stream may be scheduled (its CTAs then wait on the SMs this
+// grid leaves free), and waits before its first global memory access until
+// the previous grid has completed and its writes are visible.  The wait is a
+// hardware dependency (no spin); a dependent grid is only launched once every
+// CTA of this grid has started, so waiting CTAs never starve this grid.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Offset of index i under a separable output layout: split i mixed-radix
 // over the runs (run 0 most significant) and sum digit * stride.
 // Power-of-two extents use shifts and masks; other extents divide (32-bit

@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -334,6 +335,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    // barriers and TMEM are set up (shared memory only); global memory after
+    // the previous grid on the stream has completed
+    pdl_wait();
 
     const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + BN - 1) / BN;
     const int64_t tiles = mtiles * ntiles;
@@ -724,8 +728,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
             if (e != cudaSuccess) return e;
             *attr = true;
         }
-        kernel<<<grid, THREADS, smem, stream>>>(args);
-        return cudaSuccess;
+        return launch_pdl(kernel, dim3(grid), dim3(THREADS), (size_t)smem, stream, args);
     };
     static bool attr_bf16 = false, attr_tf32 = false, attr_3p = false;
     cudaError_t e;
@@ -735,8 +738,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
         e = launch(dense_kernel<MODE_TF32_3P>, Cfg<MODE_TF32_3P>::SMEM, &attr_3p);
     else
         e = launch(dense_kernel<MODE_TF32>, Cfg<MODE_TF32>::SMEM, &attr_tf32);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return e;
 }
 
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,

@@ -18,6 +18,8 @@ constexpr int kThreads = 256;
 constexpr int kItems = 4;
 
 __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant__ PermLaunch a) {
+    pdl_trigger();
+    pdl_wait();
     // Find this CTA's job (uniform across the CTA).
     int lo = 0, hi = a.njobs - 1;
     const int b = blockIdx.x;
@@ -71,8 +73,7 @@ int permute_ctas(int64_t size) {
 
 cudaError_t launch_permute(const PermLaunch &args, int total_ctas, cudaStream_t stream) {
     if (args.njobs <= 0) return cudaSuccess;
-    permute_kernel<<<total_ctas, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(permute_kernel, dim3(total_ctas), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace tn

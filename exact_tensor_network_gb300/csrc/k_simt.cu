@@ -26,6 +26,8 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_constant__ NodeArgs a) {
     __shared__ float2 As[BK][BM + 1];
     __shared__ float2 Bs[BK][BN + 1];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     const int tx = tid % (BN / TN), ty = tid / (BN / TN);
     const int64_t mt = (a.m + BM - 1) / BM, nt = (a.n + BN - 1) / BN;
@@ -114,14 +116,12 @@ cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
     const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN) * args.ksplit;
     const int64_t grid = tiles < 152 * 16 ? tiles : 152 * 16;
     if (args.out_fmt == FMT_SPLIT4)
-        simt_node_kernel<FMT_SPLIT4><<<(unsigned)grid, kThreads, 0, stream>>>(args);
+        return launch_pdl(simt_node_kernel<FMT_SPLIT4>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_GAUSS6)
-        simt_node_kernel<FMT_GAUSS6><<<(unsigned)grid, kThreads, 0, stream>>>(args);
+        return launch_pdl(simt_node_kernel<FMT_GAUSS6>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_BF2)
-        simt_node_kernel<FMT_BF2><<<(unsigned)grid, kThreads, 0, stream>>>(args);
-    else
-        simt_node_kernel<FMT_C64><<<(unsigned)grid, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+        return launch_pdl(simt_node_kernel<FMT_BF2>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
+    return launch_pdl(simt_node_kernel<FMT_C64>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace tn

@@ -22,6 +22,8 @@ constexpr int kThreads = 256;
 template <int FMT>
 __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_constant__ StreamArgs a) {
     __shared__ float2 Bs[kStreamMaxN * kStreamKc];
+    pdl_trigger();
+    pdl_wait();
     const int s = blockIdx.y;
     const int64_t k0 = (int64_t)s * a.kchunk;
     const int64_t k1 = min(a.k, k0 + a.kchunk);
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
     // row-major [m, n] outputs: each warp's 32 rows are one contiguous run,
     // staged here and stored by consecutive lanes
     __shared__ float2 Cs[kThreads / 32][32 * (kStreamMaxN + 1)];
+    pdl_trigger();
+    pdl_wait();
     const int n = (int)a.n, k = (int)a.k;
     for (int e = threadIdx.x; e < n * K; e += kThreads) {
         const int j = e / K, kk = e - j * K;
@@ -195,6 +199,8 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
 }
 
 __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_constant__ ReduceArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t mn = a.m * a.n;
     for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < mn;
          e += (int64_t)gridDim.x * kThreads) {
@@ -226,33 +232,31 @@ cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
         int64_t blocks = (args.m + pass - 1) / pass;
         if (blocks > 152 * 8) blocks = 152 * 8;
         if (blocks < 1) blocks = 1;
+        cudaError_t e;
         switch (K) {
-            case 2: stream_rows_kernel<2><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
-            case 4: stream_rows_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
-            case 8: stream_rows_kernel<8><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
-            default: stream_rows_kernel<16><<<(unsigned)blocks, kThreads, 0, stream>>>(a2); break;
+            case 2: e = launch_pdl(stream_rows_kernel<2>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a2); break;
+            case 4: e = launch_pdl(stream_rows_kernel<4>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a2); break;
+            case 8: e = launch_pdl(stream_rows_kernel<8>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a2); break;
+            default: e = launch_pdl(stream_rows_kernel<16>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a2); break;
         }
-        return cudaGetLastError();
+        return e;
     }
     const int64_t blocks = (args.m + args.rows_per_cta - 1) / args.rows_per_cta;
     dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
     if (args.out_fmt == FMT_SPLIT4)
-        stream_node_kernel<FMT_SPLIT4><<<grid, kThreads, 0, stream>>>(args);
+        return launch_pdl(stream_node_kernel<FMT_SPLIT4>, grid, dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_GAUSS6)
-        stream_node_kernel<FMT_GAUSS6><<<grid, kThreads, 0, stream>>>(args);
+        return launch_pdl(stream_node_kernel<FMT_GAUSS6>, grid, dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_BF2)
-        stream_node_kernel<FMT_BF2><<<grid, kThreads, 0, stream>>>(args);
-    else
-        stream_node_kernel<FMT_C64><<<grid, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+        return launch_pdl(stream_node_kernel<FMT_BF2>, grid, dim3(kThreads), 0, stream, args);
+    return launch_pdl(stream_node_kernel<FMT_C64>, grid, dim3(kThreads), 0, stream, args);
 }
 
 cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream) {
     const int64_t mn = args.m * args.n;
     int64_t blocks = (mn + kThreads - 1) / kThreads;
     if (blocks > 152 * 8) blocks = 152 * 8;
-    splitk_reduce_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace tn

@@ -22,6 +22,8 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_constant__ TinyLaunch a) {
+    pdl_trigger();
+    pdl_wait();
     // this CTA's node: last descriptor whose cta_base <= blockIdx.x
     int lo = a.first, hi = a.first + a.count - 1;
     const int b = blockIdx.x;
@@ -91,8 +93,7 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
 
 cudaError_t launch_tiny_batch(const TinyLaunch &args, int ctas, cudaStream_t stream) {
     if (ctas <= 0) return cudaSuccess;
-    tiny_batch_kernel<<<ctas, kThreads, 0, stream>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(tiny_batch_kernel, dim3(ctas), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace tn
