@@ -66,14 +66,22 @@ void choose_split(const Plan &p, NodePlan &nd) {
     nd.ksplit = 1;
     nd.kchunk = (int64_t)nd.k;
     nd.swap = 0;
+    nd.narrow = 0;
     nd.tail_first = -1;
     uint64_t units = 0, outs = nd.m * nd.n;
     if (nd.cls == TN_NODE_DENSE) {
-        // tensor-core tiles are 128 x 128 and one CTA runs per SM; splits are
-        // whole multiples of the 256-entry accumulation chunk
+        // a side of at most 64 goes to N (operands swapped when it is m) and
+        // the node runs 128 x 64 tiles
+        if (std::min(nd.m, nd.n) <= (uint64_t)(kDenseBN / 2)) {
+            nd.swap = nd.m < nd.n ? 1 : 0;
+            nd.narrow = 1;
+        }
+        // tensor-core tiles are 128 x 128 (or 128 x 64) and one CTA runs per
+        // SM; splits are whole multiples of the 256-entry accumulation chunk
         const uint64_t tiles = dense_tiles(nd);
         const uint64_t sms = kTargetCtas / 2;
         if (tiles >= sms) {
+            if (nd.narrow) return;   // no tail split on narrow tiles
             // a last wave at most half full runs its tiles as two k halves:
             // it then takes half a tile's time instead of a whole one
             const uint64_t tail = tiles % sms;
@@ -389,9 +397,15 @@ tn_status build_dense_maps(Plan *p) {
         std::memset(&dm, 0, sizeof(dm));
         dm.node = (int32_t)s;
         std::string err;
-        const int32_t fa = p->fmt[nd.a], fb = p->fmt[nd.b];
-        if (!encode_operand_map(&dm.a, arena + nd.pa.off, (int64_t)nd.m, (int64_t)nd.k, fa, nd.ktiled != 0, &err) ||
-            !encode_operand_map(&dm.b, arena + nd.pb.off, (int64_t)nd.n, (int64_t)nd.k, fb, nd.ktiled != 0, &err)) {
+        // kernel view: A = the operand with the rows, B = the one with the
+        // columns (swapped when the node runs C^T = B A^T)
+        const Place &pa = nd.swap ? nd.pb : nd.pa, &pb = nd.swap ? nd.pa : nd.pb;
+        const int32_t fa = p->fmt[nd.swap ? nd.b : nd.a], fb = p->fmt[nd.swap ? nd.a : nd.b];
+        const int32_t brows = nd.narrow ? (int32_t)(kDenseBN / 2) : (int32_t)kDenseBN;
+        if (!encode_operand_map(&dm.a, arena + pa.off, (int64_t)dense_rows(nd), (int64_t)nd.k, fa,
+                                nd.ktiled != 0, (int32_t)kDenseBM, &err) ||
+            !encode_operand_map(&dm.b, arena + pb.off, (int64_t)dense_cols(nd), (int64_t)nd.k, fb,
+                                nd.ktiled != 0, brows, &err)) {
             p->last_error = "step " + std::to_string(s) + ": " + err;
             return TN_ECUDA;
         }
@@ -537,11 +551,14 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 std::memcpy(&d->tmA, &dm.a, sizeof(CUtensorMap));
                 std::memcpy(&d->tmB, &dm.b, sizeof(CUtensorMap));
                 d->C = resolve(nd.pc);
-                d->m = (int64_t)nd.m;
-                d->n = (int64_t)nd.n;
+                // kernel view: rows and columns after the operand swap (the
+                // maps were built for that view)
+                d->m = (int64_t)dense_rows(nd);
+                d->n = (int64_t)dense_cols(nd);
                 d->k = (int64_t)nd.k;
-                d->lm = nd.lm;
-                d->ln = nd.ln;
+                d->lm = nd.swap ? nd.ln : nd.lm;
+                d->ln = nd.swap ? nd.lm : nd.ln;
+                d->narrow = nd.narrow;
                 d->accumulate = accumulate;
                 d->out_fmt = nd.out_fmt;
                 d->out_tile = nd.out_tile;
@@ -618,7 +635,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             if (e == cudaSuccess && nd.ksplit > 1) {
                 ReduceArgs r;
                 std::memset(&r, 0, sizeof(r));
-                const bool sw = nd.cls == TN_NODE_STREAM && nd.swap;
+                const bool sw = nd.swap != 0;   // partials are [split][rows][cols] of the kernel's view
                 r.part = reinterpret_cast<const float2 *>(arena + nd.part.off);
                 r.C = resolve(nd.pc);
                 r.m = (int64_t)(sw ? nd.n : nd.m);

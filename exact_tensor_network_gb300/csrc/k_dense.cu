@@ -84,20 +84,28 @@ struct Cfg {
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
     static constexpr int STAGE_BYTES = 2 * PLANES * PLANE_TILE;
     static constexpr int STAGES = BF16 ? 6 : THREE ? 2 : 3;
+    // the ring holds 192 KiB in every mode; narrow tiles (B of 64 rows) fit
+    // more of their smaller stages into it
+    static constexpr int RING = STAGES * STAGE_BYTES;
+    static constexpr int NARROW_STAGE_BYTES = PLANES * PLANE_TILE + PLANES * (PLANE_TILE / 2);
+    static constexpr int NARROW_STAGES = RING / NARROW_STAGE_BYTES;
     // stages, alignment slack, barriers, then one 32 x 16 complex staging
     // tile per drain warp for coalesced stores
     static constexpr int STAGING = DRAIN_WARPS * 32 * 16 * 8;
     static constexpr int EP_BYTES = (int)((sizeof(EpTable) + 127) / 128 * 128);
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + STAGING + EP_BYTES;
+    static constexpr int SMEM = RING + 1024 + 256 + STAGING + EP_BYTES;
     // four products: B tiles stacked [Br; Bi] give N = 256 per MMA; three
     // products: each real product is its own N = 128 MMA
     static constexpr uint32_t MMA_N = THREE ? 128 : 256;
-    // instruction descriptor: D f32, A/B tf32 (2) or bf16 (1), both K-major,
-    // N = MMA_N, M = 128
-    static constexpr uint32_t IDESC = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
-                                      ((BF16 ? 1u : 2u) << 10) | ((MMA_N >> 3) << 17) |
-                                      ((128u >> 4) << 24);
+    // instruction descriptor without N: D f32, A/B tf32 (2) or bf16 (1),
+    // both K-major, M = 128; idesc(N) adds N
+    static constexpr uint32_t IDESC_BASE = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
+                                           ((BF16 ? 1u : 2u) << 10) | ((128u >> 4) << 24);
+    static constexpr uint32_t idesc(uint32_t n) { return IDESC_BASE | ((n >> 3) << 17); }
 };
+constexpr int MAX_STAGES = 8;   // barrier slots (narrow bf16 tiles: 8 stages)
+static_assert(Cfg<MODE_BF16>::NARROW_STAGES <= MAX_STAGES && Cfg<MODE_TF32>::NARROW_STAGES <= MAX_STAGES,
+              "barrier slots");
 static_assert(Cfg<MODE_TF32_3P>::SMEM <= 232448 && Cfg<MODE_TF32>::SMEM <= 232448 &&
                   Cfg<MODE_BF16>::SMEM <= 232448,
               "shared memory per CTA");
@@ -188,17 +196,17 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 }
 
 template <int MODE>
-__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc, uint32_t idesc) {
     if constexpr (MODE == MODE_BF16) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(a), "l"(b), "r"(Cfg<MODE>::IDESC), "r"(acc));
+            "l"(a), "l"(b), "r"(idesc), "r"(acc));
     } else {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(a), "l"(b), "r"(Cfg<MODE>::IDESC), "r"(acc));
+            "l"(a), "l"(b), "r"(idesc), "r"(acc));
     }
 }
 
@@ -302,19 +310,25 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    // narrow tiles: B of 64 rows, smaller stages, more of them, MMA N = 128
+    const bool narrow = a.narrow && !C::THREE;
+    const int stages = narrow ? C::NARROW_STAGES : C::STAGES;
+    const int stage_bytes = narrow ? C::NARROW_STAGE_BYTES : C::STAGE_BYTES;
+    const int bn = narrow ? BN / 2 : BN;
+    const int b_plane = narrow ? PLANE_TILE / 2 : PLANE_TILE;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING);
     const uint32_t full0 = smem_u32(bars);
-    const uint32_t empty0 = smem_u32(bars + C::STAGES);
-    const uint32_t tmem_full = smem_u32(bars + 2 * C::STAGES);
-    const uint32_t tmem_empty = smem_u32(bars + 2 * C::STAGES + 1);
-    const uint32_t drain = smem_u32(bars + 2 * C::STAGES + 2);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * C::STAGES + 3);
+    const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
+    const uint32_t tmem_full = smem_u32(bars + 2 * MAX_STAGES);
+    const uint32_t tmem_empty = smem_u32(bars + 2 * MAX_STAGES + 1);
+    const uint32_t drain = smem_u32(bars + 2 * MAX_STAGES + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     pdl_trigger();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     // the previous grid on the stream has completed
     pdl_wait();
 
-    const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + BN - 1) / BN;
+    const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + bn - 1) / bn;
     const int64_t tiles = mtiles * ntiles;
     const int nkb = static_cast<int>((a.k + C::KB - 1) / C::KB);
     // work item w = (tile w / ksplit, k split w % ksplit); a split covers kbs
@@ -362,7 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
                 int64_t mt, nt;
                 tile_coords(it.t, mtiles, ntiles, mt, nt);
-                const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * BN);
+                const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * bn);
                 const int kb0 = it.kb0, kb1 = it.kb1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
@@ -370,8 +384,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         break;
                     }
                     const uint32_t bar = full0 + 8 * stage;
-                    mbar_expect_tx(bar, C::STAGE_BYTES);
-                    const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
+                    mbar_expect_tx(bar, stage_bytes);
+                    const uint32_t base = smem_u32(smem + stage * stage_bytes);
                     const int32_t kx = kb * C::KB;
                     // B planes in the same order land as the stacks [re; im]
                     // of each split part (hi stack, then lo stack)
@@ -380,30 +394,32 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 #pragma unroll
                         for (int p = 0; p < C::PLANES; ++p) {
                             tma_load_4d(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
-                            tma_load_4d(bbase + p * PLANE_TILE, &a.tmB, bar, 0, yn, kb, p);
+                            tma_load_4d(bbase + p * b_plane, &a.tmB, bar, 0, yn, kb, p);
                         }
                     } else {
 #pragma unroll
                         for (int p = 0; p < C::PLANES; ++p) {
                             tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
-                            tma_load_3d(bbase + p * PLANE_TILE, &a.tmB, bar, kx, yn, p);
+                            tma_load_3d(bbase + p * b_plane, &a.tmB, bar, kx, yn, p);
                         }
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::STAGES) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
             if (!ok) {
-                for (int s = 0; s < C::STAGES; ++s)
+                for (int s = 0; s < stages; ++s)
                     if (issued & (1u << s)) drain_wait(full0 + 8 * s, (last_par >> s) & 1);
             }
         } else if (warp == 1 && lane == 0) {
             // ---- MMA issuer ----
-            const uint32_t d1 = tmem, d2 = tmem + 256;
+            // four products: D1 = Ar [Br; Bi], D2 = Ai [Br; Bi], 2 bn columns each
+            const uint32_t d1 = tmem, d2 = tmem + 2 * bn;
+            const uint32_t idesc = C::idesc(C::THREE ? 128u : (uint32_t)(2 * bn));
             uint32_t stage = 0, phase = 0, tphase = 0;
             bool ok = true;
             for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                             break;
                         }
                         fence_after();
-                        const uint32_t base = smem_u32(smem + stage * C::STAGE_BYTES);
+                        const uint32_t base = smem_u32(smem + stage * stage_bytes);
                         const uint32_t bbase = base + C::PLANES * PLANE_TILE;
                         const bool first = kb == kb_beg;
 #pragma unroll
@@ -435,8 +451,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                 const uint64_t ar = sdesc(base + off);
                                 const uint64_t ai = sdesc(base + PLANE_TILE + off);
                                 const uint64_t b = sdesc(bbase + off);
-                                mma<MODE>(d1, ar, b, acc);
-                                mma<MODE>(d2, ai, b, acc);
+                                mma<MODE>(d1, ar, b, acc, idesc);
+                                mma<MODE>(d2, ai, b, acc, idesc);
                             } else if constexpr (C::THREE) {
                                 // D_c (128 columns at 128 c) = A_c B_c for the
                                 // components c = re, im, re + im
@@ -447,9 +463,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                     const uint64_t al = sdesc(base + (c + 3) * PLANE_TILE + off);
                                     const uint64_t bh = sdesc(bbase + c * PLANE_TILE + off);
                                     const uint64_t bl = sdesc(bbase + (c + 3) * PLANE_TILE + off);
-                                    mma<MODE>(dc, al, bh, acc);
-                                    mma<MODE>(dc, ah, bl, 1);
-                                    mma<MODE>(dc, ah, bh, 1);
+                                    mma<MODE>(dc, al, bh, acc, idesc);
+                                    mma<MODE>(dc, ah, bl, 1, idesc);
+                                    mma<MODE>(dc, ah, bh, 1, idesc);
                                 }
                             } else {
                                 const uint64_t arh = sdesc(base + off);
@@ -457,17 +473,17 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                 const uint64_t arl = sdesc(base + 2 * PLANE_TILE + off);
                                 const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
                                 const uint64_t bh = sdesc(bbase + off);
-                                const uint64_t bl = sdesc(bbase + 2 * PLANE_TILE + off);
-                                mma<MODE>(d1, arl, bh, acc);
-                                mma<MODE>(d1, arh, bl, 1);
-                                mma<MODE>(d1, arh, bh, 1);
-                                mma<MODE>(d2, ail, bh, acc);
-                                mma<MODE>(d2, aih, bl, 1);
-                                mma<MODE>(d2, aih, bh, 1);
+                                const uint64_t bl = sdesc(bbase + 2 * b_plane + off);
+                                mma<MODE>(d1, arl, bh, acc, idesc);
+                                mma<MODE>(d1, arh, bl, 1, idesc);
+                                mma<MODE>(d1, arh, bh, 1, idesc);
+                                mma<MODE>(d2, ail, bh, acc, idesc);
+                                mma<MODE>(d2, aih, bl, 1, idesc);
+                                mma<MODE>(d2, aih, bh, 1, idesc);
                             }
                         }
                         mma_commit(empty0 + 8 * stage);
-                        if (++stage == C::STAGES) {
+                        if (++stage == stages) {
                             stage = 0;
                             phase ^= 1;
                         }
@@ -486,6 +502,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         // ---- drain: TMEM chunks -> fp32 running sums -> global ----
         const int q = warp & 3;                 // TMEM lane quarter (rows)
         const int h = (warp - 4) >> 2;          // column half of the tile
+        const int half_cols = bn / 2;           // columns per drain warp (64, narrow 32)
+        const int ncc = bn / 32;                // 16-column blocks per drain warp
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const int64_t plane = a.m * a.n;
         const int nl = a.ln.nrun;
@@ -502,10 +520,10 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const int32_t fmt = plain ? (int32_t)FMT_C64 : a.out_fmt;
         const int32_t accum = plain ? 0 : a.accumulate;
         float2 *stage_tile = reinterpret_cast<float2 *>(
-            smem + C::STAGES * C::STAGE_BYTES + 256 + (warp - 4) * 32 * 16 * 8);
+            smem + C::RING + 256 + (warp - 4) * 32 * 16 * 8);
         EpTable *ep_s = nullptr;
         if (a.ep && !plain) {
-            ep_s = reinterpret_cast<EpTable *>(smem + C::STAGES * C::STAGE_BYTES + 256 + C::STAGING);
+            ep_s = reinterpret_cast<EpTable *>(smem + C::RING + 256 + C::STAGING);
             const uint32_t *src = reinterpret_cast<const uint32_t *>(a.ep);
             uint32_t *dstw = reinterpret_cast<uint32_t *>(ep_s);
             for (int x = threadIdx.x - 128; x < (int)(sizeof(EpTable) / 4); x += DRAIN_WARPS * 32)
@@ -542,7 +560,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 fence_after();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t col = h * 64 + cc * 16;
+                    if (cc >= ncc) break;   // warp-uniform (narrow tiles: 2 blocks)
+                    const uint32_t col = h * half_cols + cc * 16;
                     if constexpr (C::THREE) {
                         // P1 = ArBr, P2 = AiBi, P3 = (Ar + Ai)(Br + Bi):
                         // re = P1 - P2, im = P3 - (P1 + P2)
@@ -559,9 +578,9 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     } else {
                         float rr[16], ri[16], ir[16], ii[16];
                         tmem_ld16(lane_base + col, rr);
-                        tmem_ld16(lane_base + 128 + col, ri);
-                        tmem_ld16(lane_base + 256 + col, ir);
-                        tmem_ld16(lane_base + 384 + col, ii);
+                        tmem_ld16(lane_base + bn + col, ri);
+                        tmem_ld16(lane_base + 2 * bn + col, ir);
+                        tmem_ld16(lane_base + 3 * bn + col, ii);
                         tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
@@ -616,8 +635,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             // xor-swizzled by row) and every store loop reads it from there,
             // so the loops stay rolled and the kernel's code stays small.
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int64_t j0 = nt * BN + h * 64 + cc * 16;
+            for (int cc = 0; cc < ncc; ++cc) {
+                const int64_t j0 = nt * bn + h * half_cols + cc * 16;
                 if (j0 >= a.n) break;   // warp-uniform
                 stage_block(stage_tile, lane, sr, si, cc);
                 if (other) {
@@ -716,7 +735,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream) {
-    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + BN - 1) / BN);
+    const int64_t bn = (args.narrow && !args.three) ? BN / 2 : BN;
+    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + bn - 1) / bn);
     const int64_t work = args.ksplit > 1          ? tiles * args.ksplit
                          : args.tail_first >= 0 ? args.tail_first + 2 * (tiles - args.tail_first)
                                                 : tiles;
@@ -742,7 +762,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
 }
 
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,
-                        bool tiled, std::string *err) {
+                        bool tiled, int32_t box_rows, std::string *err) {
     const bool bf16 = fmt == FMT_BF2;
     const cuuint64_t planes = static_cast<cuuint64_t>(fmt_planes(fmt));
     if (planes == 0) {
@@ -769,7 +789,7 @@ bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_
                                   planes};
         const cuuint64_t s4[3] = {kt * esz, static_cast<cuuint64_t>(rows) * kt * esz,
                                   static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
-        const cuuint32_t b4[4] = {static_cast<cuuint32_t>(kt), BM, 1, 1};
+        const cuuint32_t b4[4] = {static_cast<cuuint32_t>(kt), static_cast<cuuint32_t>(box_rows), 1, 1};
         const cuuint32_t e4[4] = {1, 1, 1, 1};
         CUresult r4 = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                              4, const_cast<void *>(base), d4, s4, b4, e4,
@@ -784,7 +804,7 @@ bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows), planes};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k) * esz,
                                    static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(k) * esz};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ROW_BYTES / esz), BM, 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(ROW_BYTES / esz), static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                         3, const_cast<void *>(base), dims, strides, box, estr,

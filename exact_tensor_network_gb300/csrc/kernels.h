@@ -97,6 +97,7 @@ struct DenseArgs {
     PlanarTile out_tile;
     int32_t bf16;         // operands are FMT_BF2
     int32_t three;        // operands are FMT_GAUSS6: three real products
+    int32_t narrow;       // 128 x 64 tiles (B boxes of 64 rows, MMA N = 128)
     int32_t ktiled;       // operands K-tiled (4-D maps) rather than row-major (3-D)
     DevStatus *status;
     // split-K as in NodeArgs (kchunk a multiple of 256)
@@ -115,8 +116,10 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
 // Build the TMA map of a planar operand in format `fmt` (FMT_SPLIT4,
 // FMT_GAUSS6 or FMT_BF2): rows x k entries per plane.  Returns false (with a
 // message) when the driver call is unavailable or rejects the shape.
+// A TMA box is 64 bytes of k by box_rows rows (128, or 64 for the B side of
+// a narrow node).
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,
-                        bool tiled, std::string *err);
+                        bool tiled, int32_t box_rows, std::string *err);
 
 constexpr int kPermBatch = 512;   // permutation jobs per launch
 

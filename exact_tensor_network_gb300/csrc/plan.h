@@ -132,7 +132,13 @@ struct NodePlan {
     int32_t ksplit;
     int64_t kchunk;
     Place part;
-    int32_t swap;           // stream class: operands swapped so B is the small side
+    // stream and dense classes: operands swapped (the kernel computes
+    // C^T = B A^T, rows n and columns m, through the swapped layouts) so that
+    // B is the small side
+    int32_t swap;
+    // dense class: tiles of 128 x 64 (n <= 64 after the swap): B stacked
+    // [Br; Bi] fills one N = 128 MMA instead of half an N = 256 one
+    int32_t narrow;
     // dense class: byte offset (from the workspace start) of the node's
     // address-order store table (EpTable), or -1 when it has none
     int64_t ep_off;
@@ -154,8 +160,12 @@ struct NodePlan {
 // partials, or the two halves of every tail tile.
 constexpr int64_t kDenseBM = 128, kDenseBN = 128;
 constexpr uint64_t kDrainWarps = 8;
+// Kernel view of a dense node: rows and columns after the operand swap.
+inline uint64_t dense_rows(const NodePlan &nd) { return nd.swap ? nd.n : nd.m; }
+inline uint64_t dense_cols(const NodePlan &nd) { return nd.swap ? nd.m : nd.n; }
 inline uint64_t dense_tiles(const NodePlan &nd) {
-    return ((nd.m + kDenseBM - 1) / kDenseBM) * ((nd.n + kDenseBN - 1) / kDenseBN);
+    const uint64_t bn = nd.narrow ? kDenseBN / 2 : kDenseBN;
+    return ((dense_rows(nd) + kDenseBM - 1) / kDenseBM) * ((dense_cols(nd) + bn - 1) / bn);
 }
 inline uint64_t part_bytes(const NodePlan &nd) {
     if (nd.ksplit > 1) return (uint64_t)nd.ksplit * nd.m * nd.n * 8;

@@ -185,7 +185,7 @@ tn_status layout_plan(Plan *p) {
         nd.three_products = 0;
         if (nd.cls != TN_NODE_DENSE) continue;
         int32_t f = dense_fmt;
-        if (f == FMT_SPLIT4 && p->three_products && three_products_pay(nd)) {
+        if (f == FMT_SPLIT4 && p->three_products && !nd.narrow && three_products_pay(nd)) {
             f = FMT_GAUSS6;
             nd.three_products = 1;
         }
@@ -307,8 +307,15 @@ tn_status layout_plan(Plan *p) {
     for (auto &nd : p->nodes) {
         nd.ep_off = -1;
         if (nd.cls != TN_NODE_DENSE || nd.ksplit > 1) continue;
+        // the table follows the kernel's view (rows and columns swapped with
+        // the operands)
+        NodePlan view = nd;
+        if (nd.swap) {
+            std::swap(view.m, view.n);
+            std::swap(view.lm, view.ln);
+        }
         EpTable t;
-        if (!make_ep_table(nd, &t)) continue;
+        if (!make_ep_table(view, &t)) continue;
         nd.ep_off = (int64_t)(p->table_off + ep_start + eps.size() * sizeof(EpTable));
         eps.push_back(t);
     }

@@ -286,3 +286,23 @@ def test_three_product_nodes(m, n, k):
         assert kernel in [r["kernel"] for r in plan.profile()]
         assert_close(out.cpu().numpy().astype(np.complex128), ref, TOL_C64,
                      f"{m}x{n}x{k} three products={three}")
+
+
+@pytest.mark.parametrize("m,n,k,precision,policy,tol", [
+    (64, 4096, 2048, "tf32x3", NT, TOL_C64),                   # m = 64: operands swapped, split-K
+    (4096, 64, 512, "tf32x3", NT, TOL_C64),                    # n = 64: narrow, no swap
+    (64, 64, 1024, "tf32x3", tn.TN_POLICY_DENSE, TOL_C64),     # both sides 64
+    (64, 1024, 8192, "tf32x3", NT, TOL_C64),                   # K-tiled operands, narrow B boxes
+    (200, 48, 1040, "tf32x3", tn.TN_POLICY_DENSE, TOL_C64),    # ragged narrow tiles
+    (30, 300, 96, "tf32x3", tn.TN_POLICY_DENSE, TOL_C64),      # swapped, ragged on both sides
+    (64, 4096, 2048, "bf16", NT, TOL_BF16),                    # bf16: eight 24 KiB stages
+])
+def test_dense_narrow_tiles(m, n, k, precision, policy, tol):
+    """A node with a side of at most 64 runs 128 x 64 tiles: that side goes
+    to N (operands swapped when it is m) and B stacked [Br; Bi] fills one
+    N = 128 MMA."""
+    net = node_network(m, n, k, 3 * m + n + k)
+    plan = tn.Plan.from_network(net, [(0, 1)], (), precision, policy)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE
+    got, _ = run_gpu(net, [(0, 1)], precision=precision, policy=policy, repeat=2)
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"narrow {m}x{n}x{k} {precision}")
