@@ -88,6 +88,7 @@ SIGNATURES = {
     "tn_plan_set_three_products": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_execute_slices": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P, ctypes.c_uint64,
                                          ctypes.c_uint64]),
+    "tn_execute_host": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_check": (ctypes.c_int, [_P]),
     "tn_plan_launches": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_profiling": (ctypes.c_int, [_P, ctypes.c_int32]),
@@ -223,6 +224,13 @@ def tn_execute_slices(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, stream:
                       first: int, step: int) -> None:
     arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
     _check(lib().tn_execute_slices(plan, arr, out_ptr, stream, first, step), plan)
+
+
+def tn_execute_host(plan: int, host_leaf_ptrs: Sequence[int], host_out: int,
+                    dev_leaf_ptrs: Sequence[int], dev_out: int, stream: int) -> None:
+    h = (_P * max(len(host_leaf_ptrs), 1))(*host_leaf_ptrs)
+    d = (_P * max(len(dev_leaf_ptrs), 1))(*dev_leaf_ptrs)
+    _check(lib().tn_execute_host(plan, h, host_out, d, dev_out, stream), plan)
 
 
 def shard_slices(n_slices: int, rank: int, world: int) -> Tuple[int, int, int]:
@@ -362,17 +370,24 @@ class Plan:
                           first, step)
 
     def execute_host(self, host_leaves, host_out, dev_leaves, dev_out, stream=None) -> None:
-        """End-to-end call with host buffers: copy the (pinned) host leaves
-        into ``dev_leaves``, contract into ``dev_out``, copy the result into
-        ``host_out`` and wait for the stream."""
+        """End-to-end call with host buffers (tn_execute_host): the host
+        leaves (pinned: one gather kernel; pageable: one copy each) into
+        ``dev_leaves``, the contraction into ``dev_out``, the result into
+        ``host_out``; then waits for the stream."""
         import torch
+        if self._ws is None:
+            self.bind_workspace(dev_out.device)
         if stream is None:
             stream = torch.cuda.current_stream(dev_out.device)
-        with torch.cuda.stream(stream):
-            for d, h in zip(dev_leaves, host_leaves):
-                d.copy_(h, non_blocking=True)
-            self.execute(dev_leaves, dev_out, stream)
-            host_out.copy_(dev_out, non_blocking=True)
+        for t in list(host_leaves) + [host_out]:
+            if t.dtype != torch.complex64 or not t.is_contiguous() or t.is_cuda:
+                raise ValueError("host leaves and host_out must be contiguous complex64 CPU tensors")
+        for t in list(dev_leaves) + [dev_out]:
+            if t.dtype != torch.complex64 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("dev_leaves and dev_out must be contiguous complex64 CUDA tensors")
+        sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        tn_execute_host(self.handle, [t.data_ptr() for t in host_leaves], host_out.data_ptr(),
+                        [t.data_ptr() for t in dev_leaves], dev_out.data_ptr(), sp)
         stream.synchronize()
 
     def check(self) -> None:

@@ -17,6 +17,8 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
 tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
                         uint64_t first, uint64_t step);
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len);
+tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
+                       void *const *dev_leaves, void *dev_out, cudaStream_t stream);
 }  // namespace tn
 
 namespace {
@@ -105,6 +107,27 @@ tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy) {
     if (!plan || policy < TN_POLICY_AUTO || policy > TN_POLICY_DENSE) return TN_EINVAL;
     plan->p.policy = policy;
     return tn::layout_plan(&plan->p);
+}
+
+tn_status tn_execute_host(tn_plan_t *plan, const void *const *host_leaves, void *host_out,
+                          void *const *dev_leaves, void *dev_out, tn_stream_t stream) {
+    if (!plan) return TN_EINVAL;
+    tn::Plan &p = plan->p;
+    if (!host_leaves || !host_out || !dev_leaves || !dev_out) {
+        p.last_error = "host_leaves, host_out, dev_leaves and dev_out are required";
+        return TN_EINVAL;
+    }
+    for (int t = 0; t < p.n_tensors; ++t)
+        if (!host_leaves[t] || !dev_leaves[t]) {
+            p.last_error = "leaf pointer " + std::to_string(t) + " is NULL";
+            return TN_EINVAL;
+        }
+    if (!p.ws) {
+        p.last_error = "no workspace bound (tn_plan_set_workspace)";
+        return TN_ENOMEM;
+    }
+    return tn::execute_host(&p, host_leaves, host_out, dev_leaves, dev_out,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable) {

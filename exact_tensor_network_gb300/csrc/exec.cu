@@ -742,6 +742,65 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     return TN_OK;
 }
 
+// tn_execute_host: the caller's host leaves into its device leaf buffers
+// (pinned leaves through one gather kernel over their device mappings,
+// others by cudaMemcpyAsync), the contraction, the result back to the host.
+tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
+                       void *const *dev_leaves, void *dev_out, cudaStream_t stream) {
+    const int n = p->n_tensors;
+    if ((int)p->host_leaves_seen.size() != n) {
+        p->host_leaves_seen.assign(n, nullptr);
+        p->host_leaves_dev.assign(n, nullptr);
+    }
+    for (int t = 0; t < n; ++t) {
+        if (p->host_leaves_seen[t] == host_leaves[t]) continue;
+        cudaPointerAttributes attr;
+        const void *dev = nullptr;
+        if (cudaPointerGetAttributes(&attr, host_leaves[t]) == cudaSuccess &&
+            attr.type == cudaMemoryTypeHost && attr.devicePointer)
+            dev = attr.devicePointer;
+        cudaGetLastError();   // pageable memory may report an error: not sticky
+        p->host_leaves_seen[t] = host_leaves[t];
+        p->host_leaves_dev[t] = dev;
+    }
+    GatherLaunch *g = new GatherLaunch;
+    g->njobs = 0;
+    int ctas = 0;
+    cudaError_t e = cudaSuccess;
+    auto flush = [&]() {
+        if (g->njobs == 0) return;
+        g->cta_start[g->njobs] = ctas;
+        e = launch_gather(*g, ctas, stream);
+        g->njobs = 0;
+        ctas = 0;
+    };
+    for (int t = 0; t < n && e == cudaSuccess; ++t) {
+        const int64_t size = p->leaves[t].full_size;
+        if (size <= 0) continue;
+        if (!p->host_leaves_dev[t]) {
+            e = cudaMemcpyAsync(dev_leaves[t], host_leaves[t], (size_t)size * sizeof(float2),
+                                cudaMemcpyHostToDevice, stream);
+            continue;
+        }
+        const int j = g->njobs++;
+        g->cta_start[j] = ctas;
+        g->src[j] = static_cast<const float2 *>(p->host_leaves_dev[t]);
+        g->dst[j] = static_cast<float2 *>(dev_leaves[t]);
+        g->size[j] = size;
+        ctas += permute_ctas(size);
+        if (g->njobs == kGatherBatch) flush();
+    }
+    if (e == cudaSuccess) flush();
+    delete g;
+    if (e != cudaSuccess) return cuda_fail(p, e, "copying the leaves in");
+    const tn_status st = execute_replayed(p, reinterpret_cast<const void *const *>(dev_leaves), dev_out,
+                                          stream);
+    if (st != TN_OK) return st;
+    e = cudaMemcpyAsync(host_out, dev_out, p->out_elems * sizeof(float2), cudaMemcpyDeviceToHost,
+                        stream);
+    return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "copying the result out");
+}
+
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len) {
     const size_t n = p->records.size();
     for (size_t i = 0; i < n; ++i) {

@@ -61,6 +61,38 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
     }
 }
 
+__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ GatherLaunch a) {
+    pdl_trigger();
+    pdl_wait();
+    int lo = 0, hi = a.njobs - 1;
+    const int b = blockIdx.x;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cta_start[mid] <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    const int ctas = a.cta_start[lo + 1] - a.cta_start[lo];
+    const int local = b - a.cta_start[lo];
+    const float2 *src = a.src[lo];
+    float2 *dst = a.dst[lo];
+    const int64_t size = a.size[lo];
+    const int64_t step = (int64_t)ctas * kThreads * kItems;
+    for (int64_t base = (int64_t)local * kThreads * kItems; base < size; base += step) {
+        // all loads of the pass in flight before the stores (host-link latency)
+        float2 v[kItems];
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int64_t e = base + it * kThreads + threadIdx.x;
+            v[it] = e < size ? src[e] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int64_t e = base + it * kThreads + threadIdx.x;
+            if (e < size) dst[e] = v[it];
+        }
+    }
+}
+
 }  // namespace
 
 int permute_ctas(int64_t size) {
@@ -74,6 +106,11 @@ int permute_ctas(int64_t size) {
 cudaError_t launch_permute(const PermLaunch &args, int total_ctas, cudaStream_t stream) {
     if (args.njobs <= 0) return cudaSuccess;
     return launch_pdl(permute_kernel, dim3(total_ctas), dim3(kThreads), 0, stream, args);
+}
+
+cudaError_t launch_gather(const GatherLaunch &args, int total_ctas, cudaStream_t stream) {
+    if (args.njobs <= 0) return cudaSuccess;
+    return launch_pdl(gather_kernel, dim3(total_ctas), dim3(kThreads), 0, stream, args);
 }
 
 }  // namespace tn

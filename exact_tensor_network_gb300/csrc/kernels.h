@@ -140,4 +140,17 @@ cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream);
 // CTAs a permutation job of `size` elements gets.
 int permute_ctas(int64_t size);
 
+// Copy of whole leaves from pinned host memory (read through its device
+// mapping over the host link) into device buffers: one launch for many
+// leaves instead of one copy each.
+constexpr int kGatherBatch = 256;
+struct GatherLaunch {
+    int32_t njobs;
+    int32_t cta_start[kGatherBatch + 1];
+    const float2 *src[kGatherBatch];   // device addresses of the pinned host leaves
+    float2 *dst[kGatherBatch];
+    int64_t size[kGatherBatch];        // elements
+};
+cudaError_t launch_gather(const GatherLaunch &args, int total_ctas, cudaStream_t stream);
+
 }  // namespace tn

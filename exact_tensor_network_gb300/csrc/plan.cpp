@@ -273,6 +273,7 @@ tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices
             ustride[i] = s;
             s *= p->extents[um[i]];
         }
+        lp.full_size = s;
         for (int i = 0; i < r; ++i)
             if (is_sliced[um[i]]) {
                 const int pos = (int)(std::find(p->slice_modes.begin(), p->slice_modes.end(), um[i]) -

@@ -108,6 +108,7 @@ struct LeafPlan {
     bool identity;          // caller's layout already is the lifetime order
     bool in_place;          // consumed straight from the caller's pointer
     int64_t size;           // elements after slicing
+    int64_t full_size;      // elements of the caller's leaf (all its modes)
     Place place;            // where the consumer reads it
     PermDesc perm;          // valid when !in_place
     // slicing: sliced modes this leaf carries, as (slice position, stride)
@@ -327,6 +328,9 @@ struct Plan {
     void *graph_exec = nullptr;
     void *capture_stream = nullptr;
     std::vector<void *> lane_streams;           // recording: extra streams for independent launches
+    // tn_execute_host: host leaf pointers seen last and their device mappings
+    // (null: pageable, copied with cudaMemcpyAsync)
+    std::vector<const void *> host_leaves_seen, host_leaves_dev;
     std::vector<void *> dag_events;             // recording: one event per launch
     std::vector<const void *> graph_leaves;
     void *graph_out = nullptr;

@@ -247,6 +247,21 @@ TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs
 TN_API tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
                                    tn_stream_t stream, uint64_t first, uint64_t step);
 
+/*
+ * End to end from host memory: copy each caller leaf host_leaves[t] (its
+ * whole storage, complex64, caller's order) into the device buffer
+ * dev_leaves[t] (caller-owned, at least as large), contract into dev_out as
+ * tn_execute does, and copy the result (open-mode order) into host_out.
+ * Leaves in pinned (page-locked) host memory are read through their device
+ * mapping by one gather kernel for all of them; other leaves are copied one
+ * cudaMemcpyAsync each (synchronous for pageable memory).  Asynchronous on
+ * `stream` for pinned buffers: synchronise the stream before reading
+ * host_out.  The host buffers must stay valid until then.
+ * Errors: as tn_execute; TN_EINVAL for NULL pointers.
+ */
+TN_API tn_status tn_execute_host(tn_plan_t *plan, const void *const *host_leaves, void *host_out,
+                                 void *const *dev_leaves, void *dev_out, tn_stream_t stream);
+
 /* Enable (1, the default) or disable (0) graph replay in tn_execute; any
  * recorded graph is released either way. */
 TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);

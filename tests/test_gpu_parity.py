@@ -294,3 +294,34 @@ def test_replayed_dependency_graph(case):
         torch.cuda.synchronize()
         assert_close(out.cpu().numpy().astype(np.complex128), ref, what=f"{case} call {it}")
     plan.check()
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("case", ["random_60", "tiny_sliced"])
+def test_execute_from_host_buffers(pinned, case):
+    """tn_execute_host: host leaves in (pinned: one gather kernel over their
+    device mappings; pageable: one copy each), contraction, result out."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    if case == "random_60":
+        net, tree, _ = configs.random_60()
+        sl = []
+    else:
+        net = random_tiny_network(507)
+        tree = greedy_tree(net, 7)
+        sl = net.closed_modes()[:2]
+    ref = _ref(net, tree)
+    plan = tn.Plan.from_network(net, tree, sl)
+    dev = torch.device("cuda:0")
+    host_leaves = [torch.from_numpy(np.ascontiguousarray(d)) for d in net.data]
+    host_out = torch.zeros(plan.out_shape, dtype=torch.complex64)
+    if pinned:
+        host_leaves = [h.pin_memory() for h in host_leaves]
+        host_out = host_out.pin_memory()
+    dev_leaves = [torch.empty_like(h, device=dev) for h in host_leaves]
+    dev_out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
+    for it in range(3):
+        host_out.fill_(complex(5.0, 5.0))
+        plan.execute_host(host_leaves, host_out, dev_leaves, dev_out)
+        assert_close(host_out.numpy().astype(np.complex128), ref, what=f"{case} call {it}")
+    plan.check()
