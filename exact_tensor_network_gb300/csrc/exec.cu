@@ -89,9 +89,21 @@ void choose_split(const Plan &p, NodePlan &nd) {
             return;
         }
         if (nd.k < 512) return;
-        // whole waves only: tiles x splits <= SMs
-        uint64_t s = std::min<uint64_t>(sms / tiles, nd.k / 256);
-        s = std::min<uint64_t>(s, kPartialBudget / (8 * outs));
+        // the split count whose tiles x splits work items fill their waves
+        // best (fewer splits when nearly equal: each split adds partials to
+        // write and reduce); splits are whole 256-entry chunks
+        const uint64_t smax = std::min<uint64_t>(std::min<uint64_t>(nd.k / 256, 64),
+                                                 kPartialBudget / (8 * outs));
+        uint64_t s = 1;
+        double best = (double)tiles / (double)sms;
+        for (uint64_t c = 2; c <= smax; ++c) {
+            const uint64_t items = tiles * c, waves = (items + sms - 1) / sms;
+            const double eff = (double)items / (double)(waves * sms);
+            if (eff > best + 0.02) {
+                best = eff;
+                s = c;
+            }
+        }
         if (s < 2) return;
         uint64_t chunk = (nd.k + s - 1) / s;
         chunk = (chunk + 255) / 256 * 256;
