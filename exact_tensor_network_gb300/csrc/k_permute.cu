@@ -37,26 +37,67 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
     const int32_t fmt = d.dst_off < 0 ? (int32_t)FMT_C64 : d.fmt;
     const int rank = d.rank;
     const int64_t size = d.size;
+    // source offset of destination entry e (mixed radix over dims)
+    auto source = [&](int64_t e) {
+        int64_t rem = e, so = 0;
+#pragma unroll 1
+        for (int r = rank - 1; r >= 0; --r) {
+            const int64_t dim = d.dims[r];
+            if (d.dshift[r] >= 0) {
+                so += (rem & (dim - 1)) * d.sstride[r];
+                rem >>= d.dshift[r];
+            } else {
+                const int64_t q = rem / dim;
+                so += (rem - q * dim) * d.sstride[r];
+                rem = q;
+            }
+        }
+        return so;
+    };
+    if (d.vec4 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        // four consecutive entries per thread: consecutive in the source
+        // too; all loads of the pass first, then one store per plane each
+        // K-tiled destinations are walked in their physical order (whole
+        // 64-byte tile rows per plane in turn); q * 4 is then a physical
+        // index, and its logical index comes from undoing the tiling
+        const PlanarTile &tl = d.tile;
+        const bool phys = tl.kt != 0;
+        const PlanarTile untiled{0, 0, -1, 0};
+        const int64_t n4 = size / 4;
+        const int64_t step4 = (int64_t)ctas * kThreads * kItems;
+        for (int64_t base = (int64_t)local * kThreads * kItems; base < n4; base += step4) {
+            float2 v[kItems][4];
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int64_t q = base + it * kThreads + threadIdx.x;
+                if (q < n4) {
+                    int64_t e = q * 4;
+                    if (phys) {
+                        // physical ((c / kt) * rows + r) * kt + c % kt
+                        const int64_t cl = e % tl.kt, t2 = e / tl.kt;
+                        const int64_t r = t2 % tl.rows, ct = t2 / tl.rows;
+                        e = r * tl.k + ct * tl.kt + cl;
+                    }
+                    const float2 *p = src + source(e);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[it][u] = p[u];
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int64_t q = base + it * kThreads + threadIdx.x;
+                if (q < n4) store_quad(dst, fmt, size, q * 4, v[it], a.accumulate, phys ? untiled : d.tile);
+            }
+        }
+        return;
+    }
     const int64_t step = (int64_t)ctas * kThreads * kItems;
     for (int64_t base = (int64_t)local * kThreads * kItems; base < size; base += step) {
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
             const int64_t e = base + it * kThreads + threadIdx.x;
             if (e >= size) break;
-            int64_t rem = e, so = 0;
-#pragma unroll 1
-            for (int r = rank - 1; r >= 0; --r) {
-                const int64_t dim = d.dims[r];
-                if (d.dshift[r] >= 0) {
-                    so += (rem & (dim - 1)) * d.sstride[r];
-                    rem >>= d.dshift[r];
-                } else {
-                    const int64_t q = rem / dim;
-                    so += (rem - q * dim) * d.sstride[r];
-                    rem = q;
-                }
-            }
-            store_entry(dst, fmt, size, e, src[so], a.accumulate, d.tile);
+            store_entry(dst, fmt, size, e, src[source(e)], a.accumulate, d.tile);
         }
     }
 }

@@ -101,6 +101,11 @@ struct PermDesc {
     int64_t dims[kMaxPermRank];
     int64_t sstride[kMaxPermRank];
     int32_t dshift[kMaxPermRank];   // log2(dims) for powers of two, else -1
+    // 1: the innermost dimension is contiguous in the source and a multiple
+    // of 4 long, and size is a multiple of 4: a thread moves four
+    // consecutive entries at a time
+    int32_t vec4;
+    int32_t pad;
 };
 
 struct LeafPlan {

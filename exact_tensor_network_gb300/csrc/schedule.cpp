@@ -279,6 +279,8 @@ tn_status layout_plan(Plan *p) {
             d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
             d.fmt = (S == 0) ? FMT_C64 : p->fmt[t];
             d.tile = (S == 0) ? untiled : tile[t];
+            d.vec4 = d.rank >= 1 && d.sstride[d.rank - 1] == 1 && d.dims[d.rank - 1] % 4 == 0 &&
+                     d.size % 4 == 0;
             p->perm_table.push_back(d);
             p->perm_leaves.push_back(t);
         }
