@@ -68,6 +68,7 @@ void choose_split(const Plan &p, NodePlan &nd) {
     nd.swap = 0;
     nd.narrow = 0;
     nd.tail_first = -1;
+    nd.red_ctas = 0;
     uint64_t units = 0, outs = nd.m * nd.n;
     if (nd.cls == TN_NODE_DENSE) {
         // a side of at most 64 goes to N (operands swapped when it is m) and
@@ -120,6 +121,7 @@ void choose_split(const Plan &p, NodePlan &nd) {
         int64_t rpc;
         stream_shape(rows, nd.k, &lanes, &rpc);
         units = (rows + rpc - 1) / rpc;
+        nd.red_ctas = (int64_t)units;
     } else if (nd.cls == TN_NODE_SIMT) {
         units = ((nd.m + 63) / 64) * ((nd.n + 63) / 64);
     } else {
@@ -140,11 +142,17 @@ void choose_split(const Plan &p, NodePlan &nd) {
     }
 }
 
+// Split-K nodes of the streaming class reduce their partials in the node
+// kernel (the last split to finish a row block); the others get a reduction
+// launch, which spreads the sums over every SM (the tensor-core kernel's
+// last splits alone took longer than kernel plus reduction).
+bool fused_reduction(const NodePlan &nd) { return nd.cls == TN_NODE_STREAM && nd.ksplit > 1; }
+
 uint64_t launches_per_slice(const Plan &p) {
     uint64_t n = (p.perm_table.size() + kPermBatch - 1) / kPermBatch;
     for (const auto &L : p.sched) {
         if (L.kind == LAUNCH_TINY) ++n;
-        if (L.kind == LAUNCH_NODE) n += p.nodes[L.node].ksplit > 1 ? 2 : 1;   // + reduction
+        if (L.kind == LAUNCH_NODE) n += fused_reduction(p.nodes[L.node]) ? 1 : p.nodes[L.node].ksplit > 1 ? 2 : 1;
     }
     return n;
 }
@@ -273,7 +281,10 @@ std::vector<Access> slice_accesses(const Plan &p) {
         add_range(a.rd, nd.pb, nd.n * nd.k * fmt_bytes(p.fmt[nd.b]));
         add_range(a.wr, nd.pc, nd.m * nd.n * fmt_bytes(nd.out_fmt));
         if (nd.tail_first >= 0) add_range(a.wr, nd.part, part_bytes(nd));
-        if (nd.ksplit > 1) {
+        if (nd.ksplit > 1 && fused_reduction(nd)) {
+            add_range(a.wr, nd.part, part_bytes(nd));
+            acc.push_back(a);
+        } else if (nd.ksplit > 1) {
             add_range(a.wr, nd.part, part_bytes(nd));
             acc.push_back(a);
             Access r;
@@ -617,6 +628,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 stream_shape((uint64_t)a.m, nd.k, &lanes, &rpc);
                 a.lanes = lanes;
                 a.rows_per_cta = (int32_t)rpc;
+                a.cnt = nd.ksplit > 1 ? reinterpret_cast<int32_t *>(ws + nd.red_cnt_off) : nullptr;
                 rec.begin(TN_KERNEL_STREAM, nd.step, flops, node_bytes(nd, accumulate));
                 e = launch_stream_node(a, dag ? dag->begin() : stream);
                 if (dag) dag->end();
@@ -644,7 +656,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 if (dag) dag->end();
                 rec.end();
             }
-            if (e == cudaSuccess && nd.ksplit > 1) {
+            if (e == cudaSuccess && nd.ksplit > 1 && !fused_reduction(nd)) {
                 ReduceArgs r;
                 std::memset(&r, 0, sizeof(r));
                 const bool sw = nd.swap != 0;   // partials are [split][rows][cols] of the kernel's view

@@ -7,9 +7,10 @@
 // shared memory one k-chunk at a time; each row of A is read once, by
 // `lanes` threads that split its k range and then combine their partial
 // sums with warp shuffles.  Long k ranges are cut into ksplit chunks run by
-// different CTAs; their fp32 partial sums land in the workspace and
-// splitk_reduce adds them in split order (deterministic), then stores the
-// node's output through its separable offsets in the consumer's format.
+// different CTAs; their fp32 partial sums land in the workspace and the
+// last split of each row block adds them in a fixed order (deterministic),
+// then stores the node's output through its separable offsets in the
+// consumer's format.  splitk_reduce does the same for the other classes.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -104,6 +105,73 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
                                            a.accumulate, a.out_tile);
             }
         }
+    }
+    if (a.ksplit > 1) {
+        // The last split of this row block to finish sums the partials of
+        // all splits and stores the rows; a counter, not a wait.  Row blocks
+        // are small (often a few dozen entries) and splits many, so the
+        // threads split both: E threads (a power of two covering the block,
+        // at most all of them) per entry, G = 256 / E groups over the splits
+        // (group g takes splits g, g + G, ...: four loads in flight), then
+        // group 0 adds the G group sums in order.  The order is fixed, so
+        // runs are bit-identical.
+        __shared__ int last;
+        __shared__ float2 red_s[kThreads];
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(a.cnt + blockIdx.x, 1) == a.ksplit - 1;
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        // rows r0..r1 are one contiguous run of each split's partials
+        const int64_t cnt = (r1 - r0) * n, plane = a.m * a.n;
+        const float2 *base = a.part + r0 * a.n;
+        int E = 1;
+        while (E < cnt && E < kThreads) E <<= 1;
+        const int G = kThreads / E;
+        const int eg = threadIdx.x % E, gi = threadIdx.x / E;
+        for (int64_t e0 = 0; e0 < cnt; e0 += E) {
+            const int64_t e = e0 + eg;
+            float2 v = make_float2(0.f, 0.f);
+            if (e < cnt) {
+                const float2 *pe = base + e;
+                int sp = gi;
+                for (; sp + 3 * G < a.ksplit; sp += 4 * G) {
+                    float2 x[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) x[u] = __ldcg(pe + (int64_t)(sp + u * G) * plane);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v.x += x[u].x;
+                        v.y += x[u].y;
+                    }
+                }
+                for (; sp < a.ksplit; sp += G) {
+                    const float2 x = __ldcg(pe + (int64_t)sp * plane);
+                    v.x += x.x;
+                    v.y += x.y;
+                }
+            }
+            if (G > 1) {
+                red_s[threadIdx.x] = v;
+                __syncthreads();
+                if (gi == 0 && e < cnt) {
+                    for (int g2 = 1; g2 < G; ++g2) {
+                        const float2 x = red_s[g2 * E + eg];
+                        v.x += x.x;
+                        v.y += x.y;
+                    }
+                }
+                __syncthreads();
+            }
+            if (gi == 0 && e < cnt) {
+                const int64_t r = r0 + e / n;
+                const int j = (int)(e - (r - r0) * n);
+                store_entry_t<FMT>(a.C, plane, sep_offset(a.lm, r) + sep_offset(a.ln, j), v,
+                                   a.accumulate, a.out_tile);
+            }
+        }
+        if (threadIdx.x == 0) a.cnt[blockIdx.x] = 0;   // ready for the next run
     }
 }
 
@@ -204,9 +272,21 @@ __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_co
     const int64_t mn = a.m * a.n;
     for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < mn;
          e += (int64_t)gridDim.x * kThreads) {
+        // splits added in order, four loads in flight
         float2 v = make_float2(0.f, 0.f);
-        for (int s = 0; s < a.ksplit; ++s) {
-            const float2 p = a.part[(int64_t)s * mn + e];
+        int s = 0;
+        for (; s + 4 <= a.ksplit; s += 4) {
+            float2 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = __ldcg(a.part + (int64_t)(s + u) * mn + e);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                v.x += x[u].x;
+                v.y += x[u].y;
+            }
+        }
+        for (; s < a.ksplit; ++s) {
+            const float2 p = __ldcg(a.part + (int64_t)s * mn + e);
             v.x += p.x;
             v.y += p.y;
         }

@@ -38,7 +38,8 @@ struct NodeArgs {
 
 // Bandwidth-bound node: B (n <= kStreamMaxN rows) is small and staged in
 // shared memory k-chunk by k-chunk; the rows of A stream through once.
-// Same output and split-K conventions as NodeArgs.
+// Same output conventions as NodeArgs; split-K partials are reduced by the
+// kernel itself (cnt).
 constexpr int kStreamMaxN = 16;
 constexpr int kStreamKc = 256;     // k entries of B staged per chunk (<= 32 KiB)
 struct StreamArgs {
@@ -55,6 +56,9 @@ struct StreamArgs {
     int32_t out_fmt;
     PlanarTile out_tile;
     int32_t rows_contig;  // set by the launcher: entry (i, j) lies at i n + j
+    // split-K: one counter per row-block CTA (zero between runs); the last
+    // split of a block to finish reduces the block's partials into C
+    int32_t *cnt;
 };
 
 // Ordered sum of split-K partials into the node's output.

@@ -155,6 +155,11 @@ struct NodePlan {
     // second to arrive adds the other half and stores.  -1: no tail split.
     int64_t tail_first;
     int64_t tail_cnt_off;
+    // stream class with split-K: CTAs per split (row blocks) and their
+    // counters (byte offset from the workspace start); the kernel reduces
+    // its own partials, so the node has no separate reduction launch
+    int64_t red_ctas;
+    int64_t red_cnt_off;
     // dense class, tf32x3: the complex product from three real products
     // (Ar Br, Ai Bi, (Ar + Ai)(Br + Bi)) instead of four; operands are
     // FMT_GAUSS6

@@ -369,9 +369,15 @@ tn_status layout_plan(Plan *p) {
     uint64_t cnt = 0;
     for (auto &nd : p->nodes) {
         nd.tail_cnt_off = -1;
-        if (nd.tail_first < 0) continue;
-        nd.tail_cnt_off = (int64_t)(p->table_off + cnt_start + 4 * cnt);
-        cnt += (dense_tiles(nd) - (uint64_t)nd.tail_first) * kDrainWarps;
+        nd.red_cnt_off = -1;
+        if (nd.tail_first >= 0) {
+            nd.tail_cnt_off = (int64_t)(p->table_off + cnt_start + 4 * cnt);
+            cnt += (dense_tiles(nd) - (uint64_t)nd.tail_first) * kDrainWarps;
+        }
+        if (nd.cls == TN_NODE_STREAM && nd.ksplit > 1) {
+            nd.red_cnt_off = (int64_t)(p->table_off + cnt_start + 4 * cnt);
+            cnt += (uint64_t)nd.red_ctas;
+        }
     }
     p->table_blob.assign(cnt_start + 4 * cnt, 0);
     if (perm_bytes) std::memcpy(p->table_blob.data(), p->perm_table.data(), perm_bytes);

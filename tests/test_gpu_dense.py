@@ -159,6 +159,24 @@ def test_dense_split_k_feeding_dense():
     assert_close(got, _ref(net, tree), TOL_C64, "split dense feeding dense")
 
 
+def test_split_k_interleaved_sliced_root_repeated():
+    """Split-K node whose output interleaves M and N modes, sliced over a
+    K mode so the root accumulates, executed three times."""
+    rng = np.random.default_rng(57)
+    ext = [8, 8, 64, 32, 2048, 2]               # a1 a2 b1 b2 x1 x2
+    tensors = [[0, 1, 4, 5], [2, 4, 5, 3]]
+    data = [_rand(rng, [ext[x] for x in t], 0.05) for t in tensors]
+    net = Network(tensors, ext, [3, 0, 2, 1], data)
+    tree = [(0, 1)]
+    sl = [5]
+    assert _classes(net, tree, sl) == [tn.TN_NODE_DENSE]
+    p = tn.Plan.from_network(net, tree, sl, "tf32x3", NT)
+    assert p.launches == 6                      # per slice: leaf conversion, dense, reduction
+    got, plan = run_gpu(net, tree, sl, policy=NT, repeat=3)
+    assert plan.num_slices == 2
+    assert_close(got, _ref(net, tree, sl), TOL_C64, "split-K interleaved sliced root")
+
+
 def test_sliced_dense_root_accumulates():
     net = gemm_network(8, 8, 9, 3)
     sl = [net.tensors[0][-1], net.tensors[0][-2]]     # two K modes -> 4 slices
