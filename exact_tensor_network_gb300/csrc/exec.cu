@@ -545,6 +545,13 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 tl.arena = arena;
                 tl.out = out;
                 tl.accumulate_root = later ? 1 : 0;
+                const unsigned char *descs = p->table_blob.data() + (p->tiny_off - p->table_off);
+                for (int x = 0; x < L.count; ++x) {
+                    TinyDesc d;
+                    std::memcpy(&d, descs + (size_t)(L.first + x) * sizeof(TinyDesc), sizeof(d));
+                    tl.base[x] = d.cta_base;
+                }
+                tl.base[L.count] = L.ctas;
                 rec.begin(TN_KERNEL_TINY, -1, L.flops, L.bytes);
                 cudaError_t e = launch_tiny_batch(tl, L.ctas, dag ? dag->begin() : stream);
                 if (dag) dag->end();

@@ -22,17 +22,28 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_constant__ TinyLaunch a) {
+    __shared__ int node_s;
+    __shared__ __align__(16) TinyDesc ds;
     pdl_trigger();
-    pdl_wait();
-    // this CTA's node: last descriptor whose cta_base <= blockIdx.x
-    int lo = a.first, hi = a.first + a.count - 1;
+    // This CTA's node: the one whose CTA range holds blockIdx.x, found with
+    // one compare per thread over the launch parameters; then its
+    // descriptor, copied once into shared memory, where the output loop
+    // reads it.  The table is written once, before any launch, so both
+    // steps may run before the previous launch has finished.
     const int b = blockIdx.x;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.table[mid].cta_base <= b) lo = mid;
-        else hi = mid - 1;
+    if (threadIdx.x == 0) node_s = 0;   // (every CTA matches one node)
+    __syncthreads();
+    for (int t = threadIdx.x; t < a.count; t += kThreads)
+        if (a.base[t] <= b && b < a.base[t + 1]) node_s = t;
+    __syncthreads();
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.table + a.first + node_s);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(&ds);
+        for (int x = threadIdx.x; x < (int)(sizeof(TinyDesc) / 4); x += kThreads) dst[x] = src[x];
     }
-    const TinyDesc &d = a.table[lo];
+    __syncthreads();
+    pdl_wait();
+    const TinyDesc &d = ds;
     const int local = b - d.cta_base;
     const float2 *A = reinterpret_cast<const float2 *>(a.arena + d.a_off);
     const float2 *B = reinterpret_cast<const float2 *>(a.arena + d.b_off);

@@ -75,12 +75,16 @@ struct ReduceArgs {
 
 // One batched launch of tiny nodes: descriptors [first, first + count) of
 // the workspace table.
+// A batch holds at most kTinyLaunchNodes nodes; base[i] is the first CTA of
+// node first + i (base[count] = the launch's CTAs).  The bases travel in the
+// launch parameters, so a CTA finds its node without reading the table.
 struct TinyLaunch {
     const TinyDesc *table;
     int32_t first, count;
     char *arena;
     float2 *out;
     int32_t accumulate_root;   // later slices: the root adds into out
+    int32_t base[kTinyLaunchNodes + 1];
 };
 
 cudaError_t launch_tiny_batch(const TinyLaunch &args, int ctas, cudaStream_t stream);

@@ -253,6 +253,7 @@ struct Launch {
 constexpr uint64_t kTinyMacs = 1ull << 23;
 constexpr uint64_t kTinyMaxK = 512;
 constexpr uint64_t kTinyMaxOut = 1ull << 17;
+constexpr int kTinyLaunchNodes = 256;   // tiny nodes per batched launch (at most)
 
 inline int64_t sep_offset_host(const SepLayout &L, int64_t i) {
     int64_t off = 0;

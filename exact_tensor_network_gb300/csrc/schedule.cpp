@@ -199,8 +199,9 @@ tn_status layout_plan(Plan *p) {
         nd.ktiled = 0;
         if (nd.cls != TN_NODE_DENSE) continue;
         const int32_t kt = planar_kt(p->fmt[nd.a]);
-        // rows of 16 KiB and more: 64-byte pieces would each cost a DRAM page
-        if (nd.k % (uint64_t)kt != 0 || nd.k < 4096) continue;
+        // rows of 8 KiB and more per plane: 64-byte pieces would each cost
+        // a DRAM page
+        if (nd.k % (uint64_t)kt != 0 || nd.k < 2048) continue;
         nd.ktiled = 1;
         const int32_t ks = log2_exact((int64_t)nd.k);
         tile[nd.a] = PlanarTile{(int64_t)nd.k, (int64_t)nd.m, ks, kt};
@@ -224,12 +225,14 @@ tn_status layout_plan(Plan *p) {
         std::vector<int> tiny;
         for (int s : by_stage[st])
             if (p->nodes[s].cls == TN_NODE_TINY) tiny.push_back(s);
-        if (!tiny.empty()) {
+        // batches of at most kTinyLaunchNodes nodes (independent launches)
+        for (size_t b0 = 0; b0 < tiny.size(); b0 += kTinyLaunchNodes) {
+            const size_t b1 = std::min(tiny.size(), b0 + (size_t)kTinyLaunchNodes);
             Launch L{};
             L.kind = LAUNCH_TINY;
             L.node = -1;
-            for (int s : tiny) t_of[n + s] = (int)p->sched.size();
-            tiny_batches.push_back(tiny);
+            for (size_t x = b0; x < b1; ++x) t_of[n + tiny[x]] = (int)p->sched.size();
+            tiny_batches.emplace_back(tiny.begin() + b0, tiny.begin() + b1);
             p->sched.push_back(L);
         }
         for (int s : by_stage[st]) {

@@ -228,6 +228,45 @@ def test_tiny_batching_matches_unbatched(name):
     assert_close(b, ref, what=f"{name} one launch per node")
 
 
+def _unitary_chain(pairs, seed):
+    """Leaves 2i = U[a_i, x_i] and 2i + 1 = V[x_i, a_(i+1)], random 2 x 2
+    unitaries (so every partial product stays unitary); a_0 and a_pairs are
+    open.  The tree contracts every pair first (`pairs` tiny nodes in the
+    first stage), then neighbours pairwise."""
+    rng = np.random.default_rng(seed)
+    tensors, data = [], []
+    for i in range(pairs):
+        tensors += [[i, pairs + 1 + i], [pairs + 1 + i, i + 1]]
+    for _ in tensors:
+        q, r = np.linalg.qr(rng.standard_normal((2, 2)) + 1j * rng.standard_normal((2, 2)))
+        data.append((q * (np.diag(r) / np.abs(np.diag(r)))).astype(np.complex64))
+    tree = [(2 * i, 2 * i + 1) for i in range(pairs)]
+    cur, nid = [2 * pairs + i for i in range(pairs)], 3 * pairs
+    while len(cur) > 1:
+        nxt = []
+        for x in range(0, len(cur) - 1, 2):
+            tree.append((cur[x], cur[x + 1]))
+            nxt.append(nid)
+            nid += 1
+        cur = nxt + ([cur[-1]] if len(cur) % 2 else [])
+    return Network(tensors, [2] * (2 * pairs + 1), [0, pairs], data, f"chain_{pairs}"), tree
+
+
+def test_tiny_stage_over_one_launch():
+    """300 tiny nodes in one stage run as two batched launches (at most 256
+    nodes each)."""
+    import exact_tensor_network_gb300 as tn
+    net, tree = _unitary_chain(300, 5)
+    got, plan = run_gpu(net, tree)
+    # 2 leaf launches (600 leaves, 512 per launch) + 10 tiny stages, the
+    # first of them split in two
+    assert plan.launches == 13
+    ref = _ref(net, tree)
+    assert_close(got, ref, what="300-node tiny stage")
+    # a unitary, up to the complex64 rounding of 600 leaves
+    assert np.allclose(ref @ ref.conj().T, np.eye(2), atol=1e-4)
+
+
 def test_profiling_records_every_launch():
     import torch
     import exact_tensor_network_gb300 as tn
