@@ -9,7 +9,8 @@
 // descriptor table), enough that every thread group computes at most two
 // outputs, since each output is a serial chain of memory waits; `lanes`
 // threads cooperate on one output's k range (k <= 512: at most two rounds of
-// loads) and combine with warp shuffles.  Operands are complex64 in the workspace arena; the
+// loads) and combine with warp shuffles.  One lane decodes each output's
+// address into (i, j) and passes it to the lanes that compute it.  Operands are complex64 in the workspace arena; the
 // output goes through the node's separable offsets in its consumer's format
 // (the root adds into the caller's output on later slices).
 #include "common.cuh"
@@ -53,17 +54,23 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
     const int64_t o0 = (int64_t)local * per;
     const int64_t o1 = min(mn, o0 + per);
     const int lanes = d.lanes;
-    const int g = threadIdx.x / lanes, l = threadIdx.x % lanes;
-    const int groups = kThreads / lanes;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int opw = 32 / lanes;                        // outputs per warp and pass
+    const int chunk = opw * 2 < 32 ? opw * 2 : 32;     // outputs of one decode pass
+    const int l = lane % lanes, gq = lane / lanes;
     const int accumulate = d.is_root ? a.accumulate_root : 0;
     const int k = d.k;
-    for (int64_t ob = o0; ob < o1; ob += groups) {
-        // outputs in address order: o is the address, (i, j) from the walk;
-        // m n <= 2^23 here, so 32-bit index arithmetic is exact
-        const int64_t o = ob + g;
-        float2 acc = make_float2(0.f, 0.f);
-        if (o < o1) {
-            int rem = static_cast<int>(o), i = 0, j = 0;
+    // rows of even length on 16-byte boundaries load two entries at a time
+    const bool pairs = (k & 1) == 0 && ((reinterpret_cast<uintptr_t>(A) |
+                                         reinterpret_cast<uintptr_t>(B)) & 15) == 0;
+    // Each warp takes `chunk` consecutive addresses at a time: lane q
+    // decodes address cb + q into (i, j) (the walk; m n <= 2^23 here, so
+    // 32-bit index arithmetic is exact), then groups of `lanes` lanes take
+    // the outputs in address order, reading (i, j) from the decoding lane.
+    for (int64_t cb = o0 + (int64_t)warp * chunk; cb < o1; cb += (int64_t)(kThreads / 32) * chunk) {
+        int wi = 0, wj = 0;
+        if (lane < chunk && cb + lane < o1) {
+            int rem = static_cast<int>(cb + lane);
 #pragma unroll 1
             for (int t = 0; t < d.wn; ++t) {
                 int dg;
@@ -75,28 +82,59 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
                     dg = rem - q * d.wext[t];
                     rem = q;
                 }
-                if ((d.wside >> t) & 1u) j += dg * d.wt[t];
-                else i += dg * d.wt[t];
+                if ((d.wside >> t) & 1u) wj += dg * d.wt[t];
+                else wi += dg * d.wt[t];
             }
-            const float2 *ar = A + (int64_t)i * k, *br = B + (int64_t)j * k;
-            // eight independent load pairs in flight per round
-            for (int kk = l; kk < k; kk += 8 * lanes) {
-                float2 av[8], bv[8];
+        }
+#pragma unroll 1
+        for (int q0 = 0; q0 < chunk; q0 += opw) {
+            const int q = q0 + gq;
+            const int64_t o = cb + q;
+            const int i = __shfl_sync(0xffffffffu, wi, q);
+            const int j = __shfl_sync(0xffffffffu, wj, q);
+            float2 acc = make_float2(0.f, 0.f);
+            if (o < o1) {
+                const float2 *ar = A + (int64_t)i * k, *br = B + (int64_t)j * k;
+                if (pairs) {
+                    // eight independent 16-byte load pairs in flight per round
+                    const float4 *ar4 = reinterpret_cast<const float4 *>(ar);
+                    const float4 *br4 = reinterpret_cast<const float4 *>(br);
+                    const int k2 = k >> 1;
+                    for (int kk = l; kk < k2; kk += 8 * lanes) {
+                        float4 av[8], bv[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int idx = kk + u * lanes;
-                    av[u] = idx < k ? ar[idx] : make_float2(0.f, 0.f);
-                    bv[u] = idx < k ? br[idx] : make_float2(0.f, 0.f);
+                        for (int u = 0; u < 8; ++u) {
+                            const int idx = kk + u * lanes;
+                            av[u] = idx < k2 ? ar4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+                            bv[u] = idx < k2 ? br4[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            cfma(acc, make_float2(av[u].x, av[u].y), make_float2(bv[u].x, bv[u].y));
+                            cfma(acc, make_float2(av[u].z, av[u].w), make_float2(bv[u].z, bv[u].w));
+                        }
+                    }
+                } else {
+                    // eight independent load pairs in flight per round
+                    for (int kk = l; kk < k; kk += 8 * lanes) {
+                        float2 av[8], bv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int idx = kk + u * lanes;
+                            av[u] = idx < k ? ar[idx] : make_float2(0.f, 0.f);
+                            bv[u] = idx < k ? br[idx] : make_float2(0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) cfma(acc, av[u], bv[u]);
+                    }
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) cfma(acc, av[u], bv[u]);
             }
+            for (int off = lanes >> 1; off > 0; off >>= 1) {
+                acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, lanes);
+                acc.y += __shfl_down_sync(0xffffffffu, acc.y, off, lanes);
+            }
+            if (l == 0 && o < o1) store_entry(C, d.out_fmt, mn, o, acc, accumulate, d.out_tile);
         }
-        for (int off = lanes >> 1; off > 0; off >>= 1) {
-            acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, lanes);
-            acc.y += __shfl_down_sync(0xffffffffu, acc.y, off, lanes);
-        }
-        if (l == 0 && o < o1) store_entry(C, d.out_fmt, mn, o, acc, accumulate, d.out_tile);
     }
 }
 

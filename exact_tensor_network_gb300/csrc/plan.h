@@ -221,7 +221,7 @@ struct TinyDesc {
     PlanarTile out_tile;
     int32_t cta_base;      // first CTA of this node within its launch
     int32_t ctas;
-    int32_t lanes;         // threads that share one output's k range (1, 4 or 32)
+    int32_t lanes;         // threads that share one output's k range (a power of two <= 32)
     // Output walk, so that consecutive threads store consecutive addresses:
     // address p (< m n <= 2^23) splits mixed-radix over the wn runs of the
     // output's modes, fastest first; digit d of run t adds d * wt[t] to i

@@ -347,7 +347,9 @@ tn_status layout_plan(Plan *p) {
             const uint64_t macs = nd.m * nd.n * nd.k;
             // `lanes` threads per output; enough CTAs that each group of a CTA
             // computes at most two outputs (the rounds are serial memory waits)
-            d.lanes = nd.k >= 64 ? 32 : nd.k >= 8 ? 4 : 1;
+            // (a lane covers up to 16 entries of k per round of loads)
+            d.lanes = 1;
+            while (d.lanes < 32 && (uint64_t)d.lanes * 16 < nd.k) d.lanes *= 2;
             const uint64_t per_cta = 2 * (256 / (uint64_t)d.lanes);
             d.ctas = (int32_t)std::max<uint64_t>(1, (nd.m * nd.n + per_cta - 1) / per_cta);
             d.cta_base = ctas;
