@@ -57,8 +57,10 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
                 Bs[c][r] = (j < a.n && kk < kend) ? a.B[j * a.k + kk] : make_float2(0.f, 0.f);
             }
             __syncthreads();
+            // the stage's valid k entries only (small-k nodes: one short stage)
+            const int kn = (int)min((int64_t)BK, kend - k0);
 #pragma unroll 2
-            for (int kk = 0; kk < BK; ++kk) {
+            for (int kk = 0; kk < kn; ++kk) {
                 float2 av[TM], bv[TN];
 #pragma unroll
                 for (int r = 0; r < TM; ++r) av[r] = As[kk][ty + r * (BM / TM)];
