@@ -20,9 +20,10 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int FMT>
+// NB: a bound on n (4, 8 or 16) that sizes the unrolled column loops.
+template <int FMT, int NB>
 __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_constant__ StreamArgs a) {
-    __shared__ float2 Bs[kStreamMaxN * kStreamKc];
+    __shared__ float2 Bs[NB * kStreamKc];
     pdl_trigger();
     pdl_wait();
     const int s = blockIdx.y;
@@ -38,9 +39,9 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
     // accumulators per row, B staged chunk by chunk
     for (int64_t rb = r0; rb < r1; rb += groups) {
         const int64_t r = rb + g;
-        float2 acc[kStreamMaxN];
+        float2 acc[NB];
 #pragma unroll
-        for (int j = 0; j < kStreamMaxN; ++j) acc[j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < NB; ++j) acc[j] = make_float2(0.f, 0.f);
         for (int64_t c0 = k0; c0 < k1; c0 += kStreamKc) {
             const int clen = (int)min((int64_t)kStreamKc, k1 - c0);
             // this lane's first eight entries of the row are in flight while
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
                         const int idx = kb + u * lanes;
                         if (idx < clen) {
 #pragma unroll
-                            for (int j = 0; j < kStreamMaxN; ++j)
+                            for (int j = 0; j < NB; ++j)
                                 if (j < n) cfma(acc[j], av[u], Bs[j * kStreamKc + idx]);
                         }
                     }
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
         // combine the lanes of a row
         for (int off = lanes >> 1; off > 0; off >>= 1) {
 #pragma unroll
-            for (int j = 0; j < kStreamMaxN; ++j) {
+            for (int j = 0; j < NB; ++j) {
                 if (j < n) {
                     acc[j].x += __shfl_down_sync(0xffffffffu, acc[j].x, off, lanes);
                     acc[j].y += __shfl_down_sync(0xffffffffu, acc[j].y, off, lanes);
@@ -94,12 +95,12 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
             if (a.ksplit > 1) {
                 float2 *dst = a.part + ((int64_t)s * a.m + r) * a.n;
 #pragma unroll
-                for (int j = 0; j < kStreamMaxN; ++j)
+                for (int j = 0; j < NB; ++j)
                     if (j < n) dst[j] = acc[j];
             } else {
                 const int64_t offm = sep_offset(a.lm, r);
 #pragma unroll
-                for (int j = 0; j < kStreamMaxN; ++j)
+                for (int j = 0; j < NB; ++j)
                     if (j < n)
                         store_entry_t<FMT>(a.C, a.m * a.n, offm + sep_offset(a.ln, j), acc[j],
                                            a.accumulate, a.out_tile);
@@ -296,6 +297,17 @@ __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_co
     }
 }
 
+template <int NB>
+cudaError_t launch_stream_nb(const StreamArgs &args, dim3 grid, cudaStream_t stream) {
+    if (args.out_fmt == FMT_SPLIT4)
+        return launch_pdl(stream_node_kernel<FMT_SPLIT4, NB>, grid, dim3(kThreads), 0, stream, args);
+    else if (args.out_fmt == FMT_GAUSS6)
+        return launch_pdl(stream_node_kernel<FMT_GAUSS6, NB>, grid, dim3(kThreads), 0, stream, args);
+    else if (args.out_fmt == FMT_BF2)
+        return launch_pdl(stream_node_kernel<FMT_BF2, NB>, grid, dim3(kThreads), 0, stream, args);
+    return launch_pdl(stream_node_kernel<FMT_C64, NB>, grid, dim3(kThreads), 0, stream, args);
+}
+
 }  // namespace
 
 cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
@@ -323,13 +335,9 @@ cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
     }
     const int64_t blocks = (args.m + args.rows_per_cta - 1) / args.rows_per_cta;
     dim3 grid((unsigned)blocks, (unsigned)args.ksplit);
-    if (args.out_fmt == FMT_SPLIT4)
-        return launch_pdl(stream_node_kernel<FMT_SPLIT4>, grid, dim3(kThreads), 0, stream, args);
-    else if (args.out_fmt == FMT_GAUSS6)
-        return launch_pdl(stream_node_kernel<FMT_GAUSS6>, grid, dim3(kThreads), 0, stream, args);
-    else if (args.out_fmt == FMT_BF2)
-        return launch_pdl(stream_node_kernel<FMT_BF2>, grid, dim3(kThreads), 0, stream, args);
-    return launch_pdl(stream_node_kernel<FMT_C64>, grid, dim3(kThreads), 0, stream, args);
+    if (args.n <= 4) return launch_stream_nb<4>(args, grid, stream);
+    if (args.n <= 8) return launch_stream_nb<8>(args, grid, stream);
+    return launch_stream_nb<16>(args, grid, stream);
 }
 
 cudaError_t launch_splitk_reduce(const ReduceArgs &args, cudaStream_t stream) {
