@@ -86,6 +86,7 @@ SIGNATURES = {
     "tn_execute_static": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_set_replay": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_plan_set_three_products": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_plan_set_hoisting": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_execute_slices": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P, ctypes.c_uint64,
                                          ctypes.c_uint64]),
     "tn_execute_host": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(_P), _P, _P]),
@@ -251,6 +252,10 @@ def tn_plan_set_three_products(plan: int, enable: bool) -> None:
     _check(lib().tn_plan_set_three_products(plan, 1 if enable else 0), plan)
 
 
+def tn_plan_set_hoisting(plan: int, enable: bool) -> None:
+    _check(lib().tn_plan_set_hoisting(plan, 1 if enable else 0), plan)
+
+
 def tn_plan_check(plan: int) -> None:
     _check(lib().tn_plan_check(plan), plan)
 
@@ -327,6 +332,10 @@ class Plan:
 
     def set_three_products(self, enable: bool) -> None:
         tn_plan_set_three_products(self.handle, enable)
+        self._ws = None
+
+    def set_hoisting(self, enable: bool) -> None:
+        tn_plan_set_hoisting(self.handle, enable)
         self._ws = None
 
     def bind_workspace(self, device=None):

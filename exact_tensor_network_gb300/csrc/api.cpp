@@ -136,6 +136,12 @@ tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable) {
     return tn::layout_plan(&plan->p);
 }
 
+tn_status tn_plan_set_hoisting(tn_plan_t *plan, int32_t enable) {
+    if (!plan) return TN_EINVAL;
+    plan->p.hoist = enable ? 1 : 0;
+    return tn::layout_plan(&plan->p);
+}
+
 tn_status tn_plan_workspace_bytes(const tn_plan_t *plan, uint64_t *bytes) {
     if (!plan || !bytes) return TN_EINVAL;
     *bytes = plan->p.ws_bytes;

@@ -148,9 +148,21 @@ void choose_split(const Plan &p, NodePlan &nd) {
 // last splits alone took longer than kernel plus reduction).
 bool fused_reduction(const NodePlan &nd) { return nd.cls == TN_NODE_STREAM && nd.ksplit > 1; }
 
-uint64_t launches_per_slice(const Plan &p) {
-    uint64_t n = (p.perm_table.size() + kPermBatch - 1) / kPermBatch;
-    for (const auto &L : p.sched) {
+// The program a slice runs: the whole schedule (the first slice of an
+// execute, or every slice without hoisting) or the variant launches only.
+struct Program {
+    const std::vector<Launch> &sched;
+    const std::vector<int32_t> &jobs;   // perm_table entries
+};
+Program program(const Plan &p, bool first) {
+    if (first || !(p.hoist && p.n_slices > 1)) return {p.sched, p.perm_all};
+    return {p.sched_rest, p.perm_rest};
+}
+
+uint64_t launches_of(const Plan &p, bool first) {
+    const Program g = program(p, first);
+    uint64_t n = (g.jobs.size() + kPermBatch - 1) / kPermBatch;
+    for (const auto &L : g.sched) {
         if (L.kind == LAUNCH_TINY) ++n;
         if (L.kind == LAUNCH_NODE) n += fused_reduction(p.nodes[L.node]) ? 1 : p.nodes[L.node].ksplit > 1 ? 2 : 1;
     }
@@ -245,14 +257,16 @@ bool conflict(const Access &e, const Access &l) {
     return overlap(e.wr, l.rd) || overlap(e.wr, l.wr) || overlap(e.rd, l.wr);
 }
 
-// Accesses of one slice's launches, in the order execute_range issues them.
-std::vector<Access> slice_accesses(const Plan &p) {
+// Accesses of one slice's launches (the first slice's program or a later
+// one's), in the order execute_range issues them.
+std::vector<Access> slice_accesses(const Plan &p, bool first) {
+    const Program g = program(p, first);
     std::vector<Access> acc;
-    const int njobs = (int)p.perm_table.size();
+    const int njobs = (int)g.jobs.size();
     for (int j0 = 0; j0 < njobs; j0 += kPermBatch) {
         Access a;
         for (int j = j0; j < std::min(njobs, j0 + kPermBatch); ++j) {
-            const PermDesc &d = p.perm_table[j];
+            const PermDesc &d = p.perm_table[g.jobs[j]];
             if (d.dst_off < 0) a.wr.push_back({-1, -1});
             else a.wr.push_back({d.dst_off, d.dst_off + d.size * (int64_t)fmt_bytes(d.fmt)});
         }
@@ -260,7 +274,7 @@ std::vector<Access> slice_accesses(const Plan &p) {
     }
     const TinyDesc *tiny = reinterpret_cast<const TinyDesc *>(
         p.table_blob.data() + (p.tiny_off - p.table_off));
-    for (const Launch &L : p.sched) {
+    for (const Launch &L : g.sched) {
         if (L.kind == LAUNCH_PERMUTE) continue;
         if (L.kind == LAUNCH_TINY) {
             Access a;
@@ -335,11 +349,16 @@ struct Dag {
 
 // Dependencies and streams of all launches of slices first, first + step, ...
 tn_status build_dag(Plan *p, cudaStream_t origin, uint64_t first, uint64_t step, Dag *d) {
-    const std::vector<Access> one = slice_accesses(*p);
-    const size_t P = one.size();
-    uint64_t nsl = 0;
-    for (uint64_t s = first; s < p->n_slices; s += step) ++nsl;
-    const size_t N = P * nsl;
+    // every launch of the range in issue order: the first slice's program,
+    // then the later slices'
+    std::vector<Access> all;
+    if (first < p->n_slices) {
+        all = slice_accesses(*p, true);
+        const std::vector<Access> later = slice_accesses(*p, false);
+        for (uint64_t s = first + step; s < p->n_slices; s += step)
+            all.insert(all.end(), later.begin(), later.end());
+    }
+    const size_t N = all.size();
     while (p->lane_streams.size() < (size_t)kLanes - 1) {
         cudaStream_t s;
         cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
@@ -366,7 +385,7 @@ tn_status build_dag(Plan *p, cudaStream_t origin, uint64_t first, uint64_t step,
         std::fill(last.begin(), last.end(), -1);
         bool any = false;
         for (size_t e = 0; e < i; ++e)
-            if (conflict(one[e % P], one[i % P])) {
+            if (conflict(all[e], all[i])) {
                 last[d->lane[e]] = std::max(last[d->lane[e]], (int)e);
                 any = true;
             }
@@ -495,6 +514,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
 
     for (uint64_t sigma = first; sigma < p->n_slices && st == TN_OK; sigma += step) {
         const bool later = sigma != first;   // add into the output
+        const Program g = program(*p, !later);
         // slice digits, first slice mode most significant
         uint64_t rem = sigma;
         for (int i = nsl - 1; i >= 0; --i) {
@@ -507,7 +527,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             leaf_src[t] = static_cast<const float2 *>(leaf_ptrs[t]) + off;
         }
         // leaf permutations, batched
-        const int njobs = (int)p->perm_table.size();
+        const int njobs = (int)g.jobs.size();
         for (int j0 = 0; j0 < njobs; j0 += kPermBatch) {
             const int cnt = std::min(kPermBatch, njobs - j0);
             pl->njobs = cnt;
@@ -517,14 +537,15 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             pl->out = out;
             int ctas = 0;
             for (int j = 0; j < cnt; ++j) {
-                pl->job[j] = j0 + j;
+                const int32_t job = g.jobs[j0 + j];
+                pl->job[j] = job;
                 pl->cta_start[j] = ctas;
-                pl->src[j] = leaf_src[p->perm_leaves[j0 + j]];
-                ctas += permute_ctas(p->perm_table[j0 + j].size);
+                pl->src[j] = leaf_src[p->perm_leaves[job]];
+                ctas += permute_ctas(p->perm_table[job].size);
             }
             pl->cta_start[cnt] = ctas;
             uint64_t bytes = 0;
-            for (int j = 0; j < cnt; ++j) bytes += 16 * (uint64_t)p->perm_table[j0 + j].size;
+            for (int j = 0; j < cnt; ++j) bytes += 16 * (uint64_t)p->perm_table[g.jobs[j0 + j]].size;
             rec.begin(TN_KERNEL_PERMUTE, -1, 0, bytes);
             cudaError_t e = launch_permute(*pl, ctas, dag ? dag->begin() : stream);
             if (dag) dag->end();
@@ -535,7 +556,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             }
         }
         if (st != TN_OK) break;
-        for (const Launch &L : p->sched) {
+        for (const Launch &L : g.sched) {
             if (L.kind == LAUNCH_PERMUTE) continue;   // issued above
             if (L.kind == LAUNCH_TINY) {
                 TinyLaunch tl;

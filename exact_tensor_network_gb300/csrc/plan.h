@@ -313,6 +313,7 @@ struct Plan {
     // execution layout
     int32_t policy = TN_POLICY_AUTO;
     int32_t three_products = 0;   // tn_plan_set_three_products
+    int32_t hoist = 1;            // tn_plan_set_hoisting
     uint64_t table_off = 0, table_bytes = 0;    // PermDesc table
     uint64_t arena_off = 0, arena_bytes = 0;
     uint64_t ws_bytes = 0;
@@ -320,6 +321,14 @@ struct Plan {
     std::vector<int32_t> perm_leaves;           // leaf of each table entry
     std::vector<unsigned char> table_blob;      // device tables: PermDesc[], EpTable[], TinyDesc[]
     std::vector<Launch> sched;                  // launches of one slice, in order
+    // Slice-invariant hoisting (with slices and hoist set): a tensor is
+    // variant when a sliced leaf lies below it.  The first slice an execute
+    // runs takes `sched` and every leaf job; later slices take `sched_rest`
+    // (the variant launches) and `perm_rest` (the variant leaves' jobs),
+    // since the invariant tensors they read are still in the arena.
+    std::vector<uint8_t> variant;               // per SSA id
+    std::vector<Launch> sched_rest;
+    std::vector<int32_t> perm_all, perm_rest;   // perm_table entries of each program
     uint64_t tiny_off = 0;                      // workspace offset of the TinyDesc table
     std::vector<int32_t> fmt;                   // per SSA id (Fmt)
     std::vector<DenseMaps> dense_maps;          // per dense node, set at bind

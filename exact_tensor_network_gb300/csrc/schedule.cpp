@@ -22,7 +22,7 @@ namespace tn {
 
 int classify(const Plan &p, const NodePlan &nd);   // exec.cu
 void choose_split(const Plan &p, NodePlan &nd);    // exec.cu
-uint64_t launches_per_slice(const Plan &p);        // exec.cu
+uint64_t launches_of(const Plan &p, bool first);  // exec.cu
 
 namespace {
 
@@ -218,34 +218,58 @@ tn_status layout_plan(Plan *p) {
     }
     std::vector<std::vector<int>> by_stage(max_stage + 1);
     for (int s = 0; s < S; ++s) by_stage[stage[n + s]].push_back(s);
+    // Slice-invariant subtrees (section 1.1 of "Crossing the single-GPU
+    // memory wall": slicing repeats every node once per slice, although a
+    // node whose subtree holds no sliced leaf computes the same tensor in
+    // every slice).  With hoisting, later slices run only the variant
+    // launches.
+    p->variant.assign(n + S, 0);
+    for (int t = 0; t < n; ++t) p->variant[t] = p->leaves[t].slice_terms.empty() ? 0 : 1;
+    for (const auto &nd : p->nodes) p->variant[nd.out] = p->variant[nd.a] | p->variant[nd.b];
+    const bool hoist = p->hoist && p->n_slices > 1;
     p->sched.clear();
+    p->sched_rest.clear();
     std::vector<int> t_of(n + S, -1);   // launch index producing each id
-    std::vector<std::vector<int>> tiny_batches;
-    for (int st = 1; st <= max_stage; ++st) {
-        std::vector<int> tiny;
-        for (int s : by_stage[st])
-            if (p->nodes[s].cls == TN_NODE_TINY) tiny.push_back(s);
-        // batches of at most kTinyLaunchNodes nodes (independent launches)
-        for (size_t b0 = 0; b0 < tiny.size(); b0 += kTinyLaunchNodes) {
-            const size_t b1 = std::min(tiny.size(), b0 + (size_t)kTinyLaunchNodes);
-            Launch L{};
-            L.kind = LAUNCH_TINY;
-            L.node = -1;
-            for (size_t x = b0; x < b1; ++x) t_of[n + tiny[x]] = (int)p->sched.size();
-            tiny_batches.emplace_back(tiny.begin() + b0, tiny.begin() + b1);
-            p->sched.push_back(L);
+    std::vector<std::vector<int>> tiny_batches, tiny_batches_rest;
+    // one program: stage by stage, the stage's tiny nodes in batches of at
+    // most kTinyLaunchNodes (independent launches), then its other nodes
+    auto build = [&](std::vector<Launch> &sched, std::vector<std::vector<int>> &batches, bool rest) {
+        for (int st = 1; st <= max_stage; ++st) {
+            std::vector<int> tiny, other;
+            for (int s : by_stage[st]) {
+                if (rest && !p->variant[n + s]) continue;
+                (p->nodes[s].cls == TN_NODE_TINY ? tiny : other).push_back(s);
+            }
+            for (size_t b0 = 0; b0 < tiny.size(); b0 += kTinyLaunchNodes) {
+                const size_t b1 = std::min(tiny.size(), b0 + (size_t)kTinyLaunchNodes);
+                Launch L{};
+                L.kind = LAUNCH_TINY;
+                L.node = -1;
+                if (!rest)
+                    for (size_t x = b0; x < b1; ++x) t_of[n + tiny[x]] = (int)sched.size();
+                batches.emplace_back(tiny.begin() + b0, tiny.begin() + b1);
+                sched.push_back(L);
+            }
+            for (int s : other) {
+                Launch L{};
+                L.kind = LAUNCH_NODE;
+                L.node = s;
+                if (!rest) t_of[n + s] = (int)sched.size();
+                sched.push_back(L);
+            }
         }
-        for (int s : by_stage[st]) {
-            if (p->nodes[s].cls == TN_NODE_TINY) continue;
-            Launch L{};
-            L.kind = LAUNCH_NODE;
-            L.node = s;
-            t_of[n + s] = (int)p->sched.size();
-            p->sched.push_back(L);
-        }
-    }
+    };
+    build(p->sched, tiny_batches, false);
+    if (hoist) build(p->sched_rest, tiny_batches_rest, true);
     auto consume_t = [&](int id) { return p->consumer[id] < 0 ? (int)p->sched.size()
                                                                : t_of[n + p->consumer[id]]; };
+    // an invariant tensor that a variant node reads is written by the first
+    // slice and read by every later one: it stays live for the whole run
+    auto pinned = [&](int id) {
+        return hoist && !p->variant[id] && p->consumer[id] >= 0 &&
+               p->variant[p->nodes[p->consumer[id]].out];
+    };
+    const int run_end = (int)p->sched.size() + 1;
 
     // 4. lifetimes and placement
     std::vector<Interval> iv;
@@ -258,14 +282,19 @@ tn_status layout_plan(Plan *p) {
         } else if (lp.in_place) {
             lp.place = {PLACE_LEAF, t, 0};
         } else {
-            iv.push_back({(uint64_t)lp.size * fmt_bytes(p->fmt[t]), -1, consume_t(t), t, 0});
+            iv.push_back({(uint64_t)lp.size * fmt_bytes(p->fmt[t]), -1,
+                          pinned(t) ? run_end : consume_t(t), t, 0});
         }
     }
     for (int s = 0; s < S; ++s) {
         const NodePlan &nd = p->nodes[s];
         const int ts = t_of[n + s];
-        if (!nd.is_root)
-            iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), ts, consume_t(nd.out), nd.out, 0});
+        if (!nd.is_root) {
+            if (pinned(nd.out))
+                iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), -1, run_end, nd.out, 0});
+            else
+                iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), ts, consume_t(nd.out), nd.out, 0});
+        }
         if (part_bytes(nd) > 0) iv.push_back({part_bytes(nd), ts, ts, n + S + s, 0});
     }
     p->arena_bytes = place_buffers(iv);
@@ -288,13 +317,22 @@ tn_status layout_plan(Plan *p) {
             p->perm_leaves.push_back(t);
         }
     }
-    if (!p->perm_table.empty()) {
+    p->perm_all.clear();
+    p->perm_rest.clear();
+    for (int j = 0; j < (int)p->perm_table.size(); ++j) {
+        p->perm_all.push_back(j);
+        if (hoist && p->variant[p->perm_leaves[j]]) p->perm_rest.push_back(j);
+    }
+    auto perm_launch = [&](const std::vector<int32_t> &jobs, std::vector<Launch> &sched) {
+        if (jobs.empty()) return;
         Launch L{};
         L.kind = LAUNCH_PERMUTE;
         L.node = -1;
-        for (const auto &d : p->perm_table) L.bytes += 16 * (uint64_t)d.size;
-        p->sched.insert(p->sched.begin(), L);
-    }
+        for (int j : jobs) L.bytes += 16 * (uint64_t)p->perm_table[j].size;
+        sched.insert(sched.begin(), L);
+    };
+    perm_launch(p->perm_all, p->sched);
+    if (hoist) perm_launch(p->perm_rest, p->sched_rest);
     for (int s = 0; s < S; ++s) {
         NodePlan &nd = p->nodes[s];
         if (nd.is_root) where[nd.out] = {PLACE_OUT, -1, 0};
@@ -324,49 +362,56 @@ tn_status layout_plan(Plan *p) {
         nd.ep_off = (int64_t)(p->table_off + ep_start + eps.size() * sizeof(EpTable));
         eps.push_back(t);
     }
+    // tiny-node descriptors of each program's batches (the later slices'
+    // batches hold fewer nodes: their own descriptors and CTA bases)
     std::vector<TinyDesc> tiny;
-    size_t batch = 0;
-    for (auto &L : p->sched) {
-        if (L.kind != LAUNCH_TINY) continue;
-        L.first = (int32_t)tiny.size();
-        L.count = (int32_t)tiny_batches[batch].size();
-        int ctas = 0;
-        for (int s : tiny_batches[batch]) {
-            const NodePlan &nd = p->nodes[s];
-            TinyDesc d;
-            std::memset(&d, 0, sizeof(d));
-            d.a_off = (int64_t)nd.pa.off;
-            d.b_off = (int64_t)nd.pb.off;
-            d.c_off = nd.pc.kind == PLACE_OUT ? -1 : (int64_t)nd.pc.off;
-            d.m = (int32_t)nd.m;
-            d.n = (int32_t)nd.n;
-            d.k = (int32_t)nd.k;
-            d.out_fmt = nd.out_fmt;
-            d.out_tile = nd.out_tile;
-            d.is_root = nd.is_root ? 1 : 0;
-            const uint64_t macs = nd.m * nd.n * nd.k;
-            // `lanes` threads per output; enough CTAs that each group of a CTA
-            // computes at most two outputs (the rounds are serial memory waits)
-            // (a lane covers up to 16 entries of k per round of loads)
-            d.lanes = 1;
-            while (d.lanes < 32 && (uint64_t)d.lanes * 16 < nd.k) d.lanes *= 2;
-            const uint64_t per_cta = 2 * (256 / (uint64_t)d.lanes);
-            d.ctas = (int32_t)std::max<uint64_t>(1, (nd.m * nd.n + per_cta - 1) / per_cta);
-            d.cta_base = ctas;
-            if (!make_walk(nd, &d)) return TN_ENOTIMPL;   // outputs are dense: not reached
-            ctas += d.ctas;
-            L.flops += 8 * macs;
-            L.bytes += 8 * (nd.m * nd.k + nd.n * nd.k + nd.m * nd.n);
-            tiny.push_back(d);
+    auto describe = [&](std::vector<Launch> &sched, const std::vector<std::vector<int>> &batches) {
+        size_t batch = 0;
+        for (auto &L : sched) {
+            if (L.kind == LAUNCH_NODE) {
+                const NodePlan &nd = p->nodes[L.node];
+                L.flops = 8 * nd.m * nd.n * nd.k;
+            }
+            if (L.kind != LAUNCH_TINY) continue;
+            L.first = (int32_t)tiny.size();
+            L.count = (int32_t)batches[batch].size();
+            int ctas = 0;
+            for (int s : batches[batch]) {
+                const NodePlan &nd = p->nodes[s];
+                TinyDesc d;
+                std::memset(&d, 0, sizeof(d));
+                d.a_off = (int64_t)nd.pa.off;
+                d.b_off = (int64_t)nd.pb.off;
+                d.c_off = nd.pc.kind == PLACE_OUT ? -1 : (int64_t)nd.pc.off;
+                d.m = (int32_t)nd.m;
+                d.n = (int32_t)nd.n;
+                d.k = (int32_t)nd.k;
+                d.out_fmt = nd.out_fmt;
+                d.out_tile = nd.out_tile;
+                d.is_root = nd.is_root ? 1 : 0;
+                const uint64_t macs = nd.m * nd.n * nd.k;
+                // `lanes` threads per output (a lane covers up to 16 entries
+                // of k per round of loads); enough CTAs that each group of a
+                // CTA computes at most two outputs (the rounds are serial
+                // memory waits)
+                d.lanes = 1;
+                while (d.lanes < 32 && (uint64_t)d.lanes * 16 < nd.k) d.lanes *= 2;
+                const uint64_t per_cta = 2 * (256 / (uint64_t)d.lanes);
+                d.ctas = (int32_t)std::max<uint64_t>(1, (nd.m * nd.n + per_cta - 1) / per_cta);
+                d.cta_base = ctas;
+                if (!make_walk(nd, &d)) return false;   // outputs are dense: not reached
+                ctas += d.ctas;
+                L.flops += 8 * macs;
+                L.bytes += 8 * (nd.m * nd.k + nd.n * nd.k + nd.m * nd.n);
+                tiny.push_back(d);
+            }
+            L.ctas = ctas;
+            ++batch;
         }
-        L.ctas = ctas;
-        ++batch;
-    }
-    for (auto &L : p->sched) {
-        if (L.kind != LAUNCH_NODE) continue;
-        const NodePlan &nd = p->nodes[L.node];
-        L.flops = 8 * nd.m * nd.n * nd.k;
-    }
+        return true;
+    };
+    if (!describe(p->sched, tiny_batches) || !describe(p->sched_rest, tiny_batches_rest))
+        return TN_ENOTIMPL;
     const uint64_t tiny_start = align_up(ep_start + eps.size() * sizeof(EpTable));
     p->tiny_off = p->table_off + tiny_start;
     // tail-tile counters (zero; every run leaves them zero again)
@@ -393,7 +438,8 @@ tn_status layout_plan(Plan *p) {
     p->table_bytes = align_up(p->table_blob.size());
     p->arena_off = p->table_off + p->table_bytes;
     p->ws_bytes = p->arena_off + p->arena_bytes;
-    p->launches_per_exec = launches_per_slice(*p) * p->n_slices;
+    p->launches_per_exec = launches_of(*p, true) +
+                           (p->n_slices - 1) * launches_of(*p, !(p->hoist && p->n_slices > 1));
     p->dense_maps.clear();
     p->maps_ws = nullptr;
     p->ws = nullptr;

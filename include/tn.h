@@ -283,6 +283,22 @@ TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);
  */
 TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
 
+/*
+ * Slice-invariant hoisting ("Crossing the single-GPU memory wall", section
+ * 1.1: slicing repeats the whole contraction once per slice; a node none of
+ * whose leaves carries a sliced mode computes the same tensor in every
+ * slice).  With `enable` = 1 (the default) the first slice an execute runs
+ * takes every launch and each later slice only the launches that depend on
+ * a sliced leaf; invariant intermediates that those launches read stay in
+ * the workspace for the whole execute (the workspace may grow: query
+ * tn_plan_workspace_bytes again).  Results are those of the plain slice
+ * loop; tn_plan_launches counts the launches of one execute either way.
+ * No effect without slices.  Re-plans the layout (like tn_plan_set_policy):
+ * bind the workspace again afterwards.
+ * Errors: TN_EINVAL (NULL plan).
+ */
+TN_API tn_status tn_plan_set_hoisting(tn_plan_t *plan, int32_t enable);
+
 /* After the stream has been synchronised: read and clear the device status
  * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or
  * TN_ETIMEOUT (a bounded wait inside a kernel gave up). */

@@ -118,6 +118,39 @@ def test_slice_shards_add_up():
     assert_close(total.cpu().numpy(), _ref(net, tree), what="sum of 3 slice shards")
 
 
+@pytest.mark.parametrize("case", ["random_40", "circuit_4x4"])
+def test_hoisting_matches_plain_slice_loop(case):
+    """Slice-invariant hoisting (later slices rerun only the launches that
+    depend on a sliced leaf) and the plain slice loop both match the oracle,
+    over three replayed executes; hoisting launches less."""
+    import torch
+    import exact_tensor_network_gb300 as tn
+    if case == "random_40":
+        net = random_network(40, 2)
+        tree = greedy_tree(net, 0)
+        sl = choose_slices(net, tree, largest_intermediate(net, tree) // 8)[:3]
+    else:
+        net, _ = grid_circuit_network(4, 4, 8, 3)
+        tree = greedy_tree(net, 0)
+        sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
+    ref = _ref(net, tree)
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    launches = {}
+    for hoist in (True, False):
+        plan = tn.Plan.from_network(net, tree, sl)
+        plan.set_hoisting(hoist)
+        assert plan.num_slices > 1
+        out = torch.full(plan.out_shape, complex(7.0, -3.0), dtype=torch.complex64, device=dev)
+        for _ in range(3):
+            plan.execute(leaves, out)
+        torch.cuda.synchronize(dev)
+        plan.check()
+        launches[hoist] = plan.launches
+        assert_close(out.cpu().numpy().astype(np.complex128), ref, what=f"{case} hoisting={hoist}")
+    assert launches[True] < launches[False]
+
+
 def test_repeated_execute_overwrites():
     net, tree, _ = configs.circuit_3x3_d4()
     got, _ = run_gpu(net, tree, repeat=3)

@@ -133,3 +133,24 @@ def test_single_leaf_and_scalar_plans():
     h = tn.tn_plan([[], [0]], [3], [0], [(0, 1)])
     assert tn.tn_plan_node_mnk(h, 0) == (1, 3, 1)
     tn.tn_plan_destroy(h)
+
+
+def test_hoisting_launch_counts():
+    """Hoisting: the first slice runs every launch, each later slice the
+    variant ones only; without slices the setting changes nothing."""
+    net, _ = grid_circuit_network(4, 4, 8, 3)
+    tree = greedy_tree(net, 0)
+    sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
+    p = tn.Plan.from_network(net, tree, sl)
+    ns = p.num_slices
+    assert ns > 1
+    on = p.launches
+    p.set_hoisting(False)
+    off = p.launches
+    assert off % ns == 0
+    per = off // ns
+    assert on < off and (on - per) % (ns - 1) == 0 and (on - per) // (ns - 1) < per
+    u = tn.Plan.from_network(net, tree)
+    a = u.launches
+    u.set_hoisting(False)
+    assert u.launches == a
