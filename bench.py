@@ -57,6 +57,8 @@ def kernel_peak(kernel: str, pk):
         return "tensor", tf32 / 3.0, "TFLOP/s", f"3xTF32-effective = bf16 {pk['source']} x {TF32_PER_BF16:.3f} / 3"
     if kernel == "dense_bf16":
         return "tensor", pk["bf16_tflops"], "TFLOP/s", f"bf16 dense, {pk['source']}"
+    if kernel == "dense_bf16x3":
+        return "tensor", pk["bf16_tflops"] / 3.0, "TFLOP/s", f"split-bf16-effective = bf16 {pk['source']} / 3"
     if kernel in ("simt", "tiny"):
         alu = SMS * FP32_LANES * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
         return "alu", alu, "TFLOP/s", "fp32 FMA: 152 SMs x 128 lanes x 2 x max SM clock"
@@ -66,6 +68,7 @@ def kernel_peak(kernel: str, pk):
 KERNEL_SOURCES = {
     "dense_tf32x3": ["k_dense.cu", "common.cuh"],
     "dense_bf16": ["k_dense.cu", "common.cuh"],
+    "dense_bf16x3": ["k_dense.cu", "common.cuh"],
 }
 
 
@@ -488,7 +491,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="random_60")
-    ap.add_argument("--precision", default="tf32x3", choices=["tf32x3", "bf16", "fp32"])
+    ap.add_argument("--precision", default="tf32x3", choices=["tf32x3", "bf16", "bf16x3", "fp32"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--leaves", choices=["host", "device"], default="host",

@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libtn_gb300.so")
 # status codes (tn_status)
 TN_OK, TN_EINVAL, TN_ENOMEM, TN_EOVERFLOW, TN_ECUDA, TN_EDEVICE, TN_ETIMEOUT, TN_ENOTIMPL = range(8)
 # precisions
-TN_PREC_TF32X3, TN_PREC_BF16, TN_PREC_FP32 = 0, 1, 2
-PRECISIONS = {"tf32x3": TN_PREC_TF32X3, "bf16": TN_PREC_BF16, "fp32": TN_PREC_FP32}
+TN_PREC_TF32X3, TN_PREC_BF16, TN_PREC_FP32, TN_PREC_BF16X3 = 0, 1, 2, 3
+PRECISIONS = {"tf32x3": TN_PREC_TF32X3, "bf16": TN_PREC_BF16, "fp32": TN_PREC_FP32,
+              "bf16x3": TN_PREC_BF16X3}
 # node classes
 TN_NODE_SIMT, TN_NODE_DENSE, TN_NODE_STREAM, TN_NODE_TINY = 0, 1, 2, 3
 NODE_CLASS_NAMES = {0: "simt", 1: "dense", 2: "stream", 3: "tiny"}
@@ -55,7 +56,7 @@ class tn_launch_record(ctypes.Structure):
 
 
 KERNEL_NAMES = {0: "permute", 1: "simt", 2: "dense_tf32x3", 3: "dense_bf16", 4: "stream", 5: "tiny",
-                6: "reduce", 7: "dense_tf32x3_3p"}
+                6: "reduce", 7: "dense_tf32x3_3p", 8: "dense_bf16x3"}
 
 
 class tn_slices(ctypes.Structure):

@@ -103,6 +103,23 @@ __device__ __forceinline__ void store_gauss6(float *p, int64_t plane, float2 v) 
     p[5 * plane] = to_tf32(sum - sh);
 }
 
+// x as a bf16 pair: hi = x rounded to bf16, lo = (x - hi) rounded to bf16
+// (x - hi is exact in fp32).
+__device__ __forceinline__ void bf16_split(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
+    hi = __float2bfloat16_rn(x);
+    lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ void store_bf4(__nv_bfloat16 *p, int64_t plane, float2 v) {
+    __nv_bfloat16 rh, rl, ih, il;
+    bf16_split(v.x, rh, rl);
+    bf16_split(v.y, ih, il);
+    p[0] = rh;
+    p[plane] = ih;
+    p[2 * plane] = rl;
+    p[3 * plane] = il;
+}
+
 // Store entry `off` of a tensor in the compile-time format FMT (see Fmt in
 // plan.h); planes are `plane` entries apart.  `accumulate` adds into a C64
 // destination.  Kernels instantiated per format keep one store path.
@@ -127,6 +144,8 @@ __device__ __forceinline__ void store_entry_t(void *dst, int64_t plane, int64_t 
         p[3 * plane] = to_tf32(v.y - ih);
     } else if constexpr (FMT == FMT_GAUSS6) {
         store_gauss6(static_cast<float *>(dst) + off, plane, v);
+    } else if constexpr (FMT == FMT_BF4) {
+        store_bf4(static_cast<__nv_bfloat16 *>(dst) + off, plane, v);
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         p[0] = __float2bfloat16_rn(v.x);
@@ -155,6 +174,8 @@ __device__ __forceinline__ void store_entry(void *dst, int32_t fmt, int64_t plan
         p[3 * plane] = to_tf32(v.y - ih);
     } else if (fmt == FMT_GAUSS6) {
         store_gauss6(static_cast<float *>(dst) + off, plane, v);
+    } else if (fmt == FMT_BF4) {
+        store_bf4(static_cast<__nv_bfloat16 *>(dst) + off, plane, v);
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         p[0] = __float2bfloat16_rn(v.x);
@@ -211,6 +232,24 @@ __device__ __forceinline__ void store_quad(void *dst, int32_t fmt, int64_t plane
 #pragma unroll
         for (int c = 0; c < 6; ++c)
             *reinterpret_cast<float4 *>(p + c * plane) = make_float4(q[c][0], q[c][1], q[c][2], q[c][3]);
+    } else if (fmt == FMT_BF4) {
+        // planes re_hi, im_hi, re_lo, im_lo: four bf16 (8 bytes) each
+        __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
+        __nv_bfloat16 q[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            bf16_split(v[t].x, q[0][t], q[2][t]);
+            bf16_split(v[t].y, q[1][t], q[3][t]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const __nv_bfloat162 x0 = __halves2bfloat162(q[c][0], q[c][1]);
+            const __nv_bfloat162 x1 = __halves2bfloat162(q[c][2], q[c][3]);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t *>(&x0);
+            w.y = *reinterpret_cast<const uint32_t *>(&x1);
+            *reinterpret_cast<uint2 *>(p + c * plane) = w;
+        }
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(dst) + off;
         __nv_bfloat162 re0 = __halves2bfloat162(__float2bfloat16_rn(v[0].x), __float2bfloat16_rn(v[1].x));

@@ -25,15 +25,16 @@ namespace tn {
 int classify(const Plan &p, const NodePlan &nd) {
     if (p.policy == TN_POLICY_SIMT) return TN_NODE_SIMT;
     const bool bf16 = p.precision == TN_PREC_BF16;
+    const bool bf16x3 = p.precision == TN_PREC_BF16X3;
     const bool fp32 = p.precision == TN_PREC_FP32;
-    const uint64_t kq = bf16 ? 8 : 4;
+    const uint64_t kq = bf16 || bf16x3 ? 8 : 4;   // 16-byte rows of a TMA box
     if (p.policy == TN_POLICY_DENSE)
         return (!fp32 && nd.k % kq == 0) ? TN_NODE_DENSE : TN_NODE_SIMT;
     if (p.policy == TN_POLICY_AUTO && nd.m * nd.n * nd.k <= kTinyMacs && nd.k <= kTinyMaxK &&
         nd.m * nd.n <= kTinyMaxOut)
         return TN_NODE_TINY;
     if (!fp32 && nd.k % kq == 0 && nd.k >= 16 && nd.m >= 64 && nd.n >= 64) {
-        const double in_b = bf16 ? 4.0 : 16.0;
+        const double in_b = bf16 ? 4.0 : bf16x3 ? 8.0 : 16.0;
         const double m = (double)nd.m, n = (double)nd.n, k = (double)nd.k;
         const double intensity = 8.0 * m * n * k / (in_b * (m * k + n * k) + 8.0 * m * n);
         if (intensity >= 24.0) return TN_NODE_DENSE;
@@ -615,6 +616,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->out_tile = nd.out_tile;
                 d->ktiled = nd.ktiled;
                 d->bf16 = p->precision == TN_PREC_BF16;
+                d->bf16x3 = p->precision == TN_PREC_BF16X3;
                 d->three = nd.three_products;
                 d->status = status;
                 d->ksplit = nd.ksplit;
@@ -625,8 +627,9 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->tail_cnt = nd.tail_first >= 0 ? reinterpret_cast<int32_t *>(ws + nd.tail_cnt_off)
                                                  : nullptr;
                 const uint64_t in_b = fmt_bytes(p->fmt[nd.a]);
-                rec.begin(d->bf16 ? TN_KERNEL_DENSE_BF16
-                                  : d->three ? TN_KERNEL_DENSE_TF32X3_3P : TN_KERNEL_DENSE_TF32X3,
+                rec.begin(d->bf16x3 ? TN_KERNEL_DENSE_BF16X3
+                          : d->bf16 ? TN_KERNEL_DENSE_BF16
+                          : d->three ? TN_KERNEL_DENSE_TF32X3_3P : TN_KERNEL_DENSE_TF32X3,
                           nd.step, flops,
                           in_b * (nd.m * nd.k + nd.n * nd.k) +
                               fmt_bytes(nd.out_fmt) * nd.m * nd.n * (accumulate ? 2 : 1));

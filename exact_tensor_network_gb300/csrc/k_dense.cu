@@ -69,18 +69,22 @@ static_assert(4 * 32 * REGS_LOW + DRAIN_WARPS * 32 * REGS_HIGH <= THREADS * 168,
               "register split exceeds the launch's registers");
 
 // Kernel modes: split tf32 with four real products per complex product,
-// bf16 operands (four products), split tf32 with three products.
-enum : int { MODE_TF32 = 0, MODE_BF16 = 1, MODE_TF32_3P = 2 };
+// bf16 operands (four products), split tf32 with three products, split
+// bf16 (hi and lo bf16 parts, the products hi*hi + hi*lo + lo*hi like the
+// split tf32 mode, on the bf16 tensor path).
+enum : int { MODE_TF32 = 0, MODE_BF16 = 1, MODE_TF32_3P = 2, MODE_BF16X3 = 3 };
 
 template <int MODE>
 struct Cfg {
     static constexpr bool BF16 = MODE == MODE_BF16;
     static constexpr bool THREE = MODE == MODE_TF32_3P;
-    // planes per operand: [re, im] (bf16), [re_hi, im_hi, re_lo, im_lo],
-    // or [re_hi, im_hi, s_hi, re_lo, im_lo, s_lo] (s = re + im)
+    static constexpr bool HALF = MODE == MODE_BF16 || MODE == MODE_BF16X3;   // bf16 entries
+    // planes per operand: [re, im] (bf16), [re_hi, im_hi, re_lo, im_lo]
+    // (tf32 or bf16 parts), or [re_hi, im_hi, s_hi, re_lo, im_lo, s_lo]
+    // (s = re + im)
     static constexpr int PLANES = BF16 ? 2 : THREE ? 6 : 4;
-    static constexpr int KB = BF16 ? 32 : 16;           // complex k per stage
-    static constexpr int K_INSTR = BF16 ? 16 : 8;       // k per MMA instruction
+    static constexpr int KB = HALF ? 32 : 16;           // complex k per stage
+    static constexpr int K_INSTR = HALF ? 16 : 8;       // k per MMA instruction
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
     static constexpr int STAGE_BYTES = 2 * PLANES * PLANE_TILE;
     static constexpr int STAGES = BF16 ? 6 : THREE ? 2 : 3;
@@ -99,15 +103,16 @@ struct Cfg {
     static constexpr uint32_t MMA_N = THREE ? 128 : 256;
     // instruction descriptor without N: D f32, A/B tf32 (2) or bf16 (1),
     // both K-major, M = 128; idesc(N) adds N
-    static constexpr uint32_t IDESC_BASE = (1u << 4) | ((BF16 ? 1u : 2u) << 7) |
-                                           ((BF16 ? 1u : 2u) << 10) | ((128u >> 4) << 24);
+    static constexpr uint32_t IDESC_BASE = (1u << 4) | ((HALF ? 1u : 2u) << 7) |
+                                           ((HALF ? 1u : 2u) << 10) | ((128u >> 4) << 24);
     static constexpr uint32_t idesc(uint32_t n) { return IDESC_BASE | ((n >> 3) << 17); }
 };
 constexpr int MAX_STAGES = 8;   // barrier slots (narrow bf16 tiles: 8 stages)
-static_assert(Cfg<MODE_BF16>::NARROW_STAGES <= MAX_STAGES && Cfg<MODE_TF32>::NARROW_STAGES <= MAX_STAGES,
+static_assert(Cfg<MODE_BF16>::NARROW_STAGES <= MAX_STAGES && Cfg<MODE_TF32>::NARROW_STAGES <= MAX_STAGES &&
+                  Cfg<MODE_BF16X3>::NARROW_STAGES <= MAX_STAGES,
               "barrier slots");
 static_assert(Cfg<MODE_TF32_3P>::SMEM <= 232448 && Cfg<MODE_TF32>::SMEM <= 232448 &&
-                  Cfg<MODE_BF16>::SMEM <= 232448,
+                  Cfg<MODE_BF16>::SMEM <= 232448 && Cfg<MODE_BF16X3>::SMEM <= 232448,
               "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -197,7 +202,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 
 template <int MODE>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc, uint32_t idesc) {
-    if constexpr (MODE == MODE_BF16) {
+    if constexpr (Cfg<MODE>::HALF) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
@@ -750,9 +755,11 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
         }
         return launch_pdl(kernel, dim3(grid), dim3(THREADS), (size_t)smem, stream, args);
     };
-    static bool attr_bf16 = false, attr_tf32 = false, attr_3p = false;
+    static bool attr_bf16 = false, attr_tf32 = false, attr_3p = false, attr_bf16x3 = false;
     cudaError_t e;
-    if (args.bf16)
+    if (args.bf16x3)
+        e = launch(dense_kernel<MODE_BF16X3>, Cfg<MODE_BF16X3>::SMEM, &attr_bf16x3);
+    else if (args.bf16)
         e = launch(dense_kernel<MODE_BF16>, Cfg<MODE_BF16>::SMEM, &attr_bf16);
     else if (args.three)
         e = launch(dense_kernel<MODE_TF32_3P>, Cfg<MODE_TF32_3P>::SMEM, &attr_3p);
@@ -763,7 +770,7 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
 
 bool encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t k, int32_t fmt,
                         bool tiled, int32_t box_rows, std::string *err) {
-    const bool bf16 = fmt == FMT_BF2;
+    const bool bf16 = fmt_bf16(fmt);
     const cuuint64_t planes = static_cast<cuuint64_t>(fmt_planes(fmt));
     if (planes == 0) {
         *err = "operand is not in a planar format";

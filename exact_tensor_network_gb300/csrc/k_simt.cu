@@ -123,6 +123,8 @@ cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream) {
         return launch_pdl(simt_node_kernel<FMT_GAUSS6>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_BF2)
         return launch_pdl(simt_node_kernel<FMT_BF2>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
+    else if (args.out_fmt == FMT_BF4)
+        return launch_pdl(simt_node_kernel<FMT_BF4>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
     return launch_pdl(simt_node_kernel<FMT_C64>, dim3((unsigned)grid), dim3(kThreads), 0, stream, args);
 }
 

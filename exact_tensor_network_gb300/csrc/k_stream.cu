@@ -305,6 +305,8 @@ cudaError_t launch_stream_nb(const StreamArgs &args, dim3 grid, cudaStream_t str
         return launch_pdl(stream_node_kernel<FMT_GAUSS6, NB>, grid, dim3(kThreads), 0, stream, args);
     else if (args.out_fmt == FMT_BF2)
         return launch_pdl(stream_node_kernel<FMT_BF2, NB>, grid, dim3(kThreads), 0, stream, args);
+    else if (args.out_fmt == FMT_BF4)
+        return launch_pdl(stream_node_kernel<FMT_BF4, NB>, grid, dim3(kThreads), 0, stream, args);
     return launch_pdl(stream_node_kernel<FMT_C64, NB>, grid, dim3(kThreads), 0, stream, args);
 }
 

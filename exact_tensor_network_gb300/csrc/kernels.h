@@ -104,6 +104,7 @@ struct DenseArgs {
     int32_t out_fmt;
     PlanarTile out_tile;
     int32_t bf16;         // operands are FMT_BF2
+    int32_t bf16x3;       // operands are FMT_BF4 (split bf16)
     int32_t three;        // operands are FMT_GAUSS6: three real products
     int32_t narrow;       // 128 x 64 tiles (B boxes of 64 rows, MMA N = 128)
     int32_t ktiled;       // operands K-tiled (4-D maps) rather than row-major (3-D)

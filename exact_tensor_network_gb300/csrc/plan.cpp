@@ -79,7 +79,7 @@ tn_status build_plan(const tn_network *net, const tn_tree *tree, const tn_slices
     if (!net->ranks || !net->modes) return fail(TN_EINVAL, "ranks/modes is NULL");
     if (net->n_open < 0 || (net->n_open > 0 && !net->open_modes))
         return fail(TN_EINVAL, "bad open-mode list");
-    if (net->precision < TN_PREC_TF32X3 || net->precision > TN_PREC_FP32)
+    if (net->precision < TN_PREC_TF32X3 || net->precision > TN_PREC_BF16X3)
         return fail(TN_EINVAL, "unknown precision");
     p->n_tensors = n;
     p->n_modes = net->n_modes;

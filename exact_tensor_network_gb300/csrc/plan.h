@@ -53,14 +53,19 @@ inline int32_t log2_exact(int64_t e) {
 //               with s = re + im (rounded in fp32), split as in FMT_SPLIT4
 //               (24 bytes per entry): operands of nodes that form the
 //               complex product from three real products (see NodePlan)
-enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2, FMT_GAUSS6 = 3 };
+//   FMT_BF4:    four bf16 planes [re_hi, im_hi, re_lo, im_lo]; hi = x
+//               rounded to bf16 (nearest even), lo = (x - hi) rounded to
+//               bf16 (8 bytes per entry): the split-bf16 precision
+enum Fmt : int32_t { FMT_C64 = 0, FMT_SPLIT4 = 1, FMT_BF2 = 2, FMT_GAUSS6 = 3, FMT_BF4 = 4 };
 inline uint64_t fmt_bytes(int32_t f) {
-    return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : f == FMT_GAUSS6 ? 24 : 8;
+    return f == FMT_SPLIT4 ? 16 : f == FMT_BF2 ? 4 : f == FMT_GAUSS6 ? 24 : 8;   // C64, BF4: 8
 }
 // Planes of a planar format.
 inline int32_t fmt_planes(int32_t f) {
-    return f == FMT_SPLIT4 ? 4 : f == FMT_BF2 ? 2 : f == FMT_GAUSS6 ? 6 : 0;
+    return f == FMT_SPLIT4 || f == FMT_BF4 ? 4 : f == FMT_BF2 ? 2 : f == FMT_GAUSS6 ? 6 : 0;
 }
+// Planar formats with bf16 entries.
+inline bool fmt_bf16(int32_t f) { return f == FMT_BF2 || f == FMT_BF4; }
 
 // K-tiling of a planar operand.  The consumer reads the operand as a
 // row-major [rows][k] matrix; with kt > 0 each plane is stored as
@@ -77,7 +82,7 @@ struct PlanarTile {
 
 // Entries per K tile for a planar format (64 bytes of one row).
 inline int32_t planar_kt(int32_t fmt) {
-    return fmt == FMT_BF2 ? 32 : (fmt == FMT_SPLIT4 || fmt == FMT_GAUSS6) ? 16 : 0;
+    return fmt_bf16(fmt) ? 32 : (fmt == FMT_SPLIT4 || fmt == FMT_GAUSS6) ? 16 : 0;
 }
 
 // Where a tensor lives during execution.

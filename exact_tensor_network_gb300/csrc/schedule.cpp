@@ -180,7 +180,9 @@ tn_status layout_plan(Plan *p) {
 
     // 2. formats
     p->fmt.assign(n + S, FMT_C64);
-    const int32_t dense_fmt = p->precision == TN_PREC_BF16 ? FMT_BF2 : FMT_SPLIT4;
+    const int32_t dense_fmt = p->precision == TN_PREC_BF16     ? FMT_BF2
+                              : p->precision == TN_PREC_BF16X3 ? FMT_BF4
+                                                               : FMT_SPLIT4;
     for (auto &nd : p->nodes) {
         nd.three_products = 0;
         if (nd.cls != TN_NODE_DENSE) continue;

@@ -60,7 +60,14 @@ enum {
                            accumulated in fp32 (fp32-level accuracy) */
     TN_PREC_BF16 = 1,   /* tensor-core operands rounded to bf16 (round to
                            nearest even), fp32 accumulation */
-    TN_PREC_FP32 = 2    /* every node on CUDA-core fp32 FMA */
+    TN_PREC_FP32 = 2,   /* every node on CUDA-core fp32 FMA */
+    TN_PREC_BF16X3 = 3  /* split bf16: x = hi + lo (hi = x rounded to bf16,
+                           lo = x - hi rounded to bf16, 16 significant bits);
+                           products hi*hi + hi*lo + lo*hi on the bf16 tensor
+                           path accumulated in fp32: half the tensor-core time
+                           and operand bytes of TN_PREC_TF32X3, about 32 times
+                           its representation error (2^-17 against 2^-22 of
+                           each operand entry) */
 };
 
 /* Node classes reported by tn_plan_node_class and forced by
@@ -315,7 +322,8 @@ enum {
     TN_KERNEL_STREAM = 4,       /* bandwidth-bound node kernel */
     TN_KERNEL_TINY = 5,         /* batched tiny-node kernel */
     TN_KERNEL_REDUCE = 6,       /* ordered sum of split-K partials */
-    TN_KERNEL_DENSE_TF32X3_3P = 7 /* tcgen05 node kernel, split tf32, three real products */
+    TN_KERNEL_DENSE_TF32X3_3P = 7, /* tcgen05 node kernel, split tf32, three real products */
+    TN_KERNEL_DENSE_BF16X3 = 8     /* tcgen05 node kernel, split bf16 */
 };
 
 /* One kernel launch of a profiled tn_execute.  flops = 8 m n k of the

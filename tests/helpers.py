@@ -4,6 +4,10 @@ import numpy as np
 
 TOL_C64 = 1e-5     # max |gpu - ref| <= TOL * max |ref| for complex64 paths
 TOL_BF16 = 2e-2    # bf16 tensor-core operands
+# split bf16 (hi + lo keep 16 significant bits; lo*lo dropped): at most
+# 3 * 2^-16 = 4.6e-5 of |a||b| per product, random-signed over k, and
+# compounded through a chain of nodes
+TOL_BF16X3 = 2e-4
 
 
 def run_gpu(net, tree, slices=(), precision="tf32x3", policy=0, out_dtype=None, repeat=1):

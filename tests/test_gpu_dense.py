@@ -14,7 +14,7 @@ import oracle
 from workloads import configs, gemm_network
 from workloads.network import Network
 
-from helpers import TOL_BF16, TOL_C64, assert_close, run_gpu
+from helpers import TOL_BF16, TOL_BF16X3, TOL_C64, assert_close, max_rel_err, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,8 @@ def _classes(net, tree, slices=(), precision="tf32x3", policy=NT):
     return [p.node_class(s) for s in range(len(tree))]
 
 
-@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16),
+                                           ("bf16x3", TOL_BF16X3)])
 @pytest.mark.parametrize("lm,ln,lk", [(8, 8, 8), (7, 8, 10), (9, 7, 6), (8, 8, 12), (10, 9, 5),
                                       (8, 8, 14)])
 def test_gemm_networks(precision, tol, lm, ln, lk):
@@ -64,7 +65,8 @@ def test_gemm_networks(precision, tol, lm, ln, lk):
     assert_close(got, _ref(net, [(0, 1)]), tol, f"gemm {lm},{ln},{lk} {precision}")
 
 
-@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16),
+                                           ("bf16x3", TOL_BF16X3)])
 @pytest.mark.parametrize("m,n,k", [(200, 100, 40), (129, 65, 24), (64, 300, 136), (1000, 77, 48),
                                    (128, 128, 16), (333, 250, 1000), (1, 1, 8), (5, 300, 8),
                                    (300, 3, 520)])
@@ -117,7 +119,8 @@ def test_interleaved_output_general_extents(ext):
     assert_close(got, _ref(net, tree), TOL_C64, f"interleaved {ext}")
 
 
-@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16),
+                                           ("bf16x3", TOL_BF16X3)])
 def test_dense_chain(precision, tol):
     # A[a,x] B[x,b] -> C[a,b] (dense, planar output), C[a,b] D[b,c] -> root (dense)
     rng = np.random.default_rng(9)
@@ -131,7 +134,8 @@ def test_dense_chain(precision, tol):
     assert_close(got, _ref(net, tree), tol, f"dense chain {precision}")
 
 
-@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16),
+                                           ("bf16x3", TOL_BF16X3)])
 @pytest.mark.parametrize("m,n,k", [(128, 256, 16384), (64, 4096, 2048), (300, 200, 3000)])
 def test_dense_split_k(precision, tol, m, n, k):
     """Few output tiles and long k: the tensor-core kernel splits k across
@@ -193,6 +197,20 @@ def test_transposed_root_order():
     assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "reversed root order")
 
 
+def test_split_bf16_accuracy_between_bf16_and_tf32x3():
+    """The split-bf16 precision on random_60 (every node class writing the
+    four-plane bf16 format for its tensor-core consumers): its error lies
+    between those of the split-tf32 and plain bf16 precisions."""
+    net, tree, _ = configs.random_60()
+    ref = _ref(net, tree)
+    err = {}
+    for prec in ("tf32x3", "bf16x3", "bf16"):
+        got, _ = run_gpu(net, tree, precision=prec)
+        err[prec] = max_rel_err(got, ref)
+    assert err["bf16x3"] <= TOL_BF16X3, err
+    assert err["tf32x3"] < err["bf16x3"] < err["bf16"], err
+
+
 def test_random_60_uses_dense_nodes_and_matches():
     net, tree, _ = configs.random_60()
     cls = _classes(net, tree)
@@ -205,6 +223,7 @@ def test_random_60_uses_dense_nodes_and_matches():
     (64, 128, "tf32x3", TOL_C64),     # power-of-two extents: store table in tiled addresses
     (72, 96, "tf32x3", TOL_C64),      # k = 6144: tiled, offsets tiled entry by entry
     (64, 128, "bf16", TOL_BF16),
+    (64, 128, "bf16x3", TOL_BF16X3),
 ])
 def test_dense_output_k_tiled_for_dense_consumer(p_ext, a_ext, precision, tol):
     # A[p,a,x] B[y,x] -> C[p,a,y] (tensor cores), then C[p,a,y] D[q,a,y] -> root[p,q]
@@ -258,6 +277,7 @@ def test_dense_root_output_not_16_byte_aligned():
     (2048, 1280, 512, "tf32x3", TOL_C64),     # 160 tiles: 8 past the last full wave
     (2000, 1300, 528, "tf32x3", TOL_C64),     # ragged tiles, 33 k-blocks: halves of 16 and 17
     (2048, 1280, 544, "bf16", TOL_BF16),      # bf16: 17 k-blocks
+    (2048, 1280, 544, "bf16x3", TOL_BF16X3),  # split bf16: 17 k-blocks
 ])
 def test_dense_tail_tiles_split_in_k_halves(m, n, k, precision, tol):
     """Tiles past the last full wave run as two k halves on two CTAs; the
@@ -314,6 +334,8 @@ def test_three_product_nodes(m, n, k):
     (200, 48, 1040, "tf32x3", tn.TN_POLICY_DENSE, TOL_C64),    # ragged narrow tiles
     (30, 300, 96, "tf32x3", tn.TN_POLICY_DENSE, TOL_C64),      # swapped, ragged on both sides
     (64, 4096, 2048, "bf16", NT, TOL_BF16),                    # bf16: eight 24 KiB stages
+    (64, 4096, 2048, "bf16x3", NT, TOL_BF16X3),                # split bf16: four 48 KiB stages
+    (64, 1024, 8192, "bf16x3", NT, TOL_BF16X3),                # split bf16, K-tiled, narrow
 ])
 def test_dense_narrow_tiles(m, n, k, precision, policy, tol):
     """A node with a side of at most 64 runs 128 x 64 tiles: that side goes

@@ -154,3 +154,13 @@ def test_hoisting_launch_counts():
     a = u.launches
     u.set_hoisting(False)
     assert u.launches == a
+
+
+def test_precision_codes():
+    """Split bf16 (3) plans like the other precisions; unknown codes fail."""
+    net = gemm_network(8, 8, 8, 0)
+    h = tn.tn_plan(net.tensors, net.extents, net.open_modes, [(0, 1)], (), tn.TN_PREC_BF16X3)
+    assert tn.tn_plan_node_class(h, 0) == tn.TN_NODE_DENSE
+    tn.tn_plan_destroy(h)
+    with pytest.raises(RuntimeError):
+        tn.tn_plan(net.tensors, net.extents, net.open_modes, [(0, 1)], (), 4)
