@@ -185,7 +185,9 @@ __global__ void __launch_bounds__(kThreads) stream_node_kernel(const __grid_cons
 template <int K>
 __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_constant__ StreamArgs a) {
     constexpr int RPT = 16 / K;   // rows per thread and pass
-    __shared__ float2 Bs[kStreamMaxN * K];
+    __shared__ __align__(16) float2 Bs[kStreamMaxN * K];
+    // B read two entries (16 bytes, the same address in every lane) at a time
+    const float4 *Bs2 = reinterpret_cast<const float4 *>(Bs);
     __shared__ int64_t offn_s[kStreamMaxN];
     // row-major [m, n] outputs: each warp's 32 rows are one contiguous run,
     // staged here and stored by consecutive lanes
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
             const int lane = threadIdx.x & 31;
             float2 *tile = Cs[threadIdx.x >> 5];
             const int ts = n | 1;   // odd row stride: lanes' rows in distinct banks
+            const int dr = 32 / n, dc = 32 - dr * n;
 #pragma unroll
             for (int u = 0; u < RPT; ++u) {
                 const int64_t r = base + u * kThreads + threadIdx.x;
@@ -233,18 +236,29 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
                     for (int j = 0; j < n; ++j) {
                         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int kk = 0; kk < K; ++kk) cfma(acc, av[u][kk], Bs[j * K + kk]);
+                        for (int kk = 0; kk < K; kk += 2) {
+                            const float4 b2 = Bs2[(j * K + kk) >> 1];
+                            cfma(acc, av[u][kk], make_float2(b2.x, b2.y));
+                            cfma(acc, av[u][kk + 1], make_float2(b2.z, b2.w));
+                        }
                         tile[lane * ts + j] = acc;
                     }
                 }
                 __syncwarp();
                 const int64_t r0 = base + u * kThreads + (threadIdx.x & ~31);
                 const int64_t cnt = r0 < a.m ? min((int64_t)32, a.m - r0) * n : 0;
+                // entry e = rr n + cc of the warp's run; e steps by 32
+                int rr = lane / n, cc = lane - rr * n;
 #pragma unroll 1
                 for (int e = lane; e < (int)cnt; e += 32) {
-                    const int rr = e / n;
-                    store_entry(a.C, a.out_fmt, a.m * a.n, r0 * n + e, tile[rr * ts + (e - rr * n)],
+                    store_entry(a.C, a.out_fmt, a.m * a.n, r0 * n + e, tile[rr * ts + cc],
                                 a.accumulate, a.out_tile);
+                    rr += dr;
+                    cc += dc;
+                    if (cc >= n) {
+                        cc -= n;
+                        ++rr;
+                    }
                 }
                 __syncwarp();
             }
@@ -259,7 +273,11 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
             for (int j = 0; j < n; ++j) {
                 float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int kk = 0; kk < K; ++kk) cfma(acc, av[u][kk], Bs[j * K + kk]);
+                for (int kk = 0; kk < K; kk += 2) {
+                    const float4 b2 = Bs2[(j * K + kk) >> 1];
+                    cfma(acc, av[u][kk], make_float2(b2.x, b2.y));
+                    cfma(acc, av[u][kk + 1], make_float2(b2.z, b2.w));
+                }
                 store_entry(a.C, a.out_fmt, a.m * a.n, offm + offn_s[j], acc, a.accumulate,
                             a.out_tile);
             }
