@@ -400,6 +400,12 @@ class Plan:
                         [t.data_ptr() for t in dev_leaves], dev_out.data_ptr(), sp)
         stream.synchronize()
 
+    def prepare_host(self, host_leaves, host_out, dev_leaves, dev_out, stream=None) -> "HostCall":
+        """The same call as execute_host for buffers fixed in advance:
+        checked and turned into pointer arrays once, so that each call of
+        the returned object costs only tn_execute_host and the wait."""
+        return HostCall(self, host_leaves, host_out, dev_leaves, dev_out, stream)
+
     def check(self) -> None:
         tn_plan_check(self.handle)
 
@@ -412,3 +418,34 @@ class Plan:
 
     def profile(self):
         return tn_plan_profile_read(self.handle)
+
+
+class HostCall:
+    """A prepared tn_execute_host call (Plan.prepare_host): the buffers are
+    checked once and held, their pointers kept in C arrays; calling the
+    object runs leaves in, contraction, result out and waits for the
+    stream.  The buffers must keep their storage while the object is used."""
+
+    def __init__(self, plan: Plan, host_leaves, host_out, dev_leaves, dev_out, stream=None):
+        import torch
+        if plan._ws is None:
+            plan.bind_workspace(dev_out.device)
+        for t in list(host_leaves) + [host_out]:
+            if t.dtype != torch.complex64 or not t.is_contiguous() or t.is_cuda:
+                raise ValueError("host leaves and host_out must be contiguous complex64 CPU tensors")
+        for t in list(dev_leaves) + [dev_out]:
+            if t.dtype != torch.complex64 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("dev_leaves and dev_out must be contiguous complex64 CUDA tensors")
+        self.plan = plan
+        self.buffers = (list(host_leaves), host_out, list(dev_leaves), dev_out)   # held alive
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev_out.device)
+        self._sp = self.stream.cuda_stream if hasattr(self.stream, "cuda_stream") else int(self.stream)
+        self._h = (_P * max(len(host_leaves), 1))(*[t.data_ptr() for t in host_leaves])
+        self._d = (_P * max(len(dev_leaves), 1))(*[t.data_ptr() for t in dev_leaves])
+        self._ho, self._do = host_out.data_ptr(), dev_out.data_ptr()
+        self._fn = lib().tn_execute_host
+
+    def __call__(self) -> None:
+        _check(self._fn(self.plan.handle, self._h, self._ho, self._d, self._do, self._sp),
+               self.plan.handle)
+        self.stream.synchronize()

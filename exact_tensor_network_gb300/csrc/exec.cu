@@ -173,6 +173,9 @@ uint64_t launches_of(const Plan &p, bool first) {
 void drop_graph(Plan *p) {
     if (p->graph_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->graph_exec));
     p->graph_exec = nullptr;
+    if (p->host_graph_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->host_graph_exec));
+    p->host_graph_exec = nullptr;
+    p->hg_key.clear();
     p->graph_leaves.clear();
     p->graph_out = nullptr;
     p->graph_ws = nullptr;
@@ -797,27 +800,12 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
     return TN_OK;
 }
 
-// tn_execute_host: the caller's host leaves into its device leaf buffers
-// (pinned leaves through one gather kernel over their device mappings,
-// others by cudaMemcpyAsync), the contraction, the result back to the host.
-tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
-                       void *const *dev_leaves, void *dev_out, cudaStream_t stream) {
+// The host call's work on `stream`: leaves in (one gather kernel for
+// pinned leaves, a copy for each pageable one), the contraction (replayed,
+// or with a recorder its launches), the result out.
+tn_status issue_host(Plan *p, const void *const *host_leaves, void *host_out, void *const *dev_leaves,
+                     void *dev_out, cudaStream_t stream, Dag *dag) {
     const int n = p->n_tensors;
-    if ((int)p->host_leaves_seen.size() != n) {
-        p->host_leaves_seen.assign(n, nullptr);
-        p->host_leaves_dev.assign(n, nullptr);
-    }
-    for (int t = 0; t < n; ++t) {
-        if (p->host_leaves_seen[t] == host_leaves[t]) continue;
-        cudaPointerAttributes attr;
-        const void *dev = nullptr;
-        if (cudaPointerGetAttributes(&attr, host_leaves[t]) == cudaSuccess &&
-            attr.type == cudaMemoryTypeHost && attr.devicePointer)
-            dev = attr.devicePointer;
-        cudaGetLastError();   // pageable memory may report an error: not sticky
-        p->host_leaves_seen[t] = host_leaves[t];
-        p->host_leaves_dev[t] = dev;
-    }
     GatherLaunch *g = new GatherLaunch;
     g->njobs = 0;
     int ctas = 0;
@@ -848,12 +836,92 @@ tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
     if (e == cudaSuccess) flush();
     delete g;
     if (e != cudaSuccess) return cuda_fail(p, e, "copying the leaves in");
-    const tn_status st = execute_replayed(p, reinterpret_cast<const void *const *>(dev_leaves), dev_out,
-                                          stream);
+    const void *const *dl = reinterpret_cast<const void *const *>(dev_leaves);
+    tn_status st;
+    if (dag) {
+        // every lane joins back into `stream` before the result is copied
+        st = issue_range(p, dl, dev_out, stream, 0, 1, dag);
+        if (st == TN_OK && (dag->next != dag->lane.size() || !dag->join())) st = TN_ECUDA;
+    } else {
+        st = execute_replayed(p, dl, dev_out, stream);
+    }
     if (st != TN_OK) return st;
     e = cudaMemcpyAsync(host_out, dev_out, p->out_elems * sizeof(float2), cudaMemcpyDeviceToHost,
                         stream);
     return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "copying the result out");
+}
+
+// tn_execute_host: the caller's host leaves into its device leaf buffers
+// (pinned leaves through one gather kernel over their device mappings,
+// others by cudaMemcpyAsync), the contraction, the result back to the host.
+tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
+                       void *const *dev_leaves, void *dev_out, cudaStream_t stream) {
+    const int n = p->n_tensors;
+    if ((int)p->host_leaves_seen.size() != n) {
+        p->host_leaves_seen.assign(n, nullptr);
+        p->host_leaves_dev.assign(n, nullptr);
+    }
+    for (int t = 0; t < n; ++t) {
+        if (p->host_leaves_seen[t] == host_leaves[t]) continue;
+        cudaPointerAttributes attr;
+        const void *dev = nullptr;
+        if (cudaPointerGetAttributes(&attr, host_leaves[t]) == cudaSuccess &&
+            attr.type == cudaMemoryTypeHost && attr.devicePointer)
+            dev = attr.devicePointer;
+        cudaGetLastError();   // pageable memory may report an error: not sticky
+        p->host_leaves_seen[t] = host_leaves[t];
+        p->host_leaves_dev[t] = dev;
+    }
+    // the whole call as one recorded graph when every buffer on the host
+    // side is pinned (copies of pageable memory cannot be recorded)
+    bool pinned = true;
+    for (int t = 0; t < n; ++t)
+        if (p->leaves[t].full_size > 0 && !p->host_leaves_dev[t]) pinned = false;
+    if (pinned) {
+        cudaPointerAttributes attr;
+        pinned = cudaPointerGetAttributes(&attr, host_out) == cudaSuccess && attr.type == cudaMemoryTypeHost;
+        cudaGetLastError();
+    }
+    std::vector<const void *> key(host_leaves, host_leaves + n);
+    key.push_back(host_out);
+    key.insert(key.end(), dev_leaves, dev_leaves + n);
+    key.push_back(dev_out);
+    key.push_back(p->ws);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool record = pinned && p->use_graph && !p->profiling &&
+                        cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
+    cudaGetLastError();
+    if (record && p->host_graph_exec && p->hg_key == key) {
+        cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(p->host_graph_exec), stream);
+        return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "launching the recorded host call");
+    }
+    tn_status st = issue_host(p, host_leaves, host_out, dev_leaves, dev_out, stream, nullptr);
+    if (st != TN_OK || !record || !p->use_graph) return st;
+    // record the same call on the plan's capture stream for the next time
+    if (p->host_graph_exec) cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(p->host_graph_exec));
+    p->host_graph_exec = nullptr;
+    p->hg_key.clear();
+    if (!p->capture_stream) return TN_OK;   // created by the first replayed execute
+    cudaStream_t cs = static_cast<cudaStream_t>(p->capture_stream);
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return TN_OK;
+    }
+    Dag dag;
+    tn_status cst = build_dag(p, cs, 0, 1, &dag);
+    if (cst == TN_OK) cst = issue_host(p, host_leaves, host_out, dev_leaves, dev_out, cs, &dag);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(cs, &graph);
+    cudaGraphExec_t ex = nullptr;
+    if (cst == TN_OK && e == cudaSuccess && graph) e = cudaGraphInstantiate(&ex, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (cst != TN_OK || e != cudaSuccess || !ex) {
+        cudaGetLastError();   // keep issuing directly
+        return TN_OK;
+    }
+    p->host_graph_exec = ex;
+    p->hg_key = key;
+    return TN_OK;
 }
 
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len) {

@@ -356,6 +356,10 @@ struct Plan {
     // tn_execute_host: host leaf pointers seen last and their device mappings
     // (null: pageable, copied with cudaMemcpyAsync)
     std::vector<const void *> host_leaves_seen, host_leaves_dev;
+    // tn_execute_host with pinned leaves and output: the whole call (gather,
+    // contraction, copy out) recorded as one graph for these buffers
+    void *host_graph_exec = nullptr;
+    std::vector<const void *> hg_key;           // host leaves, host out, device leaves, device out, workspace
     std::vector<void *> dag_events;             // recording: one event per launch
     std::vector<const void *> graph_leaves;
     void *graph_out = nullptr;

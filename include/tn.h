@@ -263,7 +263,11 @@ TN_API tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs
  * mapping by one gather kernel for all of them; other leaves are copied one
  * cudaMemcpyAsync each (synchronous for pageable memory).  Asynchronous on
  * `stream` for pinned buffers: synchronise the stream before reading
- * host_out.  The host buffers must stay valid until then.
+ * host_out.  The host buffers must stay valid until then.  When every host
+ * buffer (leaves and host_out) is pinned and graph replay is on, the whole
+ * call (gather, contraction, copy out) is recorded after its first run and
+ * replayed by later calls with the same buffers and workspace; the buffers'
+ * contents are read afresh on every call.
  * Errors: as tn_execute; TN_EINVAL for NULL pointers.
  */
 TN_API tn_status tn_execute_host(tn_plan_t *plan, const void *const *host_leaves, void *host_out,

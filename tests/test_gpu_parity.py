@@ -392,8 +392,16 @@ def test_execute_from_host_buffers(pinned, case):
         host_out = host_out.pin_memory()
     dev_leaves = [torch.empty_like(h, device=dev) for h in host_leaves]
     dev_out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
-    for it in range(3):
+    for it in range(4):                        # direct, then recorded replays
+        if it == 3:
+            host_leaves[0].mul_(2.0)               # new values in the same buffer
+            ref = 2.0 * ref                        # the result is linear in each leaf
         host_out.fill_(complex(5.0, 5.0))
         plan.execute_host(host_leaves, host_out, dev_leaves, dev_out)
         assert_close(host_out.numpy().astype(np.complex128), ref, what=f"{case} call {it}")
+    call = plan.prepare_host(host_leaves, host_out, dev_leaves, dev_out)   # the prepared form
+    for it in range(2):
+        host_out.fill_(complex(5.0, 5.0))
+        call()
+        assert_close(host_out.numpy().astype(np.complex128), ref, what=f"{case} prepared call {it}")
     plan.check()
