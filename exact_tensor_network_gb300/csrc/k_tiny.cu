@@ -6,13 +6,14 @@
 // microseconds of launch and memory latency each, far more than their
 // arithmetic.  All tiny nodes of one schedule stage are independent, so one
 // launch runs them all: each node owns CTAs (its cta_base range in the
-// descriptor table), enough that every thread group computes at most two
-// outputs, since each output is a serial chain of memory waits; `lanes`
-// threads cooperate on one output's k range (k <= 512: at most two rounds of
-// loads) and combine with warp shuffles.  One lane decodes each output's
-// address into (i, j) and passes it to the lanes that compute it.  Operands are complex64 in the workspace arena; the
-// output goes through the node's separable offsets in its consumer's format
-// (the root adds into the caller's output on later slices).
+// descriptor table), enough that every thread group computes about one
+// output, since each output is a serial chain of memory waits; `lanes`
+// threads cooperate on one output's k range (k <= 512: one round of loads,
+// 16 entries per lane) and combine with warp shuffles.  One lane decodes
+// each output's address into (i, j) and passes it to the lanes that compute
+// it.  Operands are complex64 in the workspace arena; the output goes
+// through the node's separable offsets in its consumer's format (the root
+// adds into the caller's output on later slices).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -56,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) tiny_batch_kernel(const __grid_const
     const int lanes = d.lanes;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int opw = 32 / lanes;                        // outputs per warp and pass
-    const int chunk = opw * 2 < 32 ? opw * 2 : 32;     // outputs of one decode pass
+    const int chunk = opw;                             // outputs of one decode pass
     const int l = lane % lanes, gq = lane / lanes;
     const int accumulate = d.is_root ? a.accumulate_root : 0;
     const int k = d.k;

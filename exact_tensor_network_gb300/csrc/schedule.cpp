@@ -394,11 +394,11 @@ tn_status layout_plan(Plan *p) {
                 const uint64_t macs = nd.m * nd.n * nd.k;
                 // `lanes` threads per output (a lane covers up to 16 entries
                 // of k per round of loads); enough CTAs that each group of a
-                // CTA computes at most two outputs (the rounds are serial
-                // memory waits)
+                // CTA computes one output (the rounds are serial memory
+                // waits: one output per group measured faster than two)
                 d.lanes = 1;
                 while (d.lanes < 32 && (uint64_t)d.lanes * 16 < nd.k) d.lanes *= 2;
-                const uint64_t per_cta = 2 * (256 / (uint64_t)d.lanes);
+                const uint64_t per_cta = 256 / (uint64_t)d.lanes;
                 d.ctas = (int32_t)std::max<uint64_t>(1, (nd.m * nd.n + per_cta - 1) / per_cta);
                 d.cta_base = ctas;
                 if (!make_walk(nd, &d)) return false;   // outputs are dense: not reached
