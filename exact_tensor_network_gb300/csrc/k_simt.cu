@@ -26,6 +26,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_constant__ NodeArgs a) {
     __shared__ float2 As[BK][BM + 1];
     __shared__ float2 Bs[BK][BN + 1];
+    __shared__ int64_t offm_s[BM], offn_s[BN];   // the tile's row and column offsets
     pdl_trigger();
     pdl_wait();
     const int tid = threadIdx.x;
@@ -88,27 +89,34 @@ __global__ void __launch_bounds__(kThreads) simt_node_kernel(const __grid_consta
             }
             continue;
         }
-        int64_t offn[TN];
-#pragma unroll
-        for (int c = 0; c < TN; ++c) {
-            const int64_t j = j0 + tx + c * (BN / TN);
-            offn[c] = j < a.n ? sep_offset(a.ln, j) : 0;
+        // separable offsets of the tile's rows and columns, once per tile
+        for (int e = tid; e < BM + BN; e += kThreads) {
+            if (e < BM) {
+                const int64_t i = i0 + e;
+                offm_s[e] = i < a.m ? sep_offset(a.lm, i) : 0;
+            } else {
+                const int64_t j = j0 + (e - BM);
+                offn_s[e - BM] = j < a.n ? sep_offset(a.ln, j) : 0;
+            }
         }
+        __syncthreads();
         // rows rolled (the selects keep acc in registers): one copy of the
         // store code per column instead of one per entry
 #pragma unroll 1
         for (int r = 0; r < TM; ++r) {
             const int64_t i = i0 + ty + r * (BM / TM);
             if (i >= a.m) continue;
-            const int64_t offm = sep_offset(a.lm, i);
+            const int64_t offm = offm_s[ty + r * (BM / TM)];
 #pragma unroll
             for (int c = 0; c < TN; ++c) {
                 const int64_t j = j0 + tx + c * (BN / TN);
                 if (j >= a.n) continue;
                 const float2 v = r == 0 ? acc[0][c] : r == 1 ? acc[1][c] : r == 2 ? acc[2][c] : acc[3][c];
-                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn[c], v, a.accumulate, a.out_tile);
+                store_entry_t<FMT>(a.C, a.m * a.n, offm + offn_s[tx + c * (BN / TN)], v, a.accumulate,
+                                   a.out_tile);
             }
         }
+        __syncthreads();   // the next tile rewrites the offsets
     }
 }
 
