@@ -164,3 +164,20 @@ def test_precision_codes():
     tn.tn_plan_destroy(h)
     with pytest.raises(RuntimeError):
         tn.tn_plan(net.tensors, net.extents, net.open_modes, [(0, 1)], (), 4)
+
+
+def test_hoisting_workspace_and_replanning():
+    """Pinned invariant buffers can only add to the arena; re-planning (a
+    policy change) rebuilds both programs and keeps the hoisted count."""
+    net, _ = grid_circuit_network(4, 4, 8, 3)
+    tree = greedy_tree(net, 0)
+    sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
+    p = tn.Plan.from_network(net, tree, sl)
+    on_ws, on_l = p.workspace_bytes, p.launches
+    p.set_hoisting(False)
+    assert p.workspace_bytes <= on_ws and p.launches > on_l
+    p.set_hoisting(True)
+    assert (p.workspace_bytes, p.launches) == (on_ws, on_l)
+    p.set_policy(tn.TN_POLICY_NO_TINY)
+    p.set_policy(tn.TN_POLICY_AUTO)
+    assert (p.workspace_bytes, p.launches) == (on_ws, on_l)
