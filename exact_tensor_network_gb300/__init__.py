@@ -26,7 +26,11 @@ PRECISIONS = {"tf32x3": TN_PREC_TF32X3, "bf16": TN_PREC_BF16, "fp32": TN_PREC_FP
 TN_NODE_SIMT, TN_NODE_DENSE, TN_NODE_STREAM, TN_NODE_TINY = 0, 1, 2, 3
 NODE_CLASS_NAMES = {0: "simt", 1: "dense", 2: "stream", 3: "tiny"}
 # policies
-TN_POLICY_AUTO, TN_POLICY_SIMT, TN_POLICY_NO_TINY, TN_POLICY_DENSE = 0, 1, 2, 3
+TN_POLICY_AUTO, TN_POLICY_SIMT, TN_POLICY_NO_TINY = 0, 1, 2
+# test setting outside the C ABI: every node the tensor-core kernel can take
+# goes there (deep chains of such nodes are not held to the complex64
+# tolerance)
+TN_POLICY_DENSE = 3
 
 
 class TNError(RuntimeError):
@@ -92,6 +96,8 @@ SIGNATURES = {
                                          ctypes.c_uint64]),
     "tn_execute_host": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(_P), _P, _P]),
     "tn_plan_check": (ctypes.c_int, [_P]),
+    "tn_execute_prefix": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, ctypes.c_int32, _P]),
+    "tn_plan_tensor_gather": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_uint64, _P, _P]),
     "tn_plan_launches": (ctypes.c_int, [_P, _U64P]),
     "tn_plan_set_profiling": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_plan_profile_read": (ctypes.c_int, [_P, ctypes.POINTER(tn_launch_record), ctypes.c_int32,
@@ -235,6 +241,17 @@ def tn_execute_host(plan: int, host_leaf_ptrs: Sequence[int], host_out: int,
     _check(lib().tn_execute_host(plan, h, host_out, d, dev_out, stream), plan)
 
 
+def tn_execute_prefix(plan: int, leaf_ptrs: Sequence[int], out_ptr: int, step: int,
+                      stream: int = 0) -> None:
+    arr = (_P * max(len(leaf_ptrs), 1))(*leaf_ptrs)
+    _check(lib().tn_execute_prefix(plan, arr, out_ptr, step, stream), plan)
+
+
+def tn_plan_tensor_gather(plan: int, tensor_id: int, idx_ptr: int, count: int, dst_ptr: int,
+                          stream: int = 0) -> None:
+    _check(lib().tn_plan_tensor_gather(plan, tensor_id, idx_ptr, count, dst_ptr, stream), plan)
+
+
 def shard_slices(n_slices: int, rank: int, world: int) -> Tuple[int, int, int]:
     """Slices of rank `rank` among `world` processes: (first, step, count)
     with slices first, first + step, ... below n_slices (round robin).  The
@@ -289,6 +306,32 @@ def tn_last_error(plan: Optional[int] = None) -> str:
 
 # ---- convenience wrapper over torch tensors --------------------------------
 
+def _prod(xs) -> int:
+    r = 1
+    for x in xs:
+        r *= x
+    return r
+
+
+def _check_buffers(plan: "Plan", leaves, out, on_device: bool, what: str) -> None:
+    """dtype, contiguity, device side and entry counts of the leaves and the
+    result against the plan (a short buffer would be read or written past
+    its end by the kernels)."""
+    import torch
+    if len(leaves) != plan.n_tensors:
+        raise ValueError(f"{what}: {len(leaves)} leaves given, the network has {plan.n_tensors}")
+    where = "CUDA" if on_device else "CPU"
+    for t in list(leaves) + [out]:
+        if t.dtype != torch.complex64 or not t.is_contiguous() or t.is_cuda != on_device:
+            raise ValueError(f"{what}: leaves and result must be contiguous complex64 {where} tensors")
+    for i, (t, size) in enumerate(zip(leaves, plan.leaf_sizes)):
+        if t.numel() != size:
+            raise ValueError(f"{what}: leaf {i} has {t.numel()} entries, its modes give {size}")
+    if out.numel() != plan.out_size:
+        raise ValueError(f"{what}: result has {out.numel()} entries, the open modes give "
+                         f"{plan.out_size}")
+
+
 class Plan:
     """Owns a plan handle and (optionally) a torch workspace tensor."""
 
@@ -297,7 +340,11 @@ class Plan:
         prec = PRECISIONS[precision] if isinstance(precision, str) else int(precision)
         self.handle = tn_plan(tensors, extents, open_modes, pairs, slices, prec)
         self.n_tensors = len(tensors)
+        self.pairs = [(int(a), int(b)) for a, b in pairs]
         self.out_shape = tuple(int(extents[x]) for x in open_modes)
+        # entries of every leaf (all its modes) and of the result
+        self.leaf_sizes = [_prod(int(extents[x]) for x in t) for t in tensors]
+        self.out_size = _prod(self.out_shape)
         self._ws = None
         if policy != TN_POLICY_AUTO:
             tn_plan_set_policy(self.handle, policy)
@@ -354,13 +401,9 @@ class Plan:
         ``out`` (complex64, open-mode order).  Asynchronous on ``stream``
         (default: torch's current stream)."""
         import torch
+        _check_buffers(self, leaves, out, True, "execute")
         if self._ws is None:
             self.bind_workspace(out.device)
-        if len(leaves) != self.n_tensors:
-            raise ValueError("wrong number of leaves")
-        for t in list(leaves) + [out]:
-            if t.dtype != torch.complex64 or not t.is_contiguous() or not t.is_cuda:
-                raise ValueError("leaves and out must be contiguous complex64 CUDA tensors")
         if stream is None:
             stream = torch.cuda.current_stream(out.device)
         sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -371,6 +414,7 @@ class Plan:
         tn_execute_slices); with shard_slices this splits a sliced
         contraction over processes."""
         import torch
+        _check_buffers(self, leaves, out, True, "execute_slices")
         if self._ws is None:
             self.bind_workspace(out.device)
         if stream is None:
@@ -385,16 +429,12 @@ class Plan:
         ``dev_leaves``, the contraction into ``dev_out``, the result into
         ``host_out``; then waits for the stream."""
         import torch
+        _check_buffers(self, host_leaves, host_out, False, "execute_host")
+        _check_buffers(self, dev_leaves, dev_out, True, "execute_host")
         if self._ws is None:
             self.bind_workspace(dev_out.device)
         if stream is None:
             stream = torch.cuda.current_stream(dev_out.device)
-        for t in list(host_leaves) + [host_out]:
-            if t.dtype != torch.complex64 or not t.is_contiguous() or t.is_cuda:
-                raise ValueError("host leaves and host_out must be contiguous complex64 CPU tensors")
-        for t in list(dev_leaves) + [dev_out]:
-            if t.dtype != torch.complex64 or not t.is_contiguous() or not t.is_cuda:
-                raise ValueError("dev_leaves and dev_out must be contiguous complex64 CUDA tensors")
         sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         tn_execute_host(self.handle, [t.data_ptr() for t in host_leaves], host_out.data_ptr(),
                         [t.data_ptr() for t in dev_leaves], dev_out.data_ptr(), sp)
@@ -405,6 +445,33 @@ class Plan:
         checked and turned into pointer arrays once, so that each call of
         the returned object costs only tn_execute_host and the wait."""
         return HostCall(self, host_leaves, host_out, dev_leaves, dev_out, stream)
+
+    def execute_prefix(self, leaves, out, step: int, stream=None) -> None:
+        """Slice 0's launches up to the one computing ``step`` (see
+        tn_execute_prefix); then ``gather`` reads that step's operands and
+        output."""
+        import torch
+        _check_buffers(self, leaves, out, True, "execute_prefix")
+        if self._ws is None:
+            self.bind_workspace(out.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(out.device)
+        sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        tn_execute_prefix(self.handle, [t.data_ptr() for t in leaves], out.data_ptr(), step, sp)
+
+    def gather(self, tensor_id: int, idx, stream=None):
+        """Entries ``idx`` (an int64 CUDA tensor of logical row-major
+        indices in the tensor's lifetime order) of tensor ``tensor_id`` as a
+        complex64 CUDA tensor (tn_plan_tensor_gather)."""
+        import torch
+        if idx.dtype != torch.int64 or not idx.is_cuda or not idx.is_contiguous():
+            raise ValueError("idx must be a contiguous int64 CUDA tensor")
+        dst = torch.empty(idx.numel(), dtype=torch.complex64, device=idx.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(idx.device)
+        sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        tn_plan_tensor_gather(self.handle, tensor_id, idx.data_ptr(), idx.numel(), dst.data_ptr(), sp)
+        return dst
 
     def check(self) -> None:
         tn_plan_check(self.handle)
@@ -428,14 +495,10 @@ class HostCall:
 
     def __init__(self, plan: Plan, host_leaves, host_out, dev_leaves, dev_out, stream=None):
         import torch
+        _check_buffers(plan, host_leaves, host_out, False, "prepare_host")
+        _check_buffers(plan, dev_leaves, dev_out, True, "prepare_host")
         if plan._ws is None:
             plan.bind_workspace(dev_out.device)
-        for t in list(host_leaves) + [host_out]:
-            if t.dtype != torch.complex64 or not t.is_contiguous() or t.is_cuda:
-                raise ValueError("host leaves and host_out must be contiguous complex64 CPU tensors")
-        for t in list(dev_leaves) + [dev_out]:
-            if t.dtype != torch.complex64 or not t.is_contiguous() or not t.is_cuda:
-                raise ValueError("dev_leaves and dev_out must be contiguous complex64 CUDA tensors")
         self.plan = plan
         self.buffers = (list(host_leaves), host_out, list(dev_leaves), dev_out)   # held alive
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev_out.device)

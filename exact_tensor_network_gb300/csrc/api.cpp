@@ -17,6 +17,11 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
 tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
                         uint64_t first, uint64_t step);
 tn_status read_profile(Plan *p, tn_launch_record *buf, int32_t cap, int32_t *len);
+tn_status check_static(Plan *p);
+tn_status execute_prefix(Plan *p, const void *const *leaf_ptrs, void *out_ptr, int32_t step,
+                         cudaStream_t stream);
+tn_status tensor_gather(Plan *p, int32_t id, const int64_t *idx, uint64_t count, void *dst,
+                        cudaStream_t stream);
 tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
                        void *const *dev_leaves, void *dev_out, cudaStream_t stream);
 }  // namespace tn
@@ -104,7 +109,8 @@ tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t *cls) 
 }
 
 tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy) {
-    if (!plan || policy < TN_POLICY_AUTO || policy > TN_POLICY_DENSE) return TN_EINVAL;
+    // tn::kPolicyForceDense is a test setting outside the ABI (see plan.h)
+    if (!plan || policy < TN_POLICY_AUTO || policy > tn::kPolicyForceDense) return TN_EINVAL;
     plan->p.policy = policy;
     return tn::layout_plan(&plan->p);
 }
@@ -126,6 +132,7 @@ tn_status tn_execute_host(tn_plan_t *plan, const void *const *host_leaves, void 
         p.last_error = "no workspace bound (tn_plan_set_workspace)";
         return TN_ENOMEM;
     }
+    p.last_static = false;
     return tn::execute_host(&p, host_leaves, host_out, dev_leaves, dev_out,
                             reinterpret_cast<cudaStream_t>(stream));
 }
@@ -187,11 +194,13 @@ tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_pt
         p.last_error = "no workspace bound (tn_plan_set_workspace)";
         return TN_ENOMEM;
     }
+    p.last_static = false;
     return tn::execute_replayed(&p, leaf_ptrs, out_ptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tn_status tn_plan_check(tn_plan_t *plan) {
     if (!plan) return TN_EINVAL;
+    if (plan->p.last_static) return tn::check_static(&plan->p);
     if (!plan->p.ws) return TN_OK;
     return tn::check_plan(&plan->p);
 }
@@ -213,8 +222,45 @@ tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs, void 
         p.last_error = "no workspace bound (tn_plan_set_workspace)";
         return TN_ENOMEM;
     }
+    p.last_static = false;
     return tn::execute_range(&p, leaf_ptrs, out_ptr, reinterpret_cast<cudaStream_t>(stream), first,
                              step);
+}
+
+tn_status tn_execute_prefix(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                            int32_t step, tn_stream_t stream) {
+    if (!plan) return TN_EINVAL;
+    tn::Plan &p = plan->p;
+    if (!leaf_ptrs || !out_ptr) {
+        p.last_error = "leaf_ptrs and out_ptr are required";
+        return TN_EINVAL;
+    }
+    for (int t = 0; t < p.n_tensors; ++t)
+        if (!leaf_ptrs[t]) {
+            p.last_error = "leaf pointer " + std::to_string(t) + " is NULL";
+            return TN_EINVAL;
+        }
+    if (step < 0 || step >= (int32_t)p.nodes.size()) {
+        p.last_error = "step out of range";
+        return TN_EINVAL;
+    }
+    if (!p.ws) {
+        p.last_error = "no workspace bound (tn_plan_set_workspace)";
+        return TN_ENOMEM;
+    }
+    p.last_static = false;
+    return tn::execute_prefix(&p, leaf_ptrs, out_ptr, step, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tn_status tn_plan_tensor_gather(tn_plan_t *plan, int32_t id, const int64_t *idx, uint64_t count,
+                                void *dst, tn_stream_t stream) {
+    if (!plan) return TN_EINVAL;
+    tn::Plan &p = plan->p;
+    if ((count > 0 && (!idx || !dst)) || id < 0 || id >= (int32_t)p.orders.size()) {
+        p.last_error = "bad tensor id or NULL index / destination";
+        return TN_EINVAL;
+    }
+    return tn::tensor_gather(&p, id, idx, count, dst, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable) {

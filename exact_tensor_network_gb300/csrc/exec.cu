@@ -28,7 +28,7 @@ int classify(const Plan &p, const NodePlan &nd) {
     const bool bf16x3 = p.precision == TN_PREC_BF16X3;
     const bool fp32 = p.precision == TN_PREC_FP32;
     const uint64_t kq = bf16 || bf16x3 ? 8 : 4;   // 16-byte rows of a TMA box
-    if (p.policy == TN_POLICY_DENSE)
+    if (p.policy == kPolicyForceDense)
         return (!fp32 && nd.k % kq == 0) ? TN_NODE_DENSE : TN_NODE_SIMT;
     if (p.policy == TN_POLICY_AUTO && nd.m * nd.n * nd.k <= kTinyMacs && nd.k <= kTinyMaxK &&
         nd.m * nd.n <= kTinyMaxOut)
@@ -484,12 +484,15 @@ namespace {
 
 // Slices first, first + step, ... issued on `stream`, or, with a graph
 // recorder, each launch on the stream the recorder picks for it.
+// With stop_launch >= 0, only the first slice's program runs, and only up to
+// and including its launch of that index in sched (tn_execute_prefix).
 tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
-                      uint64_t first, uint64_t step, Dag *dag) {
+                      uint64_t first, uint64_t step, Dag *dag, int32_t stop_launch = -1) {
     if (first >= p->n_slices) {
         cudaError_t e = cudaMemsetAsync(out_ptr, 0, p->out_elems * sizeof(float2), stream);
         return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "zeroing the output");
     }
+    if (stop_launch < 0) p->prefix_step = -1;   // the buffers are about to be reused
     char *ws = static_cast<char *>(p->ws);
     char *arena = ws + p->arena_off;
     DevStatus *status = reinterpret_cast<DevStatus *>(ws);
@@ -514,7 +517,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
     for (size_t i = 0; i < p->dense_maps.size(); ++i) map_of[p->dense_maps[i].node] = (int32_t)i;
     PermLaunch *pl = new PermLaunch;
     Recorder rec{p, stream};
-    p->records.clear();
+    if (p->profiling) p->records.clear();   // records of an earlier profiled run stay otherwise
 
     for (uint64_t sigma = first; sigma < p->n_slices && st == TN_OK; sigma += step) {
         const bool later = sigma != first;   // add into the output
@@ -560,7 +563,10 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             }
         }
         if (st != TN_OK) break;
-        for (const Launch &L : g.sched) {
+        if (stop_launch >= 0) p->prefix_leaves.assign(leaf_src.begin(), leaf_src.end());
+        for (size_t li = 0; li < g.sched.size(); ++li) {
+            const Launch &L = g.sched[li];
+            if (stop_launch >= 0 && (int32_t)li > stop_launch) break;
             if (L.kind == LAUNCH_PERMUTE) continue;   // issued above
             if (L.kind == LAUNCH_TINY) {
                 TinyLaunch tl;
@@ -716,6 +722,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 break;
             }
         }
+        if (stop_launch >= 0) break;   // the first slice only
     }
     delete pl;
     return st;
@@ -726,6 +733,76 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
 tn_status execute_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cudaStream_t stream,
                         uint64_t first, uint64_t step) {
     return issue_range(p, leaf_ptrs, out_ptr, stream, first, step, nullptr);
+}
+
+// The first slice's launches up to the one that computes `step`, issued
+// directly; its operands and output stay in place for tn_plan_tensor_gather.
+tn_status execute_prefix(Plan *p, const void *const *leaf_ptrs, void *out_ptr, int32_t step,
+                         cudaStream_t stream) {
+    p->prefix_step = -1;
+    const int32_t stop = p->launch_of[step];
+    if (stop < 0) {
+        p->last_error = "step " + std::to_string(step) + " has no launch";
+        return TN_EINVAL;
+    }
+    tn_status st = issue_range(p, leaf_ptrs, out_ptr, stream, 0, 1, nullptr, stop);
+    if (st != TN_OK) return st;
+    p->prefix_step = step;
+    p->prefix_out = out_ptr;
+    return TN_OK;
+}
+
+// Where tensor `id` of the step tn_execute_prefix stopped at lies, and how.
+tn_status tensor_gather(Plan *p, int32_t id, const int64_t *idx, uint64_t count, void *dst,
+                        cudaStream_t stream) {
+    if (p->prefix_step < 0) {
+        p->last_error = "no tn_execute_prefix since the plan was bound or last executed";
+        return TN_EINVAL;
+    }
+    const NodePlan &nd = p->nodes[p->prefix_step];
+    if (id != nd.a && id != nd.b && id != nd.out) {
+        p->last_error = "tensor " + std::to_string(id) + " is not an operand or the output of step " +
+                        std::to_string(p->prefix_step);
+        return TN_EINVAL;
+    }
+    const int n = p->n_tensors;
+    GatherArgs g;
+    std::memset(&g, 0, sizeof(g));
+    Place pl;
+    if (id < n) {
+        const LeafPlan &lp = p->leaves[id];
+        pl = lp.place;
+        g.size = lp.size;
+        // in place: the caller's complex64 leaf; else the permutation
+        // job's destination format and tiling
+        g.fmt = FMT_C64;
+        g.tile = PlanarTile{0, 0, -1, 0};
+        for (size_t j = 0; !lp.in_place && j < p->perm_leaves.size(); ++j)
+            if (p->perm_leaves[j] == id) {
+                g.tile = p->perm_table[j].tile;
+                g.fmt = p->perm_table[j].fmt;
+            }
+    } else {
+        const NodePlan &pr = p->nodes[id - n];
+        pl = pr.pc;
+        g.size = (int64_t)(pr.m * pr.n);
+        g.fmt = pr.out_fmt;
+        g.tile = pr.out_tile;
+    }
+    switch (pl.kind) {
+        case PLACE_WS: g.src = static_cast<const char *>(p->ws) + p->arena_off + pl.off; break;
+        case PLACE_LEAF: g.src = p->prefix_leaves[pl.leaf]; break;
+        default:
+            g.src = p->prefix_out;
+            g.fmt = FMT_C64;
+            g.tile = PlanarTile{0, 0, -1, 0};
+    }
+    g.idx = idx;
+    g.count = (int64_t)count;
+    g.dst = static_cast<float2 *>(dst);
+    g.status = reinterpret_cast<DevStatus *>(p->ws);
+    cudaError_t e = launch_tensor_gather(g, stream);
+    return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "launching the tensor gather");
 }
 
 // All slices.
@@ -755,6 +832,7 @@ tn_status execute_replayed(Plan *p, const void *const *leaf_ptrs, void *out_ptr,
                (int)p->graph_leaves.size() == n;
     for (int t = 0; hit && t < n; ++t) hit = p->graph_leaves[t] == leaf_ptrs[t];
     if (hit) {
+        p->prefix_step = -1;
         cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(p->graph_exec), stream);
         if (e != cudaSuccess) return cuda_fail(p, e, "launching the recorded graph");
         return TN_OK;
@@ -891,6 +969,7 @@ tn_status execute_host(Plan *p, const void *const *host_leaves, void *host_out,
     const bool record = pinned && p->use_graph && !p->profiling &&
                         cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone;
     cudaGetLastError();
+    p->prefix_step = -1;
     if (record && p->host_graph_exec && p->hg_key == key) {
         cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(p->host_graph_exec), stream);
         return e == cudaSuccess ? TN_OK : cuda_fail(p, e, "launching the recorded host call");

@@ -134,7 +134,48 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant_
     }
 }
 
+__global__ void __launch_bounds__(kThreads) tensor_gather_kernel(const __grid_constant__ GatherArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < a.count;
+         t += (int64_t)gridDim.x * kThreads) {
+        const int64_t e = a.idx[t];
+        float2 v = make_float2(0.f, 0.f);
+        if (e < 0 || e >= a.size) {
+            if (a.status) atomicCAS(&a.status->code, ERR_NONE, ERR_DESC);
+        } else if (a.fmt == FMT_C64) {
+            v = static_cast<const float2 *>(a.src)[e];
+        } else {
+            const int64_t o = tiled_offset(a.tile, e), pl = a.size;
+            if (a.fmt == FMT_BF2 || a.fmt == FMT_BF4) {
+                const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.src) + o;
+                v.x = __bfloat162float(q[0]);
+                v.y = __bfloat162float(q[pl]);
+                if (a.fmt == FMT_BF4) {
+                    v.x += __bfloat162float(q[2 * pl]);
+                    v.y += __bfloat162float(q[3 * pl]);
+                }
+            } else {
+                // FMT_SPLIT4: [re_hi, im_hi, re_lo, im_lo]; FMT_GAUSS6:
+                // [re_hi, im_hi, s_hi, re_lo, im_lo, s_lo]
+                const float *q = static_cast<const float *>(a.src) + o;
+                const int64_t lo = a.fmt == FMT_GAUSS6 ? 3 * pl : 2 * pl;
+                v.x = q[0] + q[lo];
+                v.y = q[pl] + q[lo + pl];
+            }
+        }
+        a.dst[t] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_tensor_gather(const GatherArgs &args, cudaStream_t stream) {
+    if (args.count <= 0) return cudaSuccess;
+    int64_t blocks = (args.count + kThreads - 1) / kThreads;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    return launch_pdl(tensor_gather_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, args);
+}
 
 int permute_ctas(int64_t size) {
     const int64_t per = (int64_t)kThreads * kItems;

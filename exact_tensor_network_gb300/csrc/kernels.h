@@ -162,4 +162,22 @@ struct GatherLaunch {
 };
 cudaError_t launch_gather(const GatherLaunch &args, int total_ctas, cudaStream_t stream);
 
+// Entries of one stored tensor read back as complex64 (tn_plan_tensor_gather):
+// dst[t] = the value of logical entry idx[t] (row-major in the tensor's
+// lifetime order) of a tensor of `size` entries stored at src in format
+// `fmt` with K-tiling `tile`; planar split formats give hi + lo.  An index
+// outside [0, size) yields 0 and records ERR_DESC in the status word.
+struct GatherArgs {
+    const void *src;
+    int64_t size;
+    int32_t fmt;
+    int32_t pad;
+    PlanarTile tile;
+    const int64_t *idx;
+    int64_t count;
+    float2 *dst;
+    DevStatus *status;
+};
+cudaError_t launch_tensor_gather(const GatherArgs &args, cudaStream_t stream);
+
 }  // namespace tn

@@ -25,8 +25,9 @@
 //   - The first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make
 //     that first call before any stream capture.
-//   - The device status word of these calls lives in the array, so
-//     tn_plan_check() does not see it.
+//   - The device status word of these calls lives at the start of the
+//     array.  After a static call, tn_plan_check() on that plan reads it
+//     there (and clears it), as it reads a bound workspace's otherwise.
 //   - Launch timing (tn_plan_set_profiling) is suspended for these calls,
 //     since it would create CUDA events.
 #include <cuda_runtime.h>
@@ -35,6 +36,7 @@
 #include <string>
 
 #include "../../include/tn.h"
+#include "kernels.h"
 #include "plan.h"
 
 namespace tn {
@@ -82,6 +84,43 @@ tn_status scratch_address(tn::Plan &p, void **out) {
 
 }  // namespace
 
+namespace tn {
+
+// tn_plan_check after a static call: the status word at offset 0 of the
+// array on the current device (zero when no static call ran there yet).
+tn_status check_static(Plan *p) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        p->last_error = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return TN_ECUDA;
+    }
+    void *addr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (dev >= 0 && dev < kMaxDevices) addr = g_addr[dev];
+    }
+    if (!addr) return TN_OK;
+    DevStatus h{0, 0};
+    e = cudaMemcpy(&h, addr, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        p->last_error = std::string("reading the static status word: ") + cudaGetErrorString(e);
+        return TN_ECUDA;
+    }
+    if (h.code == ERR_NONE) return TN_OK;
+    // the next static call uploads the tables (tail-tile counters included)
+    // again, so clearing the word is all that is left to do
+    e = cudaMemset(addr, 0, sizeof(h));
+    if (e != cudaSuccess) {
+        p->last_error = std::string("clearing the static status word: ") + cudaGetErrorString(e);
+        return TN_ECUDA;
+    }
+    p->last_error = "device status " + std::to_string(h.code) + " at " + std::to_string(h.where);
+    return h.code == ERR_TIMEOUT ? TN_ETIMEOUT : TN_EDEVICE;
+}
+
+}  // namespace tn
+
 extern "C" TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs,
                                               void *out_ptr, tn_stream_t stream) {
     if (!plan) return TN_EINVAL;
@@ -124,5 +163,6 @@ extern "C" TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const
     p.ws = saved_ws;
     p.ws_size = saved_size;
     p.profiling = saved_prof;
+    p.last_static = true;
     return st;
 }

@@ -23,6 +23,14 @@ constexpr int kMaxPermRank = 16;   // leaf permutation rank after merging axes
 constexpr int kMaxRuns = 12;       // runs per side of a separable output layout
 constexpr uint64_t kAlign = 256;   // workspace alignment of every buffer
 
+// Node policy beyond the public TN_POLICY_* values, for tests of the
+// tensor-core kernel only: every node it can take (k a multiple of 4, of 8
+// for bf16 operands) goes to it, whatever its shape.  Deep chains of such
+// nodes carry split-tf32 operands (22 significant bits) through every level,
+// so their results are not held to the complex64 tolerance; that is why the
+// setting is not part of the C ABI.
+constexpr int32_t kPolicyForceDense = 3;
+
 // Output side layout.  An index i in [0, prod ext) is split mixed-radix into
 // digits (run 0 most significant); its offset is sum digit[r] * stride[r]
 // (in elements).  The modes of M (or N) that sit next to each other in the
@@ -326,6 +334,7 @@ struct Plan {
     std::vector<int32_t> perm_leaves;           // leaf of each table entry
     std::vector<unsigned char> table_blob;      // device tables: PermDesc[], EpTable[], TinyDesc[]
     std::vector<Launch> sched;                  // launches of one slice, in order
+    std::vector<int32_t> launch_of;             // per step: its launch's index in sched
     // Slice-invariant hoisting (with slices and hoist set): a tensor is
     // variant when a sliced leaf lies below it.  The first slice an execute
     // runs takes `sched` and every leaf job; later slices take `sched_rest`
@@ -364,6 +373,17 @@ struct Plan {
     std::vector<const void *> graph_leaves;
     void *graph_out = nullptr;
     void *graph_ws = nullptr;
+
+    // tn_execute_prefix: the step it stopped after (-1: none since the last
+    // full execute) and the slice-0 pointers of its leaves and output, read
+    // by tn_plan_tensor_gather
+    int32_t prefix_step = -1;
+    std::vector<const void *> prefix_leaves;
+    void *prefix_out = nullptr;
+
+    // the last execute of this plan ran on the library's static scratch
+    // array (tn_execute_static): tn_plan_check reads that array's status word
+    bool last_static = false;
 
     // binding
     void *ws = nullptr;

@@ -335,6 +335,11 @@ tn_status layout_plan(Plan *p) {
     };
     perm_launch(p->perm_all, p->sched);
     if (hoist) perm_launch(p->perm_rest, p->sched_rest);
+    // index in sched of the launch that computes each step (after the leaf
+    // permutation launch, when there is one)
+    p->launch_of.assign(S, -1);
+    for (int s = 0; s < S; ++s)
+        p->launch_of[s] = t_of[n + s] < 0 ? -1 : t_of[n + s] + (p->perm_all.empty() ? 0 : 1);
     for (int s = 0; s < S; ++s) {
         NodePlan &nd = p->nodes[s];
         if (nd.is_root) where[nd.out] = {PLACE_OUT, -1, 0};

@@ -82,9 +82,7 @@ enum {
 enum {
     TN_POLICY_AUTO = 0,    /* classify every node by its shape */
     TN_POLICY_SIMT = 1,    /* every node on the general CUDA-core kernel */
-    TN_POLICY_NO_TINY = 2, /* auto, but no batched tiny-node launches */
-    TN_POLICY_DENSE = 3    /* every node the tensor-core kernel can take (k a
-                              multiple of 4, of 8 for bf16) goes there */
+    TN_POLICY_NO_TINY = 2  /* auto, but no batched tiny-node launches */
 };
 
 /*
@@ -180,7 +178,7 @@ TN_API tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t
 
 /* Choose how nodes are classified (TN_POLICY_*).  Call before
  * tn_plan_workspace_bytes / tn_plan_set_workspace; it resets the workspace
- * binding. */
+ * binding.  Errors: TN_EINVAL (NULL plan or a value not listed above). */
 TN_API tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy);
 
 /* Device workspace the plan needs, in bytes (intermediates, permuted
@@ -235,8 +233,10 @@ TN_API tn_status tn_execute(tn_plan_t *plan, const void *const *leaf_ptrs, void 
  *   - The first call on a device looks up the array's address on that
  *     device (which must be current) and caches it: make that first call
  *     before any stream capture.
- *   - tn_plan_check() does not report these calls' device status; launch
- *     timing is suspended during them.
+ *   - The device status word of these calls lives at the start of the
+ *     array: after a static call (stream synchronised), tn_plan_check() on
+ *     the same plan reads and clears it there, with the device of that
+ *     call current.  Launch timing is suspended during these calls.
  * Arguments, result and other errors as for tn_execute.
  */
 TN_API tn_status tn_execute_static(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
@@ -272,6 +272,48 @@ TN_API tn_status tn_execute_slices(tn_plan_t *plan, const void *const *leaf_ptrs
  */
 TN_API tn_status tn_execute_host(tn_plan_t *plan, const void *const *host_leaves, void *host_out,
                                  void *const *dev_leaves, void *dev_out, tn_stream_t stream);
+
+/* ---- verification of intermediates ------------------------------------
+ *
+ * The value of a contraction does not depend on the tree ("Crossing the
+ * single-GPU memory wall", section 1.1), so every node can be checked on its
+ * own: its output must be the [m, k] x [n, k] product of its two operands
+ * (section 1.4 layouts).  These two calls expose one node's operands and
+ * output as they lie in the workspace, so that sampled outputs of a
+ * full-size node can be recomputed independently from the data the node
+ * actually read.
+ */
+
+/*
+ * Run the first slice's launches, in issue order and without graph replay,
+ * up to and including the launch that computes step `step` (its split-K
+ * reduction included), then stop.  Leaves and out_ptr as for tn_execute
+ * (out_ptr receives the root's slice-0 value only if `step` is the root).
+ * Afterwards, until the next execute of any kind, the step's two operands
+ * and its output are still in place for tn_plan_tensor_gather.  Other
+ * launches of the same tiny-node batch as `step` also run.
+ * Errors: TN_EINVAL (NULL pointers, step out of range), TN_ENOMEM (no
+ * workspace bound), TN_ECUDA.
+ */
+TN_API tn_status tn_execute_prefix(tn_plan_t *plan, const void *const *leaf_ptrs, void *out_ptr,
+                                   int32_t step, tn_stream_t stream);
+
+/*
+ * Read entries of tensor `id` (SSA numbering: an operand or the output of
+ * the step the last tn_execute_prefix stopped at) as complex64, after that
+ * call and on a stream ordered after it.  idx: device array of `count`
+ * logical indices, row-major over the tensor's lifetime order
+ * (tn_plan_mode_order; sliced modes at slice 0).  dst: device array of
+ * `count` complex64, receives the entries.  Tensors the planner stores in a
+ * planar split format (operands of tensor-core nodes) are returned as
+ * hi + lo, the value the tensor-core kernel multiplies; K-tiling is undone.
+ * An index outside the tensor gives 0 and makes tn_plan_check report
+ * TN_EDEVICE.  Asynchronous on `stream`.
+ * Errors: TN_EINVAL (no prefix run, or `id` not an operand or the output of
+ * its step, NULL arrays), TN_ECUDA.
+ */
+TN_API tn_status tn_plan_tensor_gather(tn_plan_t *plan, int32_t id, const int64_t *idx,
+                                       uint64_t count, void *dst, tn_stream_t stream);
 
 /* Enable (1, the default) or disable (0) graph replay in tn_execute; any
  * recorded graph is released either way. */
@@ -311,8 +353,11 @@ TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
 TN_API tn_status tn_plan_set_hoisting(tn_plan_t *plan, int32_t enable);
 
 /* After the stream has been synchronised: read and clear the device status
- * word.  TN_OK, TN_EDEVICE (a kernel saw an inconsistent descriptor) or
- * TN_ETIMEOUT (a bounded wait inside a kernel gave up). */
+ * word of the plan's last execute (in the bound workspace, or in the static
+ * scratch array when that execute was tn_execute_static).  TN_OK,
+ * TN_EDEVICE (a kernel saw an inconsistent descriptor) or TN_ETIMEOUT (a
+ * bounded wait inside a kernel gave up; the plan's descriptor tables are
+ * restored, so the next execute runs normally). */
 TN_API tn_status tn_plan_check(tn_plan_t *plan);
 
 /* ---- measurement ------------------------------------------------------ */

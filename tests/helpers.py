@@ -47,3 +47,66 @@ def assert_close(got, ref, tol=TOL_C64, what=""):
     assert np.shape(got) == np.shape(ref), (np.shape(got), np.shape(ref))
     r = max_rel_err(got, ref)
     assert r <= tol, f"{what}: max|err|/max|ref| = {r:.3e} > {tol:.1e}"
+
+
+def node_layout(plan, step, extents):
+    """(a, b, out, m, n, k, offM, offN) of a step from the plan's mode
+    orders: A = [M | K] and B = [N | K] row-major, and the offset of output
+    entry (i, j) in the output's own order is offM(i) + offN(j)."""
+    n_leaves = plan.n_tensors
+    a, b = plan.pairs[step]
+    out = n_leaves + step
+    oa, ob, oc = plan.mode_order(a), plan.mode_order(b), plan.mode_order(out)
+    M = [x for x in oa if x not in ob]
+    N = [x for x in ob if x not in oa]
+    K = oa[len(M):]
+    assert K == ob[len(N):], "operands must share the K order"
+    assert sorted(oc) == sorted(M + N)
+    ext = {x: int(extents[x]) for x in oa + ob}
+
+    def prod(xs):
+        r = 1
+        for x in xs:
+            r *= ext[x]
+        return r
+    stride_c = {}
+    acc = 1
+    for x in reversed(oc):
+        stride_c[x] = acc
+        acc *= ext[x]
+
+    def side_offsets(side, idx):
+        idx = np.asarray(idx, dtype=np.int64)
+        off = np.zeros_like(idx)
+        for x in reversed(side):
+            off += (idx % ext[x]) * stride_c[x]
+            idx = idx // ext[x]
+        return off
+    return (a, b, out, prod(M), prod(N), prod(K),
+            lambda i: side_offsets(M, i), lambda j: side_offsets(N, j))
+
+
+def check_node_sampled(plan, extents, leaves, out, step, seed, rows=64, cols=16, tol=TOL_C64):
+    """Run the first slice up to `step` (tn_execute_prefix), read `rows`
+    sampled rows of A, `cols` rows of B and the rows x cols outputs they
+    give (tn_plan_tensor_gather), and compare those outputs with fp64 dot
+    products of the gathered operand rows.  Returns the relative error."""
+    import torch
+    dev = out.device
+    a, b, c, m, n, k, offm, offn = node_layout(plan, step, extents)
+    rng = np.random.default_rng(seed)
+    I = np.unique(rng.integers(0, m, size=min(rows, m)))
+    J = np.unique(rng.integers(0, n, size=min(cols, n)))
+    plan.execute_prefix(leaves, out, step)
+    kk = np.arange(k, dtype=np.int64)
+
+    def gather(t, idx):
+        g = plan.gather(t, torch.from_numpy(np.ascontiguousarray(idx.ravel())).to(dev))
+        return g.cpu().numpy().astype(np.complex128).reshape(idx.shape)
+    A = gather(a, I[:, None] * k + kk[None, :])
+    B = gather(b, J[:, None] * k + kk[None, :])
+    C = gather(c, offm(I)[:, None] + offn(J)[None, :])
+    torch.cuda.synchronize(dev)
+    plan.check()
+    ref = A @ B.T
+    return max_rel_err(C, ref), (m, n, k)

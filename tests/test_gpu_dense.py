@@ -81,10 +81,11 @@ def test_ragged_nodes(precision, tol, m, n, k):
 
 
 def test_forced_dense_on_random_network():
-    """Stress policy, not the default path: every eligible node of the 59
-    (not only the compute-bound ones) runs on split-tf32 operands, which
-    carry 22 significant bits instead of fp32's 24, so rounding compounds
-    along the tree's depth.  Bound: 4x the complex64 tolerance."""
+    """Test setting outside the C ABI (not a public policy): every eligible
+    node of the 59 (not only the compute-bound ones) runs on split-tf32
+    operands, which carry 22 significant bits instead of fp32's 24, so
+    rounding compounds along the tree's depth.  Bound: 4x the complex64
+    tolerance."""
     net, tree, _ = configs.random_60()
     got, _ = run_gpu(net, tree, policy=tn.TN_POLICY_DENSE)
     assert_close(got, _ref(net, tree), 4 * TOL_C64, "random_60 with every eligible node dense")

@@ -405,3 +405,59 @@ def test_execute_from_host_buffers(pinned, case):
         call()
         assert_close(host_out.numpy().astype(np.complex128), ref, what=f"{case} prepared call {it}")
     plan.check()
+
+
+# ---- TN_PREC_FP32: every node on CUDA-core fp32 FMA ------------------------
+
+@pytest.mark.parametrize("case", ["circuit_3x3_d4", "random_60", "sliced_30", "twin_4x4_d12"])
+def test_fp32_precision_networks(case):
+    """The fp32 precision against the oracle at the complex64 tolerance:
+    no node may reach the tensor cores."""
+    from helpers import TOL_C64
+    sl = []
+    if case == "circuit_3x3_d4":
+        net, tree, _ = configs.circuit_3x3_d4()
+    elif case == "random_60":
+        net, tree, _ = configs.random_60()
+    elif case == "sliced_30":
+        net = random_network(30, 4)
+        tree = greedy_tree(net, 0)
+        sl = choose_slices(net, tree, largest_intermediate(net, tree) // 8)[:3]
+    else:
+        net, _ = grid_circuit_network(4, 4, 12, 2, n_open=6)
+        tree = greedy_tree(net, 28, noise=0.6, alpha=0.25)
+    got, plan = run_gpu(net, tree, sl, precision="fp32")
+    assert all(plan.node_class(s) != 1 for s in range(len(tree)))
+    if sl:
+        assert plan.num_slices > 1
+    assert_close(got, _ref(net, tree, sl), TOL_C64, f"{case} fp32")
+
+
+@pytest.mark.parametrize("m,n,k", [(512, 512, 512), (300, 257, 1000), (1, 1, 4096), (4096, 3, 16),
+                                   (64, 2048, 2), (129, 65, 1)])
+def test_fp32_precision_nodes(m, n, k):
+    from helpers import TOL_C64, node_network
+    net = node_network(m, n, k, m * 7 + n * 3 + k)
+    got, plan = run_gpu(net, [(0, 1)], precision="fp32", policy=2)
+    assert plan.node_class(0) != 1
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, f"fp32 node {m}x{n}x{k}")
+
+
+def test_reduced_precision_errors_reported():
+    """Reported, not gated (the bf16 tolerance is gated on single nodes):
+    max |gpu - ref| / max |ref| of every precision on the 3x3 circuit, the
+    random 60-tensor network and the 4x4 x 12-cycle twin of the 6x6 recipe.
+    Only a loose sanity bound applies here."""
+    from helpers import max_rel_err
+    cases = {"circuit_3x3_d4": configs.circuit_3x3_d4()[:2], "random_60": configs.random_60()[:2]}
+    net, _ = grid_circuit_network(4, 4, 12, 2, n_open=6)
+    cases["twin_4x4_d12"] = (net, greedy_tree(net, 28, noise=0.6, alpha=0.25))
+    for name, (net, tree) in cases.items():
+        ref = _ref(net, tree)
+        line = []
+        for prec in ("tf32x3", "bf16x3", "bf16", "fp32"):
+            got, _ = run_gpu(net, tree, precision=prec)
+            r = max_rel_err(got, ref)
+            line.append(f"{prec} {r:.2e}")
+            assert np.isfinite(r) and r < 0.5, f"{name} {prec}: {r}"
+        print(f"precision errors {name}: " + ", ".join(line))

@@ -117,3 +117,26 @@ def test_single_leaf_and_scalars():
     s = np.array(2.5 - 1j, dtype=np.complex64)
     net2 = Network([[], [0]], [3], [0], [s, d[0, :, 0].copy()])
     assert np.abs(_c(net2, [(0, 1)]) - s * d[0, :, 0]).max() < 1e-6
+
+
+def test_adjugate_inverse_closed_form():
+    """A circuit followed by its inverse written with adjugates is exactly
+    prod det(U) times the identity (adj(U) U = det(U) I for each stored
+    2x2 gate; CZ undoes itself).  The oracle, run on the half-state tree of
+    that network, must give the closed form to fp64 rounding."""
+    from workloads import configs
+    net, tree, _, circ = configs.circuit_norm(4, 4, 8)
+    want = 1.0 + 0.0j
+    for g in circ.gates:
+        if g[0] == "u":
+            u = np.asarray(g[2], dtype=np.complex128)
+            want *= u[0, 0] * u[1, 1] - u[0, 1] * u[1, 0]
+    assert abs(abs(want) - 1.0) < 1e-5        # the stored gates are nearly unitary
+    got = complex(oracle.contract(net.tensors, net.extents, net.open_modes, net.data, tree))
+    assert abs(got - want) < 1e-12
+    # the same network with the plain adjoint as inverse is only 1 to the
+    # gates' complex64 rounding
+    from workloads import inverse_circuit
+    net2 = circuit_network(concat(circ, inverse_circuit(circ)), ())
+    got2 = complex(oracle.contract(net2.tensors, net2.extents, net2.open_modes, net2.data, tree))
+    assert 1e-9 < abs(got2 - 1.0) < 1e-5

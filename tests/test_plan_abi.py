@@ -181,3 +181,29 @@ def test_hoisting_workspace_and_replanning():
     p.set_policy(tn.TN_POLICY_NO_TINY)
     p.set_policy(tn.TN_POLICY_AUTO)
     assert (p.workspace_bytes, p.launches) == (on_ws, on_l)
+
+
+def test_binding_checks_buffer_sizes():
+    """The binding refuses leaves or results whose entry count differs from
+    the plan's (a short buffer would be read or written past its end)."""
+    import torch
+    net = random_tiny_network(404)
+    plan = tn.Plan.from_network(net, greedy_tree(net, 0))
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)) for d in net.data]
+    out = torch.zeros(plan.out_shape, dtype=torch.complex64)
+    tn._check_buffers(plan, leaves, out, False, "host")
+    big = max(range(len(leaves)), key=lambda i: leaves[i].numel())
+    short = list(leaves)
+    short[big] = leaves[big].reshape(-1)[:-1].clone()
+    with pytest.raises(ValueError, match=f"leaf {big} has"):
+        tn._check_buffers(plan, short, out, False, "host")
+    with pytest.raises(ValueError, match="result has"):
+        tn._check_buffers(plan, leaves, torch.zeros(plan.out_size + 1, dtype=torch.complex64),
+                          False, "host")
+    with pytest.raises(ValueError, match="leaves given"):
+        tn._check_buffers(plan, leaves[:-1], out, False, "host")
+    with pytest.raises(ValueError, match="complex64"):
+        tn._check_buffers(plan, [x.to(torch.complex128) for x in leaves], out, False, "host")
+    # device buffers are required where the call runs on the GPU
+    with pytest.raises(ValueError, match="CUDA"):
+        tn._check_buffers(plan, leaves, out, True, "execute")

@@ -89,6 +89,24 @@ def inverse_circuit(c: Circuit) -> Circuit:
     return Circuit(c.rows, c.cols, inv)
 
 
+def adjugate_circuit(c: Circuit) -> Circuit:
+    """The reverse circuit with every single-qubit gate U = [[a, b], [c, d]]
+    replaced by its adjugate [[d, -b], [-c, a]] (= det(U) U^-1), and every
+    CZ kept (CZ^-1 = CZ).  The adjugate of a stored complex64 gate is
+    exactly representable (entries are only moved and negated), so the
+    stored circuit followed by this one is exactly prod det(U) times the
+    identity, whatever rounding the stored gates carry."""
+    adj = []
+    for g in reversed(c.gates):
+        if g[0] == "u":
+            u = np.asarray(g[2], dtype=np.complex64)
+            v = np.array([[u[1, 1], -u[0, 1]], [-u[1, 0], u[0, 0]]], dtype=np.complex64)
+            adj.append(("u", g[1], v))
+        else:
+            adj.append(g)
+    return Circuit(c.rows, c.cols, adj)
+
+
 def concat(c1: Circuit, c2: Circuit) -> Circuit:
     assert (c1.rows, c1.cols) == (c2.rows, c2.cols)
     return Circuit(c1.rows, c1.cols, list(c1.gates) + list(c2.gates))

@@ -148,3 +148,26 @@ def choose_slices(net: Network, tree: Tree, target: int, max_modes: int = 64) ->
         best = min(sorted(common), key=lambda x: step_volume(net, tree, chosen + [x]))
         chosen.append(best)
     return chosen
+
+
+def split_tree(net: Network, part_a: Sequence[int], tree_a: Tree, part_b: Sequence[int],
+               tree_b: Tree) -> Tree:
+    """A tree of ``net`` that contracts the leaves ``part_a`` along
+    ``tree_a`` (a tree of the sub-network of those leaves, in its own SSA
+    numbering), then ``part_b`` along ``tree_b``, then joins the two
+    results.  ``part_a`` + ``part_b`` must list every leaf once."""
+    n = net.n_tensors
+    assert sorted(list(part_a) + list(part_b)) == list(range(n))
+    out: Tree = []
+
+    def emit(part, sub_tree):
+        ids = {i: int(t) for i, t in enumerate(part)}
+        for s, (a, b) in enumerate(sub_tree):
+            out.append((ids[a], ids[b]))
+            ids[len(part) + s] = n + len(out) - 1
+        return ids[len(part) + len(sub_tree) - 1] if sub_tree else ids[0]
+
+    ra = emit(part_a, tree_a)
+    rb = emit(part_b, tree_b)
+    out.append((ra, rb))
+    return out
