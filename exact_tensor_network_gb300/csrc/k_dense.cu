@@ -23,11 +23,20 @@
 // of 128 x 128 per k-step, in exchange for 24-byte operand entries and a
 // two-stage ring (96 KiB stages).
 //
-// Accuracy: the tensor core's fp32 accumulation loses a little on every
-// accumulation, and over thousands of k-steps that loss grows linearly with
-// k.  So the k range of a tile is cut into chunks of 256; each chunk is
-// accumulated in TMEM from zero, then drained into fp32 registers of the
-// epilogue warps with ordinary rounded adds (periodic promotion).
+// Accuracy: the tensor core's fp32 accumulation rounds toward zero, so every
+// accumulation into TMEM shrinks the sum a little, always in the same
+// direction, and the shrinkage grows with the number of accumulations.  So
+// the k range of a tile is cut into chunks (64 complex k for the split
+// precisions, 256 for plain bf16 operands); each chunk is accumulated in TMEM
+// from zero, then drained into fp32 registers of the epilogue warps with
+// ordinary round-to-nearest adds (periodic promotion).  Measured on chains
+// of 2^30-2^32-entry nodes: 256-k chunks leave a relative bias of ~2e-6 per
+// node, 64-k chunks a quarter of it.
+// The two accumulators are handed over separately: the MMA warp commits D1
+// after the chunk's last D1 products, then issues the D2 products while the
+// drain reads D1, and starts the next chunk's D1 products as soon as the
+// drain has released D1 (while it reads D2).  The drain thus hides behind
+// the tensor core's work instead of stalling it once per chunk.
 //
 // Structure: persistent kernel, one CTA of 384 threads per SM.  Warpgroup
 // 0: warp 0 issues TMA loads into a ring of shared-memory stages, warp 1
@@ -60,7 +69,6 @@ constexpr int ROW_BYTES = 64;           // K bytes per smem row (64-byte swizzle
 constexpr int PLANE_TILE = BM * ROW_BYTES;   // 8 KiB: 128 rows of one plane
 constexpr int THREADS = 384;            // 3 warpgroups
 constexpr int DRAIN_WARPS = 8;
-constexpr int CHUNK_K = 256;            // complex k accumulated in TMEM per drain
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 // register split: launched with 168 per thread (384 x 168 = 64512)
@@ -85,6 +93,8 @@ struct Cfg {
     static constexpr int PLANES = BF16 ? 2 : THREE ? 6 : 4;
     static constexpr int KB = HALF ? 32 : 16;           // complex k per stage
     static constexpr int K_INSTR = HALF ? 16 : 8;       // k per MMA instruction
+    // complex k accumulated in TMEM per drain (promotion into fp32 registers)
+    static constexpr int CHUNK_K = BF16 ? 256 : 64;
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
     static constexpr int STAGE_BYTES = 2 * PLANES * PLANE_TILE;
     static constexpr int STAGES = BF16 ? 6 : THREE ? 2 : 3;
@@ -324,10 +334,13 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
+    // TMEM handoff, per accumulator: full (MMA -> drain), empty (drain -> MMA)
     const uint32_t tmem_full = smem_u32(bars + 2 * MAX_STAGES);
     const uint32_t tmem_empty = smem_u32(bars + 2 * MAX_STAGES + 1);
     const uint32_t drain = smem_u32(bars + 2 * MAX_STAGES + 2);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 3);
+    const uint32_t tmem_full2 = smem_u32(bars + 2 * MAX_STAGES + 3);
+    const uint32_t tmem_empty2 = smem_u32(bars + 2 * MAX_STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -339,6 +352,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, DRAIN_WARPS);
+        mbar_init(tmem_full2, 1);
+        mbar_init(tmem_empty2, DRAIN_WARPS);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -432,11 +447,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 const int kb0 = it.kb0, kb1 = it.kb1;
                 const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
                 for (int ch = 0; ch < nch && ok; ++ch) {
-                    if (!wait_bounded(tmem_empty, tphase ^ 1, abort_flag)) {
+                    // D1 must have been read by the drain (three products:
+                    // every accumulator, both halves)
+                    if (!wait_bounded(tmem_empty, tphase ^ 1, abort_flag) ||
+                        (C::THREE && !wait_bounded(tmem_empty2, tphase ^ 1, abort_flag))) {
                         ok = false;
                         break;
                     }
                     fence_after();
+                    bool d2_free = C::THREE;
                     const int kb_beg = kb0 + ch * C::CHUNK_STAGES;
                     const int kb_end = min(kb1, kb_beg + C::CHUNK_STAGES);
                     for (int kb = kb_beg; kb < kb_end; ++kb) {
@@ -448,16 +467,15 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         const uint32_t base = smem_u32(smem + stage * stage_bytes);
                         const uint32_t bbase = base + C::PLANES * PLANE_TILE;
                         const bool first = kb == kb_beg;
+                        const bool last = kb == kb_end - 1;
+                        // D1: the products of A's real planes (three products:
+                        // all of them)
 #pragma unroll
                         for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
                             const uint32_t off = kk * 32;   // 32 bytes of K per instruction
                             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
                             if constexpr (C::BF16) {
-                                const uint64_t ar = sdesc(base + off);
-                                const uint64_t ai = sdesc(base + PLANE_TILE + off);
-                                const uint64_t b = sdesc(bbase + off);
-                                mma<MODE>(d1, ar, b, acc, idesc);
-                                mma<MODE>(d2, ai, b, acc, idesc);
+                                mma<MODE>(d1, sdesc(base + off), sdesc(bbase + off), acc, idesc);
                             } else if constexpr (C::THREE) {
                                 // D_c (128 columns at 128 c) = A_c B_c for the
                                 // components c = re, im, re + im
@@ -474,27 +492,52 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                                 }
                             } else {
                                 const uint64_t arh = sdesc(base + off);
-                                const uint64_t aih = sdesc(base + PLANE_TILE + off);
                                 const uint64_t arl = sdesc(base + 2 * PLANE_TILE + off);
-                                const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
                                 const uint64_t bh = sdesc(bbase + off);
                                 const uint64_t bl = sdesc(bbase + 2 * b_plane + off);
                                 mma<MODE>(d1, arl, bh, acc, idesc);
                                 mma<MODE>(d1, arh, bl, 1, idesc);
                                 mma<MODE>(d1, arh, bh, 1, idesc);
-                                mma<MODE>(d2, ail, bh, acc, idesc);
-                                mma<MODE>(d2, aih, bl, 1, idesc);
-                                mma<MODE>(d2, aih, bh, 1, idesc);
+                            }
+                        }
+                        if (last) mma_commit(tmem_full);   // the drain may read D1
+                        if (!d2_free) {
+                            // the drain releases D2 while these D1 products run
+                            if (!wait_bounded(tmem_empty2, tphase ^ 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
+                            d2_free = true;
+                        }
+                        // D2: the products of A's imaginary planes
+                        if constexpr (!C::THREE) {
+#pragma unroll
+                            for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+                                const uint32_t off = kk * 32;
+                                const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                                if constexpr (C::BF16) {
+                                    mma<MODE>(d2, sdesc(base + PLANE_TILE + off), sdesc(bbase + off),
+                                              acc, idesc);
+                                } else {
+                                    const uint64_t aih = sdesc(base + PLANE_TILE + off);
+                                    const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
+                                    const uint64_t bh = sdesc(bbase + off);
+                                    const uint64_t bl = sdesc(bbase + 2 * b_plane + off);
+                                    mma<MODE>(d2, ail, bh, acc, idesc);
+                                    mma<MODE>(d2, aih, bl, 1, idesc);
+                                    mma<MODE>(d2, aih, bh, 1, idesc);
+                                }
                             }
                         }
                         mma_commit(empty0 + 8 * stage);
+                        if (last) mma_commit(tmem_full2);   // the drain may read D2
                         if (++stage == stages) {
                             stage = 0;
                             phase ^= 1;
                         }
                     }
                     if (!ok) break;
-                    mma_commit(tmem_full);
                     tphase ^= 1;
                 }
             }
@@ -563,11 +606,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     break;
                 }
                 fence_after();
+                if constexpr (C::THREE) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    if (cc >= ncc) break;   // warp-uniform (narrow tiles: 2 blocks)
-                    const uint32_t col = h * half_cols + cc * 16;
-                    if constexpr (C::THREE) {
+                    for (int cc = 0; cc < 4; ++cc) {
+                        if (cc >= ncc) break;   // warp-uniform
+                        const uint32_t col = h * half_cols + cc * 16;
                         // P1 = ArBr, P2 = AiBi, P3 = (Ar + Ai)(Br + Bi):
                         // re = P1 - P2, im = P3 - (P1 + P2)
                         float p1[16], p2[16], p3[16];
@@ -580,23 +623,63 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                             sr[cc * 16 + c] += p1[c] - p2[c];
                             si[cc * 16 + c] += p3[c] - (p1[c] + p2[c]);
                         }
-                    } else {
-                        float rr[16], ri[16], ir[16], ii[16];
-                        tmem_ld16(lane_base + col, rr);
-                        tmem_ld16(lane_base + bn + col, ri);
-                        tmem_ld16(lane_base + 2 * bn + col, ir);
-                        tmem_ld16(lane_base + 3 * bn + col, ii);
+                    }
+                } else {
+                    // D1 = [ArBr | ArBi]: two column blocks (four loads) in
+                    // flight per round
+#pragma unroll
+                    for (int cp = 0; cp < 4; cp += 2) {
+                        if (cp >= ncc) break;   // warp-uniform (narrow tiles: 2 blocks)
+                        const uint32_t col = h * half_cols + cp * 16;
+                        float rr0[16], ri0[16], rr1[16], ri1[16];
+                        tmem_ld16(lane_base + col, rr0);
+                        tmem_ld16(lane_base + bn + col, ri0);
+                        tmem_ld16(lane_base + col + 16, rr1);
+                        tmem_ld16(lane_base + bn + col + 16, ri1);
                         tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
-                            sr[cc * 16 + c] += rr[c] - ii[c];
-                            si[cc * 16 + c] += ri[c] + ir[c];
+                            sr[cp * 16 + c] += rr0[c];
+                            si[cp * 16 + c] += ri0[c];
+                            sr[cp * 16 + 16 + c] += rr1[c];
+                            si[cp * 16 + 16 + c] += ri1[c];
                         }
                     }
                 }
                 fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tmem_empty);
+                if (lane == 0) mbar_arrive(tmem_empty);   // D1 may be overwritten
+                if (lane == 0) okv = wait_bounded(tmem_full2, tphase, abort_flag) ? 1 : 0;
+                okv = __shfl_sync(0xffffffffu, okv, 0);
+                if (!okv) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                if constexpr (!C::THREE) {
+                    // D2 = [AiBr | AiBi]: re -= AiBi, im += AiBr
+#pragma unroll
+                    for (int cp = 0; cp < 4; cp += 2) {
+                        if (cp >= ncc) break;
+                        const uint32_t col = h * half_cols + cp * 16;
+                        float ir0[16], ii0[16], ir1[16], ii1[16];
+                        tmem_ld16(lane_base + 2 * bn + col, ir0);
+                        tmem_ld16(lane_base + 3 * bn + col, ii0);
+                        tmem_ld16(lane_base + 2 * bn + col + 16, ir1);
+                        tmem_ld16(lane_base + 3 * bn + col + 16, ii1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            sr[cp * 16 + c] -= ii0[c];
+                            si[cp * 16 + c] += ir0[c];
+                            sr[cp * 16 + 16 + c] -= ii1[c];
+                            si[cp * 16 + 16 + c] += ir1[c];
+                        }
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tmem_empty2);   // D2 may be overwritten
                 tphase ^= 1;
             }
             if (!ok) break;
