@@ -390,6 +390,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     device_leaves = args.leaves == "device"
     net, tree, slices = load_workload(args.workload, with_data=not device_leaves)
     plan = tn.Plan.from_network(net, tree, slices, args.precision)
+    if args.cta_pairs:
+        plan.set_cta_pairs(True)
+    if args.promotion_chunk:
+        plan.set_promotion_chunk(args.promotion_chunk)
     plan.bind_workspace(dev)
     if device_leaves:
         # seeded N(0, 1) complex entries drawn on the device (no host copy:
@@ -579,6 +583,8 @@ def finish(args, rank, world, net, plan, ct, units, value, ms, sharded, roofline
                 "data": "synthetic" + (" (leaves drawn on the device)" if args.leaves == "device" else ""),
                 "config": {"workload": net.name, "tensors": net.n_tensors, "C_t": ct,
                            "C_s": plan.peak, "slices": plan.num_slices, "precision": args.precision,
+                           "cta_pairs": bool(args.cta_pairs),
+                           "promotion_chunk": args.promotion_chunk or "per plan",
                            "l2": "flushed between timed steps (untimed 258 MiB fill)",
                            "parallelism": (f"slices round-robin over {world} ranks" if sharded
                                            else f"replicas x{world}"), **cfg_extra},
@@ -599,6 +605,10 @@ def main():
     ap.add_argument("--precision", default="tf32x3", choices=["tf32x3", "bf16", "bf16x3", "fp32"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cta-pairs", action="store_true",
+                    help="tensor-core nodes on CTA pairs (tn_plan_set_cta_pairs)")
+    ap.add_argument("--promotion-chunk", type=int, default=0,
+                    help="complex k per TMEM promotion (tn_plan_set_promotion_chunk; 0: per plan)")
     ap.add_argument("--leaves", choices=["host", "device"], default="host",
                     help="device: draw the leaves on the GPU (no end-to-end or CPU leg)")
     args = ap.parse_args()

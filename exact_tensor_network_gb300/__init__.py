@@ -23,8 +23,8 @@ TN_PREC_TF32X3, TN_PREC_BF16, TN_PREC_FP32, TN_PREC_BF16X3 = 0, 1, 2, 3
 PRECISIONS = {"tf32x3": TN_PREC_TF32X3, "bf16": TN_PREC_BF16, "fp32": TN_PREC_FP32,
               "bf16x3": TN_PREC_BF16X3}
 # node classes
-TN_NODE_SIMT, TN_NODE_DENSE, TN_NODE_STREAM, TN_NODE_TINY = 0, 1, 2, 3
-NODE_CLASS_NAMES = {0: "simt", 1: "dense", 2: "stream", 3: "tiny"}
+TN_NODE_SIMT, TN_NODE_DENSE, TN_NODE_STREAM, TN_NODE_TINY, TN_NODE_FUSED = 0, 1, 2, 3, 4
+NODE_CLASS_NAMES = {0: "simt", 1: "dense", 2: "stream", 3: "tiny", 4: "fused"}
 # policies
 TN_POLICY_AUTO, TN_POLICY_SIMT, TN_POLICY_NO_TINY = 0, 1, 2
 # test setting outside the C ABI: every node the tensor-core kernel can take
@@ -60,7 +60,7 @@ class tn_launch_record(ctypes.Structure):
 
 
 KERNEL_NAMES = {0: "permute", 1: "simt", 2: "dense_tf32x3", 3: "dense_bf16", 4: "stream", 5: "tiny",
-                6: "reduce", 7: "dense_tf32x3_3p", 8: "dense_bf16x3"}
+                6: "reduce", 7: "dense_tf32x3_3p", 8: "dense_bf16x3", 9: "fused"}
 
 
 class tn_slices(ctypes.Structure):
@@ -92,6 +92,9 @@ SIGNATURES = {
     "tn_plan_set_replay": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_plan_set_three_products": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_plan_set_hoisting": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_plan_set_fusion": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_plan_set_cta_pairs": (ctypes.c_int, [_P, ctypes.c_int32]),
+    "tn_plan_set_promotion_chunk": (ctypes.c_int, [_P, ctypes.c_int32]),
     "tn_execute_slices": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, _P, ctypes.c_uint64,
                                          ctypes.c_uint64]),
     "tn_execute_host": (ctypes.c_int, [_P, ctypes.POINTER(_P), _P, ctypes.POINTER(_P), _P, _P]),
@@ -274,6 +277,18 @@ def tn_plan_set_hoisting(plan: int, enable: bool) -> None:
     _check(lib().tn_plan_set_hoisting(plan, 1 if enable else 0), plan)
 
 
+def tn_plan_set_promotion_chunk(plan: int, chunk_k: int) -> None:
+    _check(lib().tn_plan_set_promotion_chunk(plan, int(chunk_k)), plan)
+
+
+def tn_plan_set_cta_pairs(plan: int, enable: bool) -> None:
+    _check(lib().tn_plan_set_cta_pairs(plan, 1 if enable else 0), plan)
+
+
+def tn_plan_set_fusion(plan: int, enable: bool) -> None:
+    _check(lib().tn_plan_set_fusion(plan, 1 if enable else 0), plan)
+
+
 def tn_plan_check(plan: int) -> None:
     _check(lib().tn_plan_check(plan), plan)
 
@@ -384,6 +399,18 @@ class Plan:
 
     def set_hoisting(self, enable: bool) -> None:
         tn_plan_set_hoisting(self.handle, enable)
+        self._ws = None
+
+    def set_fusion(self, enable: bool) -> None:
+        tn_plan_set_fusion(self.handle, enable)
+        self._ws = None
+
+    def set_cta_pairs(self, enable: bool) -> None:
+        tn_plan_set_cta_pairs(self.handle, enable)
+        self._ws = None
+
+    def set_promotion_chunk(self, chunk_k: int) -> None:
+        tn_plan_set_promotion_chunk(self.handle, chunk_k)
         self._ws = None
 
     def bind_workspace(self, device=None):

@@ -104,8 +104,31 @@ tn_status tn_plan_node_mnk(const tn_plan_t *plan, int32_t step, uint64_t mnk[3])
 
 tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t *cls) {
     if (!plan || !cls || step < 0 || step >= (int32_t)plan->p.nodes.size()) return TN_EINVAL;
-    *cls = plan->p.nodes[step].cls;
+    const tn::Plan &p = plan->p;
+    *cls = (step < (int32_t)p.fused.size() && p.fused[step] >= 0) ? TN_NODE_FUSED : p.nodes[step].cls;
     return TN_OK;
+}
+
+tn_status tn_plan_set_promotion_chunk(tn_plan_t *plan, int32_t chunk_k) {
+    if (!plan) return TN_EINVAL;
+    if (chunk_k != 0 && (chunk_k < 32 || chunk_k > 1024 || chunk_k % 32 != 0)) {
+        plan->p.last_error = "promotion chunk must be 0 or a multiple of 32 in [32, 1024]";
+        return TN_EINVAL;
+    }
+    plan->p.chunk_k = chunk_k;
+    return tn::layout_plan(&plan->p);
+}
+
+tn_status tn_plan_set_cta_pairs(tn_plan_t *plan, int32_t enable) {
+    if (!plan) return TN_EINVAL;
+    plan->p.cta_pairs = enable ? 1 : 0;
+    return tn::layout_plan(&plan->p);
+}
+
+tn_status tn_plan_set_fusion(tn_plan_t *plan, int32_t enable) {
+    if (!plan) return TN_EINVAL;
+    plan->p.fuse = enable ? 1 : 0;
+    return tn::layout_plan(&plan->p);
 }
 
 tn_status tn_plan_set_policy(tn_plan_t *plan, int32_t policy) {

@@ -63,11 +63,11 @@ constexpr uint64_t kPartialBudget = 1ull << 30;   // bytes of split-K partials p
 // Split-K for the CUDA-core classes: cut k when the node alone would not
 // give every SM two CTAs, keeping chunks of at least 64 entries.
 void choose_split(const Plan &p, NodePlan &nd) {
-    (void)p;
     nd.ksplit = 1;
     nd.kchunk = (int64_t)nd.k;
     nd.swap = 0;
     nd.narrow = 0;
+    nd.pair = 0;
     nd.tail_first = -1;
     nd.red_ctas = 0;
     uint64_t units = 0, outs = nd.m * nd.n;
@@ -77,13 +77,18 @@ void choose_split(const Plan &p, NodePlan &nd) {
         if (std::min(nd.m, nd.n) <= (uint64_t)(kDenseBN / 2)) {
             nd.swap = nd.m < nd.n ? 1 : 0;
             nd.narrow = 1;
+        } else if (p.cta_pairs && std::max(nd.m, nd.n) >= (uint64_t)(2 * kDenseBM)) {
+            // CTA pairs: tiles of 256 rows (the longer side) x 128 columns
+            nd.swap = nd.m < 2 * (uint64_t)kDenseBM ? 1 : 0;
+            nd.pair = 1;
         }
-        // tensor-core tiles are 128 x 128 (or 128 x 64) and one CTA runs per
-        // SM; splits are whole multiples of the 256-entry accumulation chunk
+        // tensor-core tiles are 128 x 128 (or 128 x 64; pairs 256 x 128 on
+        // two SMs) and one CTA runs per SM; splits are whole multiples of the
+        // 256-entry k chunk
         const uint64_t tiles = dense_tiles(nd);
-        const uint64_t sms = kTargetCtas / 2;
+        const uint64_t sms = nd.pair ? kTargetCtas / 4 : kTargetCtas / 2;
         if (tiles >= sms) {
-            if (nd.narrow) return;   // no tail split on narrow tiles
+            if (nd.narrow || nd.pair) return;   // no tail split on narrow tiles or pairs
             // a last wave at most half full runs its tiles as two k halves:
             // it then takes half a tile's time instead of a whole one
             const uint64_t tail = tiles % sms;
@@ -153,18 +158,19 @@ bool fused_reduction(const NodePlan &nd) { return nd.cls == TN_NODE_STREAM && nd
 // execute, or every slice without hoisting) or the variant launches only.
 struct Program {
     const std::vector<Launch> &sched;
-    const std::vector<int32_t> &jobs;   // perm_table entries
+    const std::vector<int32_t> &jobs;     // perm_table entries
+    const std::vector<int32_t> &groups;   // fused groups (LAUNCH_FUSED ranges index this)
 };
 Program program(const Plan &p, bool first) {
-    if (first || !(p.hoist && p.n_slices > 1)) return {p.sched, p.perm_all};
-    return {p.sched_rest, p.perm_rest};
+    if (first || !(p.hoist && p.n_slices > 1)) return {p.sched, p.perm_all, p.fuse_all};
+    return {p.sched_rest, p.perm_rest, p.fuse_rest};
 }
 
 uint64_t launches_of(const Plan &p, bool first) {
     const Program g = program(p, first);
     uint64_t n = (g.jobs.size() + kPermBatch - 1) / kPermBatch;
     for (const auto &L : g.sched) {
-        if (L.kind == LAUNCH_TINY) ++n;
+        if (L.kind == LAUNCH_TINY || L.kind == LAUNCH_FUSED) ++n;
         if (L.kind == LAUNCH_NODE) n += fused_reduction(p.nodes[L.node]) ? 1 : p.nodes[L.node].ksplit > 1 ? 2 : 1;
     }
     return n;
@@ -280,6 +286,16 @@ std::vector<Access> slice_accesses(const Plan &p, bool first) {
         p.table_blob.data() + (p.tiny_off - p.table_off));
     for (const Launch &L : g.sched) {
         if (L.kind == LAUNCH_PERMUTE) continue;
+        if (L.kind == LAUNCH_FUSED) {
+            // reads only the caller's leaves; writes the groups' roots
+            Access a;
+            for (int x = L.first; x < L.first + L.count; ++x) {
+                const NodePlan &rn = p.nodes[p.fuse_groups[g.groups[x]].step];
+                add_range(a.wr, rn.pc, rn.m * rn.n * fmt_bytes(rn.out_fmt));
+            }
+            acc.push_back(a);
+            continue;
+        }
         if (L.kind == LAUNCH_TINY) {
             Access a;
             for (int i = L.first; i < L.first + L.count; ++i) {
@@ -447,7 +463,7 @@ tn_status build_dense_maps(Plan *p) {
         // columns (swapped when the node runs C^T = B A^T)
         const Place &pa = nd.swap ? nd.pb : nd.pa, &pb = nd.swap ? nd.pa : nd.pb;
         const int32_t fa = p->fmt[nd.swap ? nd.b : nd.a], fb = p->fmt[nd.swap ? nd.a : nd.b];
-        const int32_t brows = nd.narrow ? (int32_t)(kDenseBN / 2) : (int32_t)kDenseBN;
+        const int32_t brows = (nd.narrow || nd.pair) ? (int32_t)(kDenseBN / 2) : (int32_t)kDenseBN;
         if (!encode_operand_map(&dm.a, arena + pa.off, (int64_t)dense_rows(nd), (int64_t)nd.k, fa,
                                 nd.ktiled != 0, (int32_t)kDenseBM, &err) ||
             !encode_operand_map(&dm.b, arena + pb.off, (int64_t)dense_cols(nd), (int64_t)nd.k, fb,
@@ -551,8 +567,13 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 ctas += permute_ctas(p->perm_table[job].size);
             }
             pl->cta_start[cnt] = ctas;
+            // algorithmic bytes: every entry read once (complex64) and written
+            // once in the destination's format
             uint64_t bytes = 0;
-            for (int j = 0; j < cnt; ++j) bytes += 16 * (uint64_t)p->perm_table[g.jobs[j0 + j]].size;
+            for (int j = 0; j < cnt; ++j) {
+                const PermDesc &pd = p->perm_table[g.jobs[j0 + j]];
+                bytes += (8 + fmt_bytes(pd.dst_off < 0 ? (int32_t)FMT_C64 : pd.fmt)) * (uint64_t)pd.size;
+            }
             rec.begin(TN_KERNEL_PERMUTE, -1, 0, bytes);
             cudaError_t e = launch_permute(*pl, ctas, dag ? dag->begin() : stream);
             if (dag) dag->end();
@@ -568,6 +589,39 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
             const Launch &L = g.sched[li];
             if (stop_launch >= 0 && (int32_t)li > stop_launch) break;
             if (L.kind == LAUNCH_PERMUTE) continue;   // issued above
+            if (L.kind == LAUNCH_FUSED) {
+                FuseLaunch *fl = new FuseLaunch;
+                std::memset(fl, 0, sizeof(FuseLaunch));
+                fl->ngroups = L.count;
+                fl->accumulate_root = later ? 1 : 0;
+                fl->groups = reinterpret_cast<const FuseGroup *>(ws + p->fuse_off);
+                fl->nodes = reinterpret_cast<const FuseNode *>(ws + p->fuse_node_off);
+                fl->gather = reinterpret_cast<const FuseGather *>(ws + p->fuse_gather_off);
+                fl->levels = reinterpret_cast<const int32_t *>(ws + p->fuse_lvl_off);
+                fl->offs = reinterpret_cast<const int32_t *>(ws + p->fuse_offs_off);
+                fl->arena = arena;
+                fl->out = out;
+                int nsrc = 0, smem = 0;
+                for (int x = 0; x < L.count; ++x) {
+                    const int32_t gi = g.groups[L.first + x];
+                    const FuseGroup &G = p->fuse_groups[gi];
+                    fl->group[x] = gi;
+                    fl->src_first[x] = nsrc;
+                    for (int l = 0; l < G.n_leaves; ++l)
+                        fl->src[nsrc++] = leaf_src[p->fuse_leaves_host[G.first_leaf + l].leaf];
+                    smem = std::max(smem, G.smem_bytes);
+                }
+                rec.begin(TN_KERNEL_FUSED, -1, L.flops, L.bytes);
+                cudaError_t e = launch_fused(*fl, smem, dag ? dag->begin() : stream);
+                if (dag) dag->end();
+                rec.end();
+                delete fl;
+                if (e != cudaSuccess) {
+                    st = cuda_fail(p, e, "launching the fused leaf subtrees");
+                    break;
+                }
+                continue;
+            }
             if (L.kind == LAUNCH_TINY) {
                 TinyLaunch tl;
                 tl.table = reinterpret_cast<const TinyDesc *>(ws + p->tiny_off);
@@ -620,6 +674,9 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 d->lm = nd.swap ? nd.ln : nd.lm;
                 d->ln = nd.swap ? nd.lm : nd.ln;
                 d->narrow = nd.narrow;
+                d->pair = nd.pair;
+                d->chunk_kb = (int32_t)(nd.chunk_k /
+                                        (p->precision == TN_PREC_BF16 || p->precision == TN_PREC_BF16X3 ? 32 : 16));
                 d->accumulate = accumulate;
                 d->out_fmt = nd.out_fmt;
                 d->out_tile = nd.out_tile;
@@ -766,6 +823,17 @@ tn_status tensor_gather(Plan *p, int32_t id, const int64_t *idx, uint64_t count,
         return TN_EINVAL;
     }
     const int n = p->n_tensors;
+    // tensors inside a fused group live only in that CTA's shared memory
+    // (its leaves are read straight from the caller's buffers): only a
+    // group's root reaches memory
+    const bool in_group = id < n ? (p->consumer[id] >= 0 && p->fused[p->consumer[id]] >= 0)
+                                 : (p->fused[id - n] >= 0 &&
+                                    p->fuse_groups[p->fused[id - n]].step != id - n);
+    if (in_group) {
+        p->last_error = "tensor " + std::to_string(id) +
+                        " lives only in the shared memory of a fused leaf subtree";
+        return TN_EINVAL;
+    }
     GatherArgs g;
     std::memset(&g, 0, sizeof(g));
     Place pl;

@@ -26,12 +26,14 @@
 // Accuracy: the tensor core's fp32 accumulation rounds toward zero, so every
 // accumulation into TMEM shrinks the sum a little, always in the same
 // direction, and the shrinkage grows with the number of accumulations.  So
-// the k range of a tile is cut into chunks (64 complex k for the split
-// precisions, 256 for plain bf16 operands); each chunk is accumulated in TMEM
-// from zero, then drained into fp32 registers of the epilogue warps with
-// ordinary round-to-nearest adds (periodic promotion).  Measured on chains
-// of 2^30-2^32-entry nodes: 256-k chunks leave a relative bias of ~2e-6 per
-// node, 64-k chunks a quarter of it.
+// the k range of a tile is cut into chunks (DenseArgs::chunk_kb k-blocks,
+// chosen by the planner: 64, 128 or 256 complex k for the split precisions
+// depending on how many tensor-core nodes the tree holds, 256 for plain bf16
+// operands); each chunk is accumulated in TMEM from zero, then drained into
+// fp32 registers of the epilogue warps with ordinary round-to-nearest adds
+// (periodic promotion).  Measured on chains of 2^30-2^32-entry nodes:
+// 256-k chunks leave a relative bias of ~1.3e-6 per node, 64-k chunks about
+// a quarter of it.
 // The two accumulators are handed over separately: the MMA warp commits D1
 // after the chunk's last D1 products, then issues the D2 products while the
 // drain reads D1, and starts the next chunk's D1 products as soon as the
@@ -96,6 +98,11 @@ struct Cfg {
     // complex k accumulated in TMEM per drain (promotion into fp32 registers)
     static constexpr int CHUNK_K = BF16 ? 256 : 64;
     static constexpr int CHUNK_STAGES = CHUNK_K / KB;
+    // CTA pairs accumulate Cr (and Ci) from six products per k-step instead
+    // of three per accumulator: half the chunk keeps the same number of
+    // accumulations per promotion
+    static constexpr int PAIR_CHUNK_K = CHUNK_K / 2;
+    static constexpr int PAIR_CHUNK_STAGES = PAIR_CHUNK_K / KB;
     static constexpr int STAGE_BYTES = 2 * PLANES * PLANE_TILE;
     static constexpr int STAGES = BF16 ? 6 : THREE ? 2 : 3;
     // the ring holds 192 KiB in every mode; narrow tiles (B of 64 rows) fit
@@ -116,6 +123,11 @@ struct Cfg {
     static constexpr uint32_t IDESC_BASE = (1u << 4) | ((HALF ? 1u : 2u) << 7) |
                                            ((HALF ? 1u : 2u) << 10) | ((128u >> 4) << 24);
     static constexpr uint32_t idesc(uint32_t n) { return IDESC_BASE | ((n >> 3) << 17); }
+    // CTA pair: M = 256 over the pair, N = 128; bit 13 negates A (the
+    // -Ai Bi term of the real part)
+    static constexpr uint32_t IDESC_PAIR =
+        (IDESC_BASE & ~(0x1Fu << 24)) | ((256u >> 4) << 24) | ((128u >> 3) << 17);
+    static constexpr uint32_t IDESC_PAIR_NEG = IDESC_PAIR | (1u << 13);
 };
 constexpr int MAX_STAGES = 8;   // barrier slots (narrow bf16 tiles: 8 stages)
 static_assert(Cfg<MODE_BF16>::NARROW_STAGES <= MAX_STAGES && Cfg<MODE_TF32>::NARROW_STAGES <= MAX_STAGES &&
@@ -231,6 +243,84 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
+// ---- CTA pairs (tcgen05 cta_group::2) ----
+// A pair is a cluster of two CTAs on two SMs.  One MMA instruction of the
+// leader (rank 0) computes M = 256 rows: rows 0-127 from the leader's shared
+// memory and rows 128-255 from the peer's, each CTA holding half of B's N
+// rows; each CTA's TMEM receives its own 128 rows.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs: shared-memory writes before it are visible to
+// the other CTA after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// The same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its cluster address (possibly the peer's).
+// Default (CTA-scope release) semantics: what it orders are the arriving
+// warp's TMEM reads, which tcgen05.fence::before_thread_sync already orders
+// before it; a cluster-scope release would add a memory barrier per arrive.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// TMA into this CTA's shared memory, completing on an mbarrier of either
+// CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+template <int MODE>
+__device__ __forceinline__ void mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t acc, uint32_t idesc) {
+    if constexpr (Cfg<MODE>::HALF) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc));
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(acc));
+    }
+}
+
+// Arrive on the mbarrier at this shared-memory offset in both CTAs of the
+// pair once the leader's MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -319,17 +409,30 @@ __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t n
     nt = r / gm;
 }
 
-template <int MODE>
+// PAIR: the kernel runs as clusters of two CTAs (cta_group::2).  A pair
+// owns output tiles of 256 rows x 128 columns: CTA r loads rows
+// 128 r .. 128 r + 127 of the tile's A and columns 64 r .. 64 r + 63 of its
+// B, the leader issues MMAs of M = 256, N = 128 that form the real and
+// imaginary parts directly (Cr = Ar Br - Ai Bi with the negate-A bit,
+// Ci = Ar Bi + Ai Br), and each CTA's TMEM holds Cr and Ci of its 128 rows:
+// 256 columns, so the accumulators are double-buffered and the drain of one
+// chunk overlaps the MMAs of the next.  Each SM reads half as much of B per
+// MMA as in the single-CTA kernel.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant__ DenseArgs a) {
     using C = Cfg<MODE>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    // narrow tiles: B of 64 rows, smaller stages, more of them, MMA N = 128
-    const bool narrow = a.narrow && !C::THREE;
+    const uint32_t rank = PAIR ? cluster_rank() : 0;
+    // k-blocks accumulated in TMEM per promotion (chosen by the planner)
+    const int CS = a.chunk_kb > 0 ? a.chunk_kb : (PAIR ? C::PAIR_CHUNK_STAGES : C::CHUNK_STAGES);
+    // narrow tiles (B of 64 rows, smaller stages, more of them, MMA N = 128)
+    // and pairs (B of 64 rows per CTA) use the same stage geometry
+    const bool narrow = PAIR || (a.narrow && !C::THREE);
     const int stages = narrow ? C::NARROW_STAGES : C::STAGES;
     const int stage_bytes = narrow ? C::NARROW_STAGE_BYTES : C::STAGE_BYTES;
-    const int bn = narrow ? BN / 2 : BN;
+    const int bn = (narrow && !PAIR) ? BN / 2 : BN;   // output columns of a tile
     const int b_plane = narrow ? PLANE_TILE / 2 : PLANE_TILE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING);
     const uint32_t full0 = smem_u32(bars);
@@ -350,30 +453,47 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
+        // pairs: the two accumulator buffers; the drain warps of both CTAs
+        // release a buffer on the leader's barrier
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, DRAIN_WARPS);
+        mbar_init(tmem_empty, PAIR ? 2 * DRAIN_WARPS : DRAIN_WARPS);
         mbar_init(tmem_full2, 1);
-        mbar_init(tmem_empty2, DRAIN_WARPS);
+        mbar_init(tmem_empty2, PAIR ? 2 * DRAIN_WARPS : DRAIN_WARPS);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (PAIR) {
+            // one warp of each CTA of the pair allocates together
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     fence_before();
     __syncthreads();
+    // pairs: both CTAs' barriers and TMEM exist before any remote access
+    if constexpr (PAIR) cluster_sync();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    // pairs: work items are per pair (the cluster's index)
+    const int64_t wfirst = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const int64_t wstride = PAIR ? gridDim.x / 2 : gridDim.x;
+    const int64_t tile_rows = PAIR ? 2 * BM : BM;
     // barriers and TMEM are set up (shared memory only); global memory after
     // the previous grid on the stream has completed
     pdl_wait();
 
-    const int64_t mtiles = (a.m + BM - 1) / BM, ntiles = (a.n + bn - 1) / bn;
+    const int64_t mtiles = (a.m + tile_rows - 1) / tile_rows, ntiles = (a.n + bn - 1) / bn;
     const int64_t tiles = mtiles * ntiles;
     const int nkb = static_cast<int>((a.k + C::KB - 1) / C::KB);
     // work item w = (tile w / ksplit, k split w % ksplit); a split covers kbs
@@ -392,19 +512,28 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, last_par = 0;   // bit s: stage s has a load; its parity
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+            for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
                 const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
                 int64_t mt, nt;
                 tile_coords(it.t, mtiles, ntiles, mt, nt);
-                const int32_t ym = static_cast<int32_t>(mt * BM), yn = static_cast<int32_t>(nt * bn);
+                // pairs: this CTA's 128 rows of A and 64 rows (columns of the
+                // tile) of B
+                const int32_t ym = static_cast<int32_t>(mt * tile_rows + rank * BM);
+                const int32_t yn = static_cast<int32_t>(nt * bn + (PAIR ? rank * (BN / 2) : 0));
                 const int kb0 = it.kb0, kb1 = it.kb1;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = full0 + 8 * stage;
-                    mbar_expect_tx(bar, stage_bytes);
+                    uint32_t bar = full0 + 8 * stage;
+                    if constexpr (PAIR) {
+                        // the leader's barrier counts both CTAs' bytes
+                        if (rank == 0) mbar_expect_tx(bar, 2 * stage_bytes);
+                        bar = map_to_rank(bar, 0);
+                    } else {
+                        mbar_expect_tx(bar, stage_bytes);
+                    }
                     const uint32_t base = smem_u32(smem + stage * stage_bytes);
                     const int32_t kx = kb * C::KB;
                     // B planes in the same order land as the stacks [re; im]
@@ -413,14 +542,24 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     if (a.ktiled) {
 #pragma unroll
                         for (int p = 0; p < C::PLANES; ++p) {
-                            tma_load_4d(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
-                            tma_load_4d(bbase + p * b_plane, &a.tmB, bar, 0, yn, kb, p);
+                            if constexpr (PAIR) {
+                                tma_load_4d_pair(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
+                                tma_load_4d_pair(bbase + p * b_plane, &a.tmB, bar, 0, yn, kb, p);
+                            } else {
+                                tma_load_4d(base + p * PLANE_TILE, &a.tmA, bar, 0, ym, kb, p);
+                                tma_load_4d(bbase + p * b_plane, &a.tmB, bar, 0, yn, kb, p);
+                            }
                         }
                     } else {
 #pragma unroll
                         for (int p = 0; p < C::PLANES; ++p) {
-                            tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
-                            tma_load_3d(bbase + p * b_plane, &a.tmB, bar, kx, yn, p);
+                            if constexpr (PAIR) {
+                                tma_load_3d_pair(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
+                                tma_load_3d_pair(bbase + p * b_plane, &a.tmB, bar, kx, yn, p);
+                            } else {
+                                tma_load_3d(base + p * PLANE_TILE, &a.tmA, bar, kx, ym, p);
+                                tma_load_3d(bbase + p * b_plane, &a.tmB, bar, kx, yn, p);
+                            }
                         }
                     }
                     issued |= 1u << stage;
@@ -431,21 +570,99 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     }
                 }
             }
-            if (!ok) {
+            // copies in flight complete before the CTA leaves (pairs: the
+            // leader's barriers count the peer's copies too)
+            if (!ok && rank == 0) {
                 for (int s = 0; s < stages; ++s)
                     if (issued & (1u << s)) drain_wait(full0 + 8 * s, (last_par >> s) & 1);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (PAIR && warp == 1 && lane == 0 && rank == 0) {
+            // ---- MMA issuer of a pair ----
+            // buffer b (chunks alternate): Cr at column 256 b, Ci at 256 b + 128
+            uint32_t stage = 0, phase = 0, cnt = 0;
+            bool ok = true;
+            for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const int kb0 = it.kb0, kb1 = it.kb1;
+                const int nch = (kb1 - kb0 + CS - 1) / CS;
+                for (int ch = 0; ch < nch && ok; ++ch, ++cnt) {
+                    const uint32_t b = cnt & 1, ph = (cnt >> 1) & 1;
+                    // both CTAs' drains have read this buffer's last chunk
+                    if (!wait_bounded(b ? tmem_empty2 : tmem_empty, ph ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t cr = tmem + 256 * b, ci = cr + 128;
+                    const int kb_beg = kb0 + ch * CS;
+                    const int kb_end = min(kb1, kb_beg + CS);
+                    for (int kb = kb_beg; kb < kb_end; ++kb) {
+                        if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        const uint32_t base = smem_u32(smem + stage * stage_bytes);
+                        const uint32_t bbase = base + C::PLANES * PLANE_TILE;
+                        const bool first = kb == kb_beg;
+#pragma unroll
+                        for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+                            const uint32_t off = kk * 32;   // 32 bytes of K per instruction
+                            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+                            constexpr uint32_t id = C::IDESC_PAIR, idn = C::IDESC_PAIR_NEG;
+                            if constexpr (C::BF16) {
+                                const uint64_t ar = sdesc(base + off), ai = sdesc(base + PLANE_TILE + off);
+                                const uint64_t br = sdesc(bbase + off), bi = sdesc(bbase + b_plane + off);
+                                mma_pair<MODE>(cr, ar, br, acc, id);
+                                mma_pair<MODE>(cr, ai, bi, 1, idn);   // - Ai Bi
+                                mma_pair<MODE>(ci, ar, bi, acc, id);
+                                mma_pair<MODE>(ci, ai, br, 1, id);
+                            } else {
+                                // planes [re_hi, im_hi, re_lo, im_lo]; each
+                                // product is hi*lo + lo*hi + hi*hi
+                                const uint64_t arh = sdesc(base + off), aih = sdesc(base + PLANE_TILE + off);
+                                const uint64_t arl = sdesc(base + 2 * PLANE_TILE + off);
+                                const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
+                                const uint64_t brh = sdesc(bbase + off), bih = sdesc(bbase + b_plane + off);
+                                const uint64_t brl = sdesc(bbase + 2 * b_plane + off);
+                                const uint64_t bil = sdesc(bbase + 3 * b_plane + off);
+                                mma_pair<MODE>(cr, arl, brh, acc, id);
+                                mma_pair<MODE>(cr, arh, brl, 1, id);
+                                mma_pair<MODE>(cr, arh, brh, 1, id);
+                                mma_pair<MODE>(cr, ail, bih, 1, idn);
+                                mma_pair<MODE>(cr, aih, bil, 1, idn);
+                                mma_pair<MODE>(cr, aih, bih, 1, idn);
+                                mma_pair<MODE>(ci, arl, bih, acc, id);
+                                mma_pair<MODE>(ci, arh, bil, 1, id);
+                                mma_pair<MODE>(ci, arh, bih, 1, id);
+                                mma_pair<MODE>(ci, ail, brh, 1, id);
+                                mma_pair<MODE>(ci, aih, brl, 1, id);
+                                mma_pair<MODE>(ci, aih, brh, 1, id);
+                            }
+                        }
+                        mma_commit_pair(empty0 + 8 * stage);   // both CTAs may refill the stage
+                        if (++stage == stages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit_pair(b ? tmem_full2 : tmem_full);   // both drains may read
+                }
+            }
+            mma_commit_pair(drain);
+            drain_wait(drain, 0);
+        } else if (!PAIR && warp == 1 && lane == 0) {
             // ---- MMA issuer ----
             // four products: D1 = Ar [Br; Bi], D2 = Ai [Br; Bi], 2 bn columns each
             const uint32_t d1 = tmem, d2 = tmem + 2 * bn;
             const uint32_t idesc = C::idesc(C::THREE ? 128u : (uint32_t)(2 * bn));
             uint32_t stage = 0, phase = 0, tphase = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+            for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
                 const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
                 const int kb0 = it.kb0, kb1 = it.kb1;
-                const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
+                const int nch = (kb1 - kb0 + CS - 1) / CS;
                 for (int ch = 0; ch < nch && ok; ++ch) {
                     // D1 must have been read by the drain (three products:
                     // every accumulator, both halves)
@@ -456,8 +673,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     }
                     fence_after();
                     bool d2_free = C::THREE;
-                    const int kb_beg = kb0 + ch * C::CHUNK_STAGES;
-                    const int kb_end = min(kb1, kb_beg + C::CHUNK_STAGES);
+                    const int kb_beg = kb0 + ch * CS;
+                    const int kb_end = min(kb1, kb_beg + CS);
                     for (int kb = kb_beg; kb < kb_end; ++kb) {
                         if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
                             ok = false;
@@ -585,19 +802,55 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const bool quads =
             ep_s && ep_s->vec && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
         const PlanarTile ep_tile = pretiled ? PlanarTile{0, 0, -1, 0} : a.out_tile;
-        uint32_t tphase = 0;
+        uint32_t tphase = 0, pcnt = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < WORK && ok; w += gridDim.x) {
+        for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
             const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
             const int sp = it.sp;
             const int kb0 = it.kb0, kb1 = it.kb1;
-            const int nch = (kb1 - kb0 + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
+            const int nch = (kb1 - kb0 + CS - 1) / CS;
             int64_t mt, nt;
             tile_coords(it.t, mtiles, ntiles, mt, nt);
             float sr[64], si[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) sr[c] = si[c] = 0.f;
-            for (int ch = 0; ch < nch; ++ch) {
+            if constexpr (PAIR) {
+                // buffer b of chunk cnt holds Cr and Ci of this CTA's rows
+                for (int ch = 0; ch < nch; ++ch, ++pcnt) {
+                    const uint32_t b = pcnt & 1, ph = (pcnt >> 1) & 1;
+                    int okv = 0;
+                    if (lane == 0) okv = wait_bounded(b ? tmem_full2 : tmem_full, ph, abort_flag) ? 1 : 0;
+                    okv = __shfl_sync(0xffffffffu, okv, 0);
+                    if (!okv) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t cr = lane_base + 256 * b, ci = cr + 128;
+#pragma unroll
+                    for (int cp = 0; cp < 4; cp += 2) {
+                        const uint32_t col = h * half_cols + cp * 16;
+                        float r0[16], i0v[16], r1[16], i1v[16];
+                        tmem_ld16(cr + col, r0);
+                        tmem_ld16(ci + col, i0v);
+                        tmem_ld16(cr + col + 16, r1);
+                        tmem_ld16(ci + col + 16, i1v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            sr[cp * 16 + c] += r0[c];
+                            si[cp * 16 + c] += i0v[c];
+                            sr[cp * 16 + 16 + c] += r1[c];
+                            si[cp * 16 + 16 + c] += i1v[c];
+                        }
+                    }
+                    fence_before();
+                    __syncwarp();
+                    // release the buffer on the leader's barrier
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(b ? tmem_empty2 : tmem_empty, 0));
+                }
+            }
+            for (int ch = 0; !PAIR && ch < nch; ++ch) {
                 int okv = 0;
                 if (lane == 0) okv = wait_bounded(tmem_full, tphase, abort_flag) ? 1 : 0;
                 okv = __shfl_sync(0xffffffffu, okv, 0);
@@ -714,7 +967,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 other = a.part + (slot * 2 + (it.half ^ 1)) * (64 * 32);
             }
             void *dst = plain ? static_cast<void *>(a.part + (int64_t)sp * plane) : a.C;
-            const int64_t i0 = mt * BM + q * 32;
+            const int64_t i0 = mt * tile_rows + rank * BM + q * 32;
             const int64_t i = i0 + lane;
             const int64_t offm = i < a.m ? (plain ? i * a.n : sep_offset(a.lm, i)) : 0;
             const int64_t bm = ep_s ? sep_offset(a.lm, i0) : 0;
@@ -810,11 +1063,19 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 #undef TAIL_FIRST
     fence_before();
     __syncthreads();
+    // pairs: neither CTA leaves (or frees TMEM) while the other may still
+    // reach its shared memory or TMEM
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        if constexpr (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(TMEM_COLS)
+                         : "memory");
     }
     if (threadIdx.x == 0 && *abort_flag && a.status)
         atomicCAS(&a.status->code, ERR_NONE, ERR_TIMEOUT);
@@ -823,12 +1084,16 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
 }  // namespace
 
 cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream) {
-    const int64_t bn = (args.narrow && !args.three) ? BN / 2 : BN;
-    const int64_t tiles = ((args.m + BM - 1) / BM) * ((args.n + bn - 1) / bn);
+    const bool pair = args.pair && !args.three;
+    const int64_t bn = (args.narrow && !args.three && !pair) ? BN / 2 : BN;
+    const int64_t rows = pair ? 2 * BM : BM;
+    const int64_t tiles = ((args.m + rows - 1) / rows) * ((args.n + bn - 1) / bn);
     const int64_t work = args.ksplit > 1          ? tiles * args.ksplit
                          : args.tail_first >= 0 ? args.tail_first + 2 * (tiles - args.tail_first)
                                                 : tiles;
-    const int grid = static_cast<int>(work < num_sms ? work : num_sms);
+    // pairs: one cluster of two CTAs per work item, at most one CTA per SM
+    const int64_t units = pair ? num_sms / 2 : num_sms;
+    const int grid = static_cast<int>((work < units ? work : units) * (pair ? 2 : 1));
     if (grid <= 0) return cudaSuccess;
     auto launch = [&](auto kernel, int smem, bool *attr) -> cudaError_t {
         if (!*attr) {
@@ -836,18 +1101,37 @@ cudaError_t launch_dense(const DenseArgs &args, int num_sms, cudaStream_t stream
             if (e != cudaSuccess) return e;
             *attr = true;
         }
-        return launch_pdl(kernel, dim3(grid), dim3(THREADS), (size_t)smem, stream, args);
+        if (!pair) return launch_pdl(kernel, dim3(grid), dim3(THREADS), (size_t)smem, stream, args);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attrs[2];
+        attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[0].val.programmaticStreamSerializationAllowed = 1;
+        attrs[1].id = cudaLaunchAttributeClusterDimension;
+        attrs[1].val.clusterDim.x = 2;
+        attrs[1].val.clusterDim.y = 1;
+        attrs[1].val.clusterDim.z = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, kernel, args);
     };
     static bool attr_bf16 = false, attr_tf32 = false, attr_3p = false, attr_bf16x3 = false;
+    static bool attr_bf16_p = false, attr_tf32_p = false, attr_bf16x3_p = false;
     cudaError_t e;
     if (args.bf16x3)
-        e = launch(dense_kernel<MODE_BF16X3>, Cfg<MODE_BF16X3>::SMEM, &attr_bf16x3);
+        e = pair ? launch(dense_kernel<MODE_BF16X3, true>, Cfg<MODE_BF16X3>::SMEM, &attr_bf16x3_p)
+                 : launch(dense_kernel<MODE_BF16X3, false>, Cfg<MODE_BF16X3>::SMEM, &attr_bf16x3);
     else if (args.bf16)
-        e = launch(dense_kernel<MODE_BF16>, Cfg<MODE_BF16>::SMEM, &attr_bf16);
+        e = pair ? launch(dense_kernel<MODE_BF16, true>, Cfg<MODE_BF16>::SMEM, &attr_bf16_p)
+                 : launch(dense_kernel<MODE_BF16, false>, Cfg<MODE_BF16>::SMEM, &attr_bf16);
     else if (args.three)
-        e = launch(dense_kernel<MODE_TF32_3P>, Cfg<MODE_TF32_3P>::SMEM, &attr_3p);
+        e = launch(dense_kernel<MODE_TF32_3P, false>, Cfg<MODE_TF32_3P>::SMEM, &attr_3p);
     else
-        e = launch(dense_kernel<MODE_TF32>, Cfg<MODE_TF32>::SMEM, &attr_tf32);
+        e = pair ? launch(dense_kernel<MODE_TF32, true>, Cfg<MODE_TF32>::SMEM, &attr_tf32_p)
+                 : launch(dense_kernel<MODE_TF32, false>, Cfg<MODE_TF32>::SMEM, &attr_tf32);
     return e;
 }
 

@@ -54,6 +54,149 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
         }
         return so;
     };
+    if (d.tax >= 0) {
+        // True transpose through shared memory.  Tiles of 32 entries along
+        // axis tax (contiguous in the source) by 32 along the destination's
+        // innermost axis L: a warp reads 32 consecutive source entries, and
+        // after the tile turns in shared memory a warp writes 32 consecutive
+        // destination entries.  The other axes index the tiles.
+        __shared__ float2 tile[32][33];
+        const int L = rank - 1, ax = d.tax;
+        const int64_t na = (d.dims[ax] + 31) / 32, nl = (d.dims[L] + 31) / 32;
+        int64_t dstride_a = 1;
+        for (int x = ax + 1; x < rank; ++x) dstride_a *= d.dims[x];
+        const int64_t ntiles = size / (d.dims[ax] * d.dims[L]) * na * nl;
+        const int lane = threadIdx.x & 31, wrp = threadIdx.x >> 5;
+        for (int64_t t = local; t < ntiles; t += ctas) {
+            // tile t -> (rest, ta, tl): tl fastest, then ta, then the other
+            // axes in destination order (row-major)
+            int64_t rem = t;
+            const int64_t tl = rem % nl;
+            rem /= nl;
+            const int64_t ta = rem % na;
+            rem /= na;
+            int64_t sbase = 0, dbase = 0, dstr = d.dims[L];
+#pragma unroll 1
+            for (int x = L - 1; x >= 0; --x) {
+                if (x == ax) {
+                    dstr *= d.dims[x];
+                    continue;
+                }
+                const int64_t dg = rem % d.dims[x];
+                rem /= d.dims[x];
+                sbase += dg * d.sstride[x];
+                dbase += dg * dstr;
+                dstr *= d.dims[x];
+            }
+            const int64_t a0 = ta * 32, l0 = tl * 32;
+            __syncthreads();   // the previous tile's readers are done
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int r = wrp + 8 * it;   // along L
+                const int64_t ia = a0 + lane, il = l0 + r;
+                if (ia < d.dims[ax] && il < d.dims[L])
+                    tile[r][lane] = src[sbase + ia + il * d.sstride[L]];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int c = wrp + 8 * it;   // along tax
+                const int64_t ia = a0 + c, il = l0 + lane;
+                if (ia < d.dims[ax] && il < d.dims[L])
+                    store_entry(dst, fmt, size, dbase + ia * dstride_a + il, tile[lane][c], a.accumulate,
+                                d.tile);
+            }
+        }
+        return;
+    }
+    if (d.contig && d.tile.kt != 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        // A conversion into a K-tiled planar operand: the source is row-major
+        // [rows][k], the destination per plane [k / kt][rows][kt].  Read
+        // along rows and write along tile rows are both strided the other
+        // way, so blocks of 32 rows x 128 entries turn through shared
+        // memory: a warp reads 512 contiguous source bytes, and a warp writes
+        // whole 64-byte tile rows of 32 consecutive rows (contiguous in every
+        // plane).
+        __shared__ __align__(16) float2 blk[32][128 + 4];
+        const PlanarTile &tl = d.tile;
+        const int64_t rows = tl.rows, kk = tl.k;
+        const int kt = tl.kt;
+        const int64_t nrb = (rows + 31) / 32, ncb = (kk + 127) / 128;
+        const PlanarTile untiled{0, 0, -1, 0};
+        for (int64_t u = local; u < nrb * ncb; u += ctas) {
+            const int64_t r0 = (u / ncb) * 32, c0 = (u % ncb) * 128;
+            const int cw = (int)min((int64_t)128, kk - c0);   // a multiple of kt
+            __syncthreads();   // the previous block's readers are done
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int f = threadIdx.x + kThreads * i;   // 64 pairs of entries per row
+                const int row = f >> 6, c2 = (f & 63) * 2;
+                if (r0 + row < rows && c2 < cw) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src + (r0 + row) * kk + c0 + c2);
+                    *reinterpret_cast<float4 *>(&blk[row][c2]) = v;
+                }
+            }
+            __syncthreads();
+            // quads of 4 entries: 8 kt quads per tile row block of 32 rows
+            const int quads = (cw / kt) * 8 * kt;
+            for (int q = threadIdx.x; q < quads; q += kThreads) {
+                const int ct = q / (8 * kt), e = (q - ct * 8 * kt) * 4;
+                const int row = e / kt, cl = e - row * kt;
+                if (r0 + row >= rows) continue;
+                const float2 v4[4] = {blk[row][ct * kt + cl], blk[row][ct * kt + cl + 1],
+                                      blk[row][ct * kt + cl + 2], blk[row][ct * kt + cl + 3]};
+                const int64_t phys = (((c0 / kt) + ct) * rows + r0 + row) * kt + cl;
+                store_quad(dst, fmt, size, phys, v4, a.accumulate, untiled);
+            }
+        }
+        return;
+    }
+    if (d.contig && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+        // a format conversion: source entry e is destination entry e.  Runs
+        // of 16 entries are walked in the destination's physical order
+        // (consecutive threads write consecutive addresses of every plane);
+        // a K-tiled run (16 entries of one tile row) comes from 16
+        // consecutive entries of one source row: 128 bytes, eight 16-byte
+        // loads when the source is 16-byte aligned
+        const PlanarTile &tl = d.tile;
+        const PlanarTile untiled{0, 0, -1, 0};
+        const bool src16 = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+        const int64_t runs = size / 16;
+        const int64_t stride = (int64_t)ctas * kThreads;
+        for (int64_t u = (int64_t)local * kThreads + threadIdx.x; u < runs; u += stride) {
+            const int64_t p0 = u * 16;
+            int64_t e0 = p0;
+            if (tl.kt != 0) {
+                // physical ((c / kt) * rows + r) * kt + c % kt -> r * k + c
+                const int sh = tl.kt == 32 ? 5 : 4;
+                const int64_t cl = p0 & (tl.kt - 1), t2 = p0 >> sh;
+                const int64_t ct = t2 / tl.rows, r = t2 - ct * tl.rows;
+                e0 = r * tl.k + (ct << sh) + cl;
+            }
+            float2 v[16];
+            if (src16) {
+                const float4 *s4 = reinterpret_cast<const float4 *>(src + e0);
+                float4 w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = s4[q];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    v[2 * q] = make_float2(w[q].x, w[q].y);
+                    v[2 * q + 1] = make_float2(w[q].z, w[q].w);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[q] = src[e0 + q];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 v4[4] = {v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]};
+                store_quad(dst, fmt, size, p0 + 4 * q, v4, a.accumulate, untiled);
+            }
+        }
+        return;
+    }
     if (d.vec4 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
         // four consecutive entries per thread: consecutive in the source
         // too; all loads of the pass first, then one store per plane each

@@ -108,6 +108,8 @@ struct DenseArgs {
     int32_t three;        // operands are FMT_GAUSS6: three real products
     int32_t narrow;       // 128 x 64 tiles (B boxes of 64 rows, MMA N = 128)
     int32_t ktiled;       // operands K-tiled (4-D maps) rather than row-major (3-D)
+    int32_t pair;         // clusters of two CTAs (tiles of 256 rows; B maps of 64-row boxes)
+    int32_t chunk_kb;     // k-blocks (stages) accumulated in TMEM per promotion
     DevStatus *status;
     // split-K as in NodeArgs (kchunk a multiple of 256)
     int32_t ksplit;
@@ -161,6 +163,25 @@ struct GatherLaunch {
     int64_t size[kGatherBatch];        // elements
 };
 cudaError_t launch_gather(const GatherLaunch &args, int total_ctas, cudaStream_t stream);
+
+// One launch of fused leaf subtrees (FuseGroup in plan.h): CTA x runs group
+// group[x], whose leaves' slice-shifted caller pointers are
+// src[src_first[x] ...].
+struct FuseLaunch {
+    int32_t ngroups;
+    int32_t accumulate_root;   // later slices: a group rooted at the tree's root adds into out
+    const FuseGroup *groups;   // device tables (workspace)
+    const FuseNode *nodes;
+    const FuseGather *gather;
+    const int32_t *levels;
+    const int32_t *offs;
+    char *arena;
+    float2 *out;
+    int32_t group[kFuseBatch];
+    int32_t src_first[kFuseBatch];
+    const float2 *src[kFuseSrc];
+};
+cudaError_t launch_fused(const FuseLaunch &args, int smem_bytes, cudaStream_t stream);
 
 // Entries of one stored tensor read back as complex64 (tn_plan_tensor_gather):
 // dst[t] = the value of logical entry idx[t] (row-major in the tensor's

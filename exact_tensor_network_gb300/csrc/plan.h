@@ -118,6 +118,16 @@ struct PermDesc {
     // of 4 long, and size is a multiple of 4: a thread moves four
     // consecutive entries at a time
     int32_t vec4;
+    // 1: the source holds the entries in the destination's order (a format
+    // conversion, possibly K-tiled, of a leaf already in lifetime order) and
+    // size is a multiple of 16: a thread moves runs of 16 entries, 16-byte
+    // loads and stores
+    int32_t contig;
+    // a true transpose: the source's contiguous axis tax is not the
+    // destination's innermost one; 32 x 32 tiles over (tax, innermost) go
+    // through shared memory so that both sides move whole 32-entry rows.
+    // -1 when not used
+    int32_t tax;
     int32_t pad;
 };
 
@@ -158,6 +168,12 @@ struct NodePlan {
     // dense class: tiles of 128 x 64 (n <= 64 after the swap): B stacked
     // [Br; Bi] fills one N = 128 MMA instead of half an N = 256 one
     int32_t narrow;
+    // dense class: runs on CTA pairs (tiles of 256 x 128, cta_group::2)
+    int32_t pair;
+    // dense class: complex k accumulated in TMEM per promotion into fp32
+    // registers (the tensor core's accumulation rounds toward zero: shorter
+    // chunks, smaller bias; see choose_chunks)
+    int32_t chunk_k;
     // dense class: byte offset (from the workspace start) of the node's
     // address-order store table (EpTable), or -1 when it has none
     int64_t ep_off;
@@ -189,7 +205,8 @@ inline uint64_t dense_rows(const NodePlan &nd) { return nd.swap ? nd.n : nd.m; }
 inline uint64_t dense_cols(const NodePlan &nd) { return nd.swap ? nd.m : nd.n; }
 inline uint64_t dense_tiles(const NodePlan &nd) {
     const uint64_t bn = nd.narrow ? kDenseBN / 2 : kDenseBN;
-    return ((dense_rows(nd) + kDenseBM - 1) / kDenseBM) * ((dense_cols(nd) + bn - 1) / bn);
+    const uint64_t bm = nd.pair ? 2 * kDenseBM : kDenseBM;
+    return ((dense_rows(nd) + bm - 1) / bm) * ((dense_cols(nd) + bn - 1) / bn);
 }
 inline uint64_t part_bytes(const NodePlan &nd) {
     if (nd.ksplit > 1) return (uint64_t)nd.ksplit * nd.m * nd.n * 8;
@@ -249,15 +266,70 @@ struct TinyDesc {
 // Launch schedule: every node gets a stage one past its operands' stages;
 // stage by stage, the tiny nodes of the stage run as one batched launch and
 // the other nodes one launch each.
-enum LaunchKind : int32_t { LAUNCH_PERMUTE = 0, LAUNCH_NODE = 1, LAUNCH_TINY = 2 };
+enum LaunchKind : int32_t { LAUNCH_PERMUTE = 0, LAUNCH_NODE = 1, LAUNCH_TINY = 2, LAUNCH_FUSED = 3 };
 struct Launch {
     int32_t kind;
     int32_t node;          // LAUNCH_NODE: step
-    int32_t first, count;  // LAUNCH_TINY: range in the tiny table
+    int32_t first, count;  // LAUNCH_TINY: range in the tiny table; LAUNCH_FUSED:
+                           // range in the program's fused-group list
     int32_t ctas;          // LAUNCH_TINY: CTAs of the launch
     uint64_t flops, bytes; // algorithmic work of the launch (measurement)
 };
 
+// Fused leaf subtrees ("leaf-gate absorption").  Near the leaves, a tree is
+// mostly chains of tiny steps (gates absorbed into wires, small tensors
+// meeting); each would cost a batched launch per tree level and a round
+// trip through HBM.  A fused group is a maximal subtree whose leaves and
+// intermediates are all small: one CTA reads its leaves straight from the
+// caller's buffers (their permutation into lifetime order absorbed into the
+// load: a list of source offsets), computes every step in shared memory
+// level by level, and writes only the subtree's root, in its consumer's
+// format.  All groups of a slice are independent of every other launch, so
+// they run in one launch at the start.  Limits: leaves and step outputs of
+// at most kFuseMaxTensor entries, a group's tensors together at most
+// kFuseSmemEntries (they all stay in shared memory: no reuse), at most
+// kFuseMaxMacs multiply-adds per group (one CTA does them all) and
+// kFuseMaxDescBytes of step descriptors and output offsets.
+constexpr int64_t kFuseMaxTensor = 2048;
+constexpr int64_t kFuseSmemEntries = 8192;   // 64 KiB of complex64
+constexpr int64_t kFuseMaxMacs = 1 << 17;    // complex multiply-adds of a group (one CTA)
+constexpr int64_t kFuseMaxDescBytes = 24 * 1024;
+constexpr int kFuseBatch = 256;              // groups per launch
+constexpr int kFuseSrc = 2048;               // leaf pointers per launch
+struct FuseLeaf {        // one leaf of a group (host side: its launch pointer)
+    int32_t slot;        // shared-memory offset (complex entries)
+    int32_t size;        // entries after slicing
+    int32_t leaf;        // caller's leaf index
+};
+struct FuseGather {      // one leaf entry loaded into shared memory: entry e of
+                         // a group's list goes to shared-memory slot e
+    int32_t src;         // element offset in the (slice-shifted) caller's leaf
+    int32_t leaf;        // the group's leaf (0 .. n_leaves - 1)
+};
+struct FuseNode {        // one step of a group (copied to shared memory)
+    int32_t a, b;        // shared-memory offsets of the operands
+    int32_t c;           // shared-memory offset of the output; -1: the group's root
+    int32_t m, n, k;
+    int32_t lanes;       // threads that split one output's k range (power of two <= 32)
+    int32_t obase;       // first thread item of this step in its level (a multiple of
+                         // 32: a warp never holds two steps)
+    int32_t off;         // output offsets: offM(i) at off + i, offN(j) at off + m + j
+};
+struct FuseGroup {
+    int32_t first_leaf, n_leaves;    // host leaf list (launch pointers)
+    int32_t first_gather, n_gather;  // leaf entries (= shared-memory slots 0 .. n_gather-1)
+    int32_t first_node, n_nodes;
+    int32_t first_level, n_levels;   // level l: nodes [lvl[l], lvl[l + 1]) of the node list
+    int32_t first_off, n_off;        // output offset table
+    int32_t smem;                    // shared-memory entries of the group's tensors
+    int32_t smem_bytes;              // tensors + descriptors (nodes, levels, offsets)
+    int32_t is_root;                 // the root is the tree's root (caller's output)
+    int32_t out_fmt;
+    int64_t out_off;                 // arena byte offset of the root's output (-1: caller's)
+    int32_t step;                    // tree step of the group's root
+    int32_t pad;
+    PlanarTile out_tile;
+};
 // Tiny nodes: at most this many complex multiply-adds (m n k), a k short
 // enough for one pass of a thread group over it, and few outputs (each
 // output reads its own A and B rows, which a tiled kernel would share).
@@ -326,6 +398,8 @@ struct Plan {
     // execution layout
     int32_t policy = TN_POLICY_AUTO;
     int32_t three_products = 0;   // tn_plan_set_three_products
+    int32_t cta_pairs = 0;        // tn_plan_set_cta_pairs
+    int32_t chunk_k = 0;          // tn_plan_set_promotion_chunk (0: per-plan rule)
     int32_t hoist = 1;            // tn_plan_set_hoisting
     uint64_t table_off = 0, table_bytes = 0;    // PermDesc table
     uint64_t arena_off = 0, arena_bytes = 0;
@@ -344,6 +418,15 @@ struct Plan {
     std::vector<Launch> sched_rest;
     std::vector<int32_t> perm_all, perm_rest;   // perm_table entries of each program
     uint64_t tiny_off = 0;                      // workspace offset of the TinyDesc table
+    // fused leaf subtrees (tn_plan_set_fusion): groups and their tables
+    int32_t fuse = 1;
+    std::vector<int32_t> fused;                 // per step: index of its group, or -1
+    std::vector<FuseGroup> fuse_groups;
+    std::vector<int32_t> fuse_all, fuse_rest;   // groups each program runs
+    uint64_t fuse_off = 0;                      // workspace offsets of FuseGroup[], FuseNode[],
+    uint64_t fuse_node_off = 0, fuse_gather_off = 0, fuse_lvl_off = 0, fuse_offs_off = 0;   // FuseGather[], levels, offsets
+    int32_t fuse_smem = 0;                      // largest group's shared memory (bytes)
+    std::vector<FuseLeaf> fuse_leaves_host;     // host copy of FuseLeaf[] (launch parameters)
     std::vector<int32_t> fmt;                   // per SSA id (Fmt)
     std::vector<DenseMaps> dense_maps;          // per dense node, set at bind
     void *maps_ws = nullptr;                    // workspace the maps point into

@@ -167,6 +167,165 @@ bool make_ep_table(const NodePlan &nd, EpTable *t) {
     return true;
 }
 
+// Fused leaf subtrees (FuseGroup in plan.h).  A step may sit in a group when
+// it is tiny, its output and its k have at most kFuseMaxTensor entries, each
+// operand is a small leaf (at most kFuseMaxTensor entries) or such a step,
+// and its subtree's tensors together fit kFuseSmemEntries, its multiply-adds
+// kFuseMaxMacs and its descriptors kFuseMaxDescBytes.  A group is a maximal
+// such subtree (at least one step); its root is a step whose consumer cannot
+// join it.
+int64_t fuse_desc_bytes(int64_t nodes, int64_t offsets, int64_t levels) {
+    return nodes * (int64_t)sizeof(FuseNode) + 4 * (offsets + levels + 1);
+}
+
+void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather> &fgather,
+                 std::vector<int32_t> &flevels, std::vector<int32_t> &foffs,
+                 std::vector<FuseLeaf> &fleaves, std::vector<uint8_t> &leaf_fused) {
+    const int n = p->n_tensors, S = (int)p->nodes.size();
+    std::vector<uint8_t> ok(n + S, 0);
+    std::vector<int64_t> cost(n + S, 0), macs(n + S, 0), nsteps(n + S, 0), noffs(n + S, 0);
+    for (int t = 0; t < n; ++t) {
+        const LeafPlan &lp = p->leaves[t];
+        ok[t] = lp.size <= kFuseMaxTensor && lp.full_size < (int64_t(1) << 31);
+        cost[t] = lp.size;
+    }
+    for (int s = 0; s < S; ++s) {
+        const NodePlan &nd = p->nodes[s];
+        const int64_t mn = (int64_t)(nd.m * nd.n);
+        cost[nd.out] = cost[nd.a] + cost[nd.b] + mn;
+        macs[nd.out] = macs[nd.a] + macs[nd.b] + mn * (int64_t)nd.k;
+        nsteps[nd.out] = nsteps[nd.a] + nsteps[nd.b] + 1;
+        noffs[nd.out] = noffs[nd.a] + noffs[nd.b] + (int64_t)(nd.m + nd.n);
+        ok[nd.out] = nd.cls == TN_NODE_TINY && ok[nd.a] && ok[nd.b] && mn <= kFuseMaxTensor &&
+                     (int64_t)nd.k <= kFuseMaxTensor && cost[nd.out] <= kFuseSmemEntries &&
+                     macs[nd.out] <= kFuseMaxMacs &&
+                     fuse_desc_bytes(nsteps[nd.out], noffs[nd.out], nsteps[nd.out]) <= kFuseMaxDescBytes;
+    }
+    for (int r = 0; r < S; ++r) {
+        const NodePlan &rn = p->nodes[r];
+        if (!ok[rn.out]) continue;
+        const int cons = p->consumer[rn.out];
+        if (cons >= 0 && ok[p->nodes[cons].out]) continue;   // the group goes on above
+        // the subtree's steps (ascending: operands before their consumers)
+        // and leaves
+        std::vector<int> steps, leaves, stack{rn.out};
+        while (!stack.empty()) {
+            const int id = stack.back();
+            stack.pop_back();
+            if (id < n) {
+                leaves.push_back(id);
+                continue;
+            }
+            steps.push_back(id - n);
+            stack.push_back(p->nodes[id - n].a);
+            stack.push_back(p->nodes[id - n].b);
+        }
+        std::sort(steps.begin(), steps.end());
+        std::sort(leaves.begin(), leaves.end());
+        const int gi = (int)p->fuse_groups.size();
+        FuseGroup G;
+        std::memset(&G, 0, sizeof(G));
+        G.step = r;
+        G.first_leaf = (int32_t)fleaves.size();
+        G.n_leaves = (int32_t)leaves.size();
+        G.first_gather = (int32_t)fgather.size();
+        // shared memory: leaves first (in list order: slot e holds gather
+        // entry e), then the outputs of the inner steps
+        std::vector<int32_t> slot(n + S, -1);
+        int32_t used = 0;
+        for (size_t l = 0; l < leaves.size(); ++l) {
+            const int t = leaves[l];
+            const LeafPlan &lp = p->leaves[t];
+            fleaves.push_back(FuseLeaf{used, (int32_t)lp.size, t});
+            slot[t] = used;
+            // entry e (row-major over the lifetime order) comes from
+            // sum digit[d] * sstride[d] of the caller's (slice-shifted) leaf
+            const PermDesc &d = lp.perm;
+            for (int64_t e = 0; e < lp.size; ++e) {
+                int64_t rem = e, so = 0;
+                for (int x = d.rank - 1; x >= 0; --x) {
+                    so += (rem % d.dims[x]) * d.sstride[x];
+                    rem /= d.dims[x];
+                }
+                fgather.push_back(FuseGather{(int32_t)so, (int32_t)l});
+            }
+            used += (int32_t)lp.size;
+            leaf_fused[t] = 1;
+        }
+        G.n_gather = used;
+        std::vector<int> level(n + S, 0);
+        int nlev = 0;
+        for (int s : steps) {
+            const NodePlan &nd = p->nodes[s];
+            level[nd.out] = 1 + std::max(level[nd.a], level[nd.b]);
+            nlev = std::max(nlev, level[nd.out]);
+            if (s != r) {
+                slot[nd.out] = used;
+                used += (int32_t)(nd.m * nd.n);
+            }
+        }
+        G.smem = used;
+        G.first_node = (int32_t)fnodes.size();
+        G.n_nodes = (int32_t)steps.size();
+        G.first_level = (int32_t)flevels.size();
+        G.n_levels = nlev;
+        G.first_off = (int32_t)foffs.size();
+        for (int lv = 1; lv <= nlev; ++lv) {
+            flevels.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
+            int32_t obase = 0;
+            for (int s : steps) {
+                const NodePlan &nd = p->nodes[s];
+                if (level[nd.out] != lv) continue;
+                FuseNode f;
+                f.a = slot[nd.a];
+                f.b = slot[nd.b];
+                f.c = s == r ? -1 : slot[nd.out];
+                f.m = (int32_t)nd.m;
+                f.n = (int32_t)nd.n;
+                f.k = (int32_t)nd.k;
+                // a few k entries per thread: long k ranges are split over
+                // up to 32 threads (one serial chain of k multiply-adds per
+                // thread would be the group's critical path)
+                f.lanes = 1;
+                while (f.lanes < 32 && f.lanes * 4 < f.k) f.lanes *= 2;
+                f.obase = obase;
+                obase += (f.m * f.n * f.lanes + 31) / 32 * 32;
+                f.off = (int32_t)(foffs.size() - (size_t)G.first_off);
+                for (uint64_t i = 0; i < nd.m; ++i) foffs.push_back((int32_t)sep_offset_host(nd.lm, (int64_t)i));
+                for (uint64_t j = 0; j < nd.n; ++j) foffs.push_back((int32_t)sep_offset_host(nd.ln, (int64_t)j));
+                fnodes.push_back(f);
+            }
+        }
+        flevels.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
+        G.n_off = (int32_t)(foffs.size() - (size_t)G.first_off);
+        G.smem_bytes = (int32_t)(8 * (int64_t)G.smem + fuse_desc_bytes(G.n_nodes, G.n_off, G.n_levels));
+        for (int s : steps) p->fused[s] = gi;
+        p->fuse_smem = std::max(p->fuse_smem, G.smem_bytes);
+        p->fuse_groups.push_back(G);
+    }
+}
+
+// Promotion chunk of the tensor-core nodes.  The tensor core accumulates in
+// TMEM with rounding toward zero, which biases every node's sums toward zero
+// by about 1.3e-6 (relative) with 256-k chunks, half of that with 128 and a
+// quarter with 64 (measured on chains of 2^30- to 2^32-entry nodes), and the
+// relative errors of a tree's nodes add up at its root.  The chunk is the
+// longest whose bias times the number of tensor-core nodes stays within 4e-6
+// (the complex64 tolerance is 1e-5): a longer chunk costs less bookkeeping
+// per k.  CTA pairs accumulate six products per k-step into one accumulator
+// instead of three: half the chunk.  Plain bf16 operands (tolerance 2e-2)
+// keep 256.
+void choose_chunks(Plan *p) {
+    int dense = 0;
+    for (const auto &nd : p->nodes) dense += nd.cls == TN_NODE_DENSE ? 1 : 0;
+    int32_t chunk = dense <= 3 ? 256 : dense <= 6 ? 128 : 64;
+    if (p->precision == TN_PREC_BF16) chunk = 256;
+    if (p->chunk_k > 0) chunk = p->chunk_k;   // tn_plan_set_promotion_chunk
+    // at least one pipeline stage (16 complex k of tf32 planes, 32 of bf16)
+    const int32_t stage = (p->precision == TN_PREC_BF16 || p->precision == TN_PREC_BF16X3) ? 32 : 16;
+    for (auto &nd : p->nodes) nd.chunk_k = std::max(stage, nd.pair ? chunk / 2 : chunk);
+}
+
 }  // namespace
 
 tn_status layout_plan(Plan *p) {
@@ -188,12 +347,14 @@ tn_status layout_plan(Plan *p) {
         if (nd.cls != TN_NODE_DENSE) continue;
         int32_t f = dense_fmt;
         if (f == FMT_SPLIT4 && p->three_products && !nd.narrow && three_products_pay(nd)) {
+            nd.pair = 0;   // the three-product kernel runs on single CTAs
             f = FMT_GAUSS6;
             nd.three_products = 1;
         }
         p->fmt[nd.a] = p->fmt[nd.b] = f;
     }
     for (auto &nd : p->nodes) nd.out_fmt = nd.is_root ? FMT_C64 : p->fmt[nd.out];
+    choose_chunks(p);
     // K-tiling of tensor-core operands whose k fills whole tiles
     const PlanarTile untiled{0, 0, -1, 0};
     std::vector<PlanarTile> tile(n + S, untiled);
@@ -211,15 +372,29 @@ tn_status layout_plan(Plan *p) {
     }
     for (auto &nd : p->nodes) nd.out_tile = nd.is_root ? untiled : tile[nd.out];
 
-    // 3. schedule
+    // 2b. fused leaf subtrees (see FuseGroup in plan.h)
+    std::vector<FuseNode> fnodes;
+    std::vector<FuseGather> fgather;
+    std::vector<FuseLeaf> fleaves;
+    std::vector<int32_t> flevels, foffs;
+    std::vector<uint8_t> leaf_fused(n, 0);
+    p->fused.assign(S, -1);
+    p->fuse_groups.clear();
+    p->fuse_smem = 0;
+    if (p->fuse && p->policy == TN_POLICY_AUTO && S > 0)
+        form_groups(p, fnodes, fgather, flevels, foffs, fleaves, leaf_fused);
+
+    // 3. schedule (group roots are ready after the fused launch at the start)
     std::vector<int> stage(n + S, 0);
     int max_stage = 0;
     for (const auto &nd : p->nodes) {
+        if (p->fused[nd.step] >= 0) continue;
         stage[nd.out] = 1 + std::max(stage[nd.a], stage[nd.b]);
         max_stage = std::max(max_stage, stage[nd.out]);
     }
     std::vector<std::vector<int>> by_stage(max_stage + 1);
-    for (int s = 0; s < S; ++s) by_stage[stage[n + s]].push_back(s);
+    for (int s = 0; s < S; ++s)
+        if (p->fused[s] < 0) by_stage[stage[n + s]].push_back(s);
     // Slice-invariant subtrees (section 1.1 of "Crossing the single-GPU
     // memory wall": slicing repeats every node once per slice, although a
     // node whose subtree holds no sliced leaf computes the same tensor in
@@ -235,7 +410,44 @@ tn_status layout_plan(Plan *p) {
     std::vector<std::vector<int>> tiny_batches, tiny_batches_rest;
     // one program: stage by stage, the stage's tiny nodes in batches of at
     // most kTinyLaunchNodes (independent launches), then its other nodes
+    p->fuse_all.clear();
+    p->fuse_rest.clear();
+    for (int g = 0; g < (int)p->fuse_groups.size(); ++g) {
+        p->fuse_all.push_back(g);
+        if (hoist && p->variant[n + p->fuse_groups[g].step]) p->fuse_rest.push_back(g);
+    }
     auto build = [&](std::vector<Launch> &sched, std::vector<std::vector<int>> &batches, bool rest) {
+        // fused groups: batches of at most kFuseBatch groups and kFuseSrc leaves
+        const std::vector<int32_t> &groups = rest ? p->fuse_rest : p->fuse_all;
+        for (size_t g0 = 0; g0 < groups.size();) {
+            Launch L{};
+            L.kind = LAUNCH_FUSED;
+            L.node = -1;
+            L.first = (int32_t)g0;
+            int leaves = 0;
+            size_t g1 = g0;
+            while (g1 < groups.size() && (int)(g1 - g0) < kFuseBatch &&
+                   leaves + p->fuse_groups[groups[g1]].n_leaves <= kFuseSrc) {
+                const FuseGroup &G = p->fuse_groups[groups[g1]];
+                leaves += G.n_leaves;
+                for (int x = G.first_node; x < G.first_node + G.n_nodes; ++x) {
+                    const FuseNode &fn = fnodes[x];
+                    L.flops += 8 * (uint64_t)fn.m * fn.n * fn.k;
+                }
+                L.bytes += 8 * (uint64_t)G.n_gather;
+                const NodePlan &rn = p->nodes[G.step];
+                L.bytes += fmt_bytes(rn.out_fmt) * rn.m * rn.n;
+                ++g1;
+            }
+            L.count = (int32_t)(g1 - g0);
+            L.ctas = L.count;
+            if (!rest)
+                for (size_t x = g0; x < g1; ++x)
+                    for (int s2 = 0; s2 < S; ++s2)
+                        if (p->fused[s2] == groups[x]) t_of[n + s2] = (int)sched.size();
+            sched.push_back(L);
+            g0 = g1;
+        }
         for (int st = 1; st <= max_stage; ++st) {
             std::vector<int> tiny, other;
             for (int s : by_stage[st]) {
@@ -279,7 +491,11 @@ tn_status layout_plan(Plan *p) {
         LeafPlan &lp = p->leaves[t];
         const bool tiny_consumer = S > 0 && p->nodes[p->consumer[t]].cls == TN_NODE_TINY;
         lp.in_place = S > 0 && lp.identity && p->fmt[t] == FMT_C64 && !tiny_consumer;
-        if (S == 0) {
+        if (leaf_fused[t]) {
+            // read by its group's CTA straight from the caller's buffer
+            lp.in_place = true;
+            lp.place = {PLACE_LEAF, t, 0};
+        } else if (S == 0) {
             lp.place = {PLACE_OUT, t, 0};
         } else if (lp.in_place) {
             lp.place = {PLACE_LEAF, t, 0};
@@ -291,6 +507,8 @@ tn_status layout_plan(Plan *p) {
     for (int s = 0; s < S; ++s) {
         const NodePlan &nd = p->nodes[s];
         const int ts = t_of[n + s];
+        // inside a fused group only the group's root reaches the workspace
+        if (p->fused[s] >= 0 && p->fuse_groups[p->fused[s]].step != s) continue;
         if (!nd.is_root) {
             if (pinned(nd.out))
                 iv.push_back({nd.m * nd.n * fmt_bytes(nd.out_fmt), -1, run_end, nd.out, 0});
@@ -308,6 +526,7 @@ tn_status layout_plan(Plan *p) {
         LeafPlan &lp = p->leaves[t];
         if (S > 0 && !lp.in_place) lp.place = where[t];
         where[t] = lp.place;
+        if (leaf_fused[t]) continue;
         if (S == 0 || !lp.in_place) {
             PermDesc d = lp.perm;
             d.dst_off = (lp.place.kind == PLACE_OUT) ? -1 : (int64_t)lp.place.off;
@@ -315,6 +534,11 @@ tn_status layout_plan(Plan *p) {
             d.tile = (S == 0) ? untiled : tile[t];
             d.vec4 = d.rank >= 1 && d.sstride[d.rank - 1] == 1 && d.dims[d.rank - 1] % 4 == 0 &&
                      d.size % 4 == 0;
+            d.contig = d.rank == 1 && d.sstride[0] == 1 && d.size % 16 == 0;
+            d.tax = -1;
+            if (d.rank >= 2 && d.sstride[d.rank - 1] != 1 && d.dims[d.rank - 1] >= 8)
+                for (int x = 0; x < d.rank - 1; ++x)
+                    if (d.sstride[x] == 1 && d.dims[x] >= 8) d.tax = x;
             p->perm_table.push_back(d);
             p->perm_leaves.push_back(t);
         }
@@ -330,7 +554,9 @@ tn_status layout_plan(Plan *p) {
         Launch L{};
         L.kind = LAUNCH_PERMUTE;
         L.node = -1;
-        for (int j : jobs) L.bytes += 16 * (uint64_t)p->perm_table[j].size;
+        for (int j : jobs)
+            L.bytes += (8 + fmt_bytes(p->perm_table[j].dst_off < 0 ? (int32_t)FMT_C64 : p->perm_table[j].fmt)) *
+                       (uint64_t)p->perm_table[j].size;
         sched.insert(sched.begin(), L);
     };
     perm_launch(p->perm_all, p->sched);
@@ -347,6 +573,14 @@ tn_status layout_plan(Plan *p) {
         nd.pb = where[nd.b];
         nd.pc = where[nd.out];
         nd.part = where[n + S + s];
+    }
+
+    for (auto &G : p->fuse_groups) {
+        const NodePlan &rn = p->nodes[G.step];
+        G.is_root = rn.is_root ? 1 : 0;
+        G.out_off = rn.pc.kind == PLACE_OUT ? -1 : (int64_t)rn.pc.off;
+        G.out_fmt = rn.out_fmt;
+        G.out_tile = rn.out_tile;
     }
 
     // 5. device tables
@@ -421,8 +655,20 @@ tn_status layout_plan(Plan *p) {
         return TN_ENOTIMPL;
     const uint64_t tiny_start = align_up(ep_start + eps.size() * sizeof(EpTable));
     p->tiny_off = p->table_off + tiny_start;
+    // fused groups: FuseGroup[], FuseNode[], FuseGather[], level starts,
+    // output offsets
+    const uint64_t fg_start = align_up(tiny_start + tiny.size() * sizeof(TinyDesc));
+    const uint64_t fn_start = align_up(fg_start + p->fuse_groups.size() * sizeof(FuseGroup));
+    const uint64_t fl_start = align_up(fn_start + fnodes.size() * sizeof(FuseNode));
+    const uint64_t fv_start = align_up(fl_start + fgather.size() * sizeof(FuseGather));
+    const uint64_t fo_start = align_up(fv_start + flevels.size() * sizeof(int32_t));
+    p->fuse_off = p->table_off + fg_start;
+    p->fuse_node_off = p->table_off + fn_start;
+    p->fuse_gather_off = p->table_off + fl_start;
+    p->fuse_lvl_off = p->table_off + fv_start;
+    p->fuse_offs_off = p->table_off + fo_start;
     // tail-tile counters (zero; every run leaves them zero again)
-    const uint64_t cnt_start = align_up(tiny_start + tiny.size() * sizeof(TinyDesc));
+    const uint64_t cnt_start = align_up(fo_start + foffs.size() * sizeof(int32_t));
     uint64_t cnt = 0;
     for (auto &nd : p->nodes) {
         nd.tail_cnt_off = -1;
@@ -442,6 +688,15 @@ tn_status layout_plan(Plan *p) {
         std::memcpy(p->table_blob.data() + ep_start, eps.data(), eps.size() * sizeof(EpTable));
     if (!tiny.empty())
         std::memcpy(p->table_blob.data() + tiny_start, tiny.data(), tiny.size() * sizeof(TinyDesc));
+    if (!p->fuse_groups.empty()) {
+        std::memcpy(p->table_blob.data() + fg_start, p->fuse_groups.data(),
+                    p->fuse_groups.size() * sizeof(FuseGroup));
+        std::memcpy(p->table_blob.data() + fn_start, fnodes.data(), fnodes.size() * sizeof(FuseNode));
+        std::memcpy(p->table_blob.data() + fl_start, fgather.data(), fgather.size() * sizeof(FuseGather));
+        std::memcpy(p->table_blob.data() + fv_start, flevels.data(), flevels.size() * sizeof(int32_t));
+        std::memcpy(p->table_blob.data() + fo_start, foffs.data(), foffs.size() * sizeof(int32_t));
+    }
+    p->fuse_leaves_host = fleaves;
     p->table_bytes = align_up(p->table_blob.size());
     p->arena_off = p->table_off + p->table_bytes;
     p->ws_bytes = p->arena_off + p->arena_bytes;

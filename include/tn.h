@@ -76,7 +76,8 @@ enum {
     TN_NODE_SIMT = 0,      /* general CUDA-core tiled kernel */
     TN_NODE_DENSE = 1,     /* tcgen05 tensor-core kernel */
     TN_NODE_STREAM = 2,    /* bandwidth-bound kernel (small n or k) */
-    TN_NODE_TINY = 3       /* batched tiny nodes, many per launch */
+    TN_NODE_TINY = 3,      /* batched tiny nodes, many per launch */
+    TN_NODE_FUSED = 4      /* inside a fused leaf subtree (tn_plan_set_fusion) */
 };
 
 enum {
@@ -337,6 +338,58 @@ TN_API tn_status tn_plan_set_replay(tn_plan_t *plan, int32_t enable);
 TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
 
 /*
+ * Promotion chunk of the tensor-core nodes: the number of complex k whose
+ * products the tensor core accumulates in its fp32 TMEM accumulator before
+ * the sum is added (round to nearest) into fp32 registers.  The tensor
+ * core's accumulation rounds toward zero, so every node's sums shrink by a
+ * relative bias that grows with the chunk (measured ~1.3e-6 per node with
+ * 256, ~0.33e-6 with 64), and the nodes' biases add up at the root; shorter
+ * chunks cost throughput (4096^3 node: ~346 TFLOP/s with 256, ~300 with 64).
+ * chunk_k = 0 (the default) picks, per plan, the longest of 256, 128 and 64
+ * whose bias times the number of tensor-core nodes stays within 4e-6 (256 for
+ * plain bf16 operands); otherwise a multiple of 32 in [32, 1024] for every
+ * tensor-core node (CTA pairs use half of it).  Re-plans the layout (like
+ * tn_plan_set_policy): bind the workspace again afterwards.
+ * Errors: TN_EINVAL (NULL plan or a value outside that set).
+ */
+TN_API tn_status tn_plan_set_promotion_chunk(tn_plan_t *plan, int32_t chunk_k);
+
+/*
+ * Tensor-core nodes on CTA pairs (tcgen05 cta_group::2): with `enable` = 1,
+ * a tensor-core node whose longer side has at least 256 entries runs on
+ * clusters of two CTAs, each pair computing tiles of 256 x 128 complex
+ * outputs with MMAs of M = 256 (each SM holds half of the tile's A rows and
+ * half of its B rows, so it reads half as much of B per MMA) and the real
+ * and imaginary parts accumulated directly (negated-A MMAs for -Ai Bi) in
+ * double-buffered TMEM.  Measured on a GB300 it is not faster than the
+ * single-CTA kernel at equal accuracy (4096^3 node, split tf32: 272 against
+ * 300 TFLOP/s), so the default is 0.  Re-plans the layout (like
+ * tn_plan_set_policy): bind the workspace again afterwards.
+ * Errors: TN_EINVAL (NULL plan).
+ */
+TN_API tn_status tn_plan_set_cta_pairs(tn_plan_t *plan, int32_t enable);
+
+/*
+ * Fused leaf subtrees ("leaf-gate absorption").  Lifetime ordering leaves
+ * the leaves as the only tensors to reorder ("Crossing the single-GPU memory
+ * wall", section 1.3), and near the leaves a tree is mostly chains of tiny
+ * steps: gates absorbed into wires, small tensors meeting.  With `enable` =
+ * 1 (the default) every maximal subtree whose leaves and intermediates all
+ * have at most 2048 entries (a subtree's tensors together at most 8192 =
+ * 64 KiB, leaves of at most 12 axes after merging) runs as one CTA of one
+ * launch at the start of each slice: the CTA reads its leaves straight from
+ * the caller's buffers (their permutation into lifetime order done on the
+ * load), computes the subtree's steps in shared memory and writes only the
+ * subtree's root.  Those leaves get no permutation job, the inner steps no
+ * launch and no workspace (tn_plan_node_class reports TN_NODE_FUSED; their
+ * tensors cannot be read with tn_plan_tensor_gather).  Only with
+ * TN_POLICY_AUTO.  Results equal the unfused plan's up to fp32 rounding
+ * order.  Re-plans the layout (like tn_plan_set_policy): bind the workspace
+ * again afterwards.  Errors: TN_EINVAL (NULL plan).
+ */
+TN_API tn_status tn_plan_set_fusion(tn_plan_t *plan, int32_t enable);
+
+/*
  * Slice-invariant hoisting ("Crossing the single-GPU memory wall", section
  * 1.1: slicing repeats the whole contraction once per slice; a node none of
  * whose leaves carries a sliced mode computes the same tensor in every
@@ -372,7 +425,8 @@ enum {
     TN_KERNEL_TINY = 5,         /* batched tiny-node kernel */
     TN_KERNEL_REDUCE = 6,       /* ordered sum of split-K partials */
     TN_KERNEL_DENSE_TF32X3_3P = 7, /* tcgen05 node kernel, split tf32, three real products */
-    TN_KERNEL_DENSE_BF16X3 = 8     /* tcgen05 node kernel, split bf16 */
+    TN_KERNEL_DENSE_BF16X3 = 8,    /* tcgen05 node kernel, split bf16 */
+    TN_KERNEL_FUSED = 9            /* fused leaf subtrees */
 };
 
 /* One kernel launch of a profiled tn_execute.  flops = 8 m n k of the

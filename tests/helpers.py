@@ -10,11 +10,16 @@ TOL_BF16 = 2e-2    # bf16 tensor-core operands
 TOL_BF16X3 = 2e-4
 
 
-def run_gpu(net, tree, slices=(), precision="tf32x3", policy=0, out_dtype=None, repeat=1):
+def run_gpu(net, tree, slices=(), precision="tf32x3", policy=0, out_dtype=None, repeat=1,
+            fuse=True, pairs=False):
     import torch
     import exact_tensor_network_gb300 as tn
     dev = torch.device("cuda:0")
     plan = tn.Plan.from_network(net, tree, slices, precision, policy)
+    if not fuse:
+        plan.set_fusion(False)
+    if pairs:
+        plan.set_cta_pairs(True)
     leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
     out = torch.full(plan.out_shape, complex(7.0, -3.0), dtype=torch.complex64, device=dev)
     for _ in range(repeat):

@@ -347,3 +347,34 @@ def test_dense_narrow_tiles(m, n, k, precision, policy, tol):
     assert plan.node_class(0) == tn.TN_NODE_DENSE
     got, _ = run_gpu(net, [(0, 1)], precision=precision, policy=policy, repeat=2)
     assert_close(got, _ref(net, [(0, 1)]), tol, f"narrow {m}x{n}x{k} {precision}")
+
+
+# ---- CTA pairs (tcgen05 cta_group::2, opt-in) --------------------------------
+
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16", TOL_BF16),
+                                           ("bf16x3", TOL_BF16X3)])
+@pytest.mark.parametrize("m,n,k", [(256, 128, 64), (512, 384, 512), (300, 200, 136), (1000, 77 + 64, 48),
+                                   (129, 700, 1000), (2048, 256, 4096), (640, 512, 2064)])
+def test_cta_pair_nodes(precision, tol, m, n, k):
+    """Single nodes on CTA pairs: full and ragged 256-row tiles, the swap
+    (the longer side becomes the rows), split-K, K-tiled operands."""
+    net = node_network(m, n, k, 3 * m + n + k)
+    got, plan = run_gpu(net, [(0, 1)], precision=precision, policy=NT, pairs=True)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"pair node {m}x{n}x{k} {precision}")
+
+
+def test_cta_pairs_network_and_slices():
+    """A chain of tensor-core nodes (planar operands written by a pair's
+    epilogue, read by the next pair) and a sliced root that accumulates."""
+    net, tree, _ = configs.random_60()
+    a, _ = run_gpu(net, tree, pairs=True)
+    assert_close(a, _ref(net, tree), TOL_C64, "random_60 on CTA pairs")
+    rng = np.random.default_rng(8)
+    ext = [512, 256, 384, 4]                   # i x j z (z sliced)
+    tensors = [[0, 1, 3], [2, 1, 3]]
+    data = [_rand(rng, [ext[x] for x in t]) for t in tensors]
+    net = Network(tensors, ext, [0, 2], data)
+    got, plan = run_gpu(net, [(0, 1)], [3], policy=NT, pairs=True)
+    assert plan.num_slices == 4 and plan.node_class(0) == tn.TN_NODE_DENSE
+    assert_close(got, _ref(net, [(0, 1)], [3]), TOL_C64, "sliced pair node")

@@ -85,7 +85,9 @@ def _node_steps(plan, n_steps, extra=3):
     """Every tensor-core step, plus the largest `extra` steps (by m n k) of
     the other classes."""
     dense = [s for s in range(n_steps) if plan.node_class(s) == tn.TN_NODE_DENSE]
-    other = sorted((s for s in range(n_steps) if plan.node_class(s) != tn.TN_NODE_DENSE),
+    # steps inside fused leaf subtrees keep their tensors in shared memory
+    other = sorted((s for s in range(n_steps)
+                    if plan.node_class(s) not in (tn.TN_NODE_DENSE, tn.TN_NODE_FUSED)),
                    key=lambda s: -int(np.prod(plan.node_mnk(s))))
     return dense + other[:extra]
 
@@ -130,8 +132,16 @@ def test_gathered_nodes_match_oracle_product():
     plan = tn.Plan.from_network(net, tree)
     leaves = _leaves(net, dev)
     out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
+    fused = 0
     for s in range(len(tree)):
         a, b, c, m, n, k, offm, offn = node_layout(plan, s, net.extents)
+        if plan.node_class(s) == tn.TN_NODE_FUSED:
+            # its tensors live in a fused group's shared memory only
+            fused += 1
+            plan.execute_prefix(leaves, out, s)
+            with pytest.raises(tn.TNError):
+                plan.gather(a, torch.zeros(1, dtype=torch.int64, device=dev))
+            continue
         if m * n * k > (1 << 26):
             continue
         plan.execute_prefix(leaves, out, s)
@@ -143,6 +153,7 @@ def test_gathered_nodes_match_oracle_product():
         plan.check()
         ref = A.astype(np.complex128) @ B.astype(np.complex128).T
         assert_close(C.astype(np.complex128), ref, TOL_C64, f"step {s} ({m}x{n}x{k})")
+    assert fused > 0
     plan.execute(leaves, out)
     torch.cuda.synchronize(dev)
     plan.check()
@@ -155,6 +166,7 @@ def test_gather_rejects_other_tensors():
     net, tree, _ = configs.circuit_3x3_d4()
     dev = torch.device("cuda:0")
     plan = tn.Plan.from_network(net, tree)
+    plan.set_fusion(False)                 # every step in the workspace
     leaves = _leaves(net, dev)
     out = torch.empty(plan.out_shape, dtype=torch.complex64, device=dev)
     idx = torch.zeros(1, dtype=torch.int64, device=dev)

@@ -139,6 +139,7 @@ def test_hoisting_matches_plain_slice_loop(case):
     launches = {}
     for hoist in (True, False):
         plan = tn.Plan.from_network(net, tree, sl)
+        plan.set_fusion(False)   # fused leaf subtrees would hold every launch here
         plan.set_hoisting(hoist)
         assert plan.num_slices > 1
         out = torch.full(plan.out_shape, complex(7.0, -3.0), dtype=torch.complex64, device=dev)
@@ -254,7 +255,7 @@ def test_tiny_batching_matches_unbatched(name):
     import exact_tensor_network_gb300 as tn
     net, tree, _ = configs.by_name(name)
     ref = _ref(net, tree)
-    a, pa = run_gpu(net, tree, policy=tn.TN_POLICY_AUTO)
+    a, pa = run_gpu(net, tree, policy=tn.TN_POLICY_AUTO, fuse=False)
     b, pb = run_gpu(net, tree, policy=tn.TN_POLICY_NO_TINY)
     assert pa.launches < pb.launches
     assert_close(a, ref, what=f"{name} batched tiny nodes")
@@ -290,7 +291,7 @@ def test_tiny_stage_over_one_launch():
     nodes each)."""
     import exact_tensor_network_gb300 as tn
     net, tree = _unitary_chain(300, 5)
-    got, plan = run_gpu(net, tree)
+    got, plan = run_gpu(net, tree, fuse=False)
     # 2 leaf launches (600 leaves, 512 per launch) + 10 tiny stages, the
     # first of them split in two
     assert plan.launches == 13
@@ -461,3 +462,33 @@ def test_reduced_precision_errors_reported():
             line.append(f"{prec} {r:.2e}")
             assert np.isfinite(r) and r < 0.5, f"{name} {prec}: {r}"
         print(f"precision errors {name}: " + ", ".join(line))
+
+
+# ---- leaf permutation paths: conversions and true transposes ----------------
+
+@pytest.mark.parametrize("perm,shape,policy", [
+    ((1, 0), (96, 200), 2),         # a transpose into a CUDA-core operand
+    ((1, 0), (300, 256), 2),
+    ((2, 0, 1), (40, 64, 48), 2),   # contiguous axis in the middle of the destination
+    ((1, 0), (256, 2048), 0),       # a transpose into a K-tiled tensor-core operand
+    ((0, 1), (4096, 2048), 0),      # a pure conversion (K-tiled split tf32)
+    ((0, 1), (256, 1000), 0),       # a pure conversion, untiled, ragged k
+])
+def test_leaf_permutation_paths(perm, shape, policy):
+    """Leaf A[i, x] (possibly several i modes) stored in a permuted order,
+    contracted with B[j, x]: the leaf permutation moves it into lifetime
+    order (and the tensor-core operand format) through the shared-memory
+    transpose, the contiguous conversion or the general path."""
+    rng = np.random.default_rng(sum(shape))
+    modes_a = list(range(len(shape)))          # A's modes in lifetime order: [M..., x]
+    x = len(shape) - 1
+    ext = list(shape) + [64]                    # last extra mode: j (B's kept mode)
+    j = len(shape)
+    stored = [modes_a[p] for p in perm]         # user order of A
+    a = (rng.standard_normal([ext[m] for m in stored]) +
+         1j * rng.standard_normal([ext[m] for m in stored])).astype(np.complex64)
+    b = (rng.standard_normal((ext[j], ext[x])) + 1j * rng.standard_normal((ext[j], ext[x]))).astype(np.complex64)
+    open_modes = modes_a[:-1] + [j]
+    net = Network([stored, [j, x]], ext, open_modes, [a, b], f"perm_{perm}_{shape}")
+    got, plan = run_gpu(net, [(0, 1)], policy=policy)
+    assert_close(got, _ref(net, [(0, 1)]), what=f"leaf {perm} {shape}")

@@ -142,6 +142,7 @@ def test_hoisting_launch_counts():
     tree = greedy_tree(net, 0)
     sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
     p = tn.Plan.from_network(net, tree, sl)
+    p.set_fusion(False)   # fused leaf subtrees would hold every launch here
     ns = p.num_slices
     assert ns > 1
     on = p.launches
@@ -173,6 +174,7 @@ def test_hoisting_workspace_and_replanning():
     tree = greedy_tree(net, 0)
     sl = choose_slices(net, tree, max(1, largest_intermediate(net, tree) // 16))[:4]
     p = tn.Plan.from_network(net, tree, sl)
+    p.set_fusion(False)   # fused leaf subtrees would hold every launch here
     on_ws, on_l = p.workspace_bytes, p.launches
     p.set_hoisting(False)
     assert p.workspace_bytes <= on_ws and p.launches > on_l
@@ -207,3 +209,53 @@ def test_binding_checks_buffer_sizes():
     # device buffers are required where the call runs on the GPU
     with pytest.raises(ValueError, match="CUDA"):
         tn._check_buffers(plan, leaves, out, True, "execute")
+
+
+def test_fused_leaf_subtrees_plan():
+    """Fused leaf subtrees: the 3x3 circuit (every tensor small) becomes one
+    group and one launch; the random network keeps its large steps on their
+    kernels; other policies and fusion off leave no fused step."""
+    net, _ = grid_circuit_network(3, 3, 4, 0)
+    tree = greedy_tree(net, 0)
+    p = tn.Plan.from_network(net, tree)
+    assert all(p.node_class(s) == tn.TN_NODE_FUSED for s in range(len(tree)))
+    assert p.launches == 1
+    p.set_fusion(False)
+    assert all(p.node_class(s) == tn.TN_NODE_TINY for s in range(len(tree)))
+    assert p.launches > 10
+    net = random_network(60, 1, with_data=False)
+    tree = greedy_tree(net, 0)
+    p = tn.Plan.from_network(net, tree)
+    cls = [p.node_class(s) for s in range(len(tree))]
+    assert tn.TN_NODE_FUSED in cls and tn.TN_NODE_DENSE in cls
+    p.set_fusion(False)
+    assert tn.TN_NODE_FUSED not in [p.node_class(s) for s in range(len(tree))]
+    p.set_fusion(True)
+    p.set_policy(tn.TN_POLICY_NO_TINY)
+    assert tn.TN_NODE_FUSED not in [p.node_class(s) for s in range(len(tree))]
+    # the leaves' and steps' integer plan data do not change with fusion
+    p2 = tn.Plan.from_network(net, tree)
+    p2.set_fusion(False)
+    p3 = tn.Plan.from_network(net, tree)
+    for s in range(len(tree)):
+        assert p2.node_mnk(s) == p3.node_mnk(s)
+    for t in range(net.n_tensors + len(tree)):
+        assert p2.mode_order(t) == p3.mode_order(t)
+
+
+def test_promotion_chunk_and_pairs_settings():
+    """The promotion chunk accepts 0 (per plan) or multiples of 32 up to
+    1024 and rejects the rest; CTA pairs and the chunk only re-plan."""
+    net = random_network(60, 1, with_data=False)
+    tree = greedy_tree(net, 0)
+    p = tn.Plan.from_network(net, tree)
+    ref = [p.node_mnk(s) for s in range(len(tree))]
+    for c in (0, 32, 64, 256, 1024):
+        p.set_promotion_chunk(c)
+    for bad in (-1, 16, 48, 2048):
+        with pytest.raises(tn.TNError) as e:
+            p.set_promotion_chunk(bad)
+        assert e.value.status == tn.TN_EINVAL
+    p.set_cta_pairs(True)
+    p.set_cta_pairs(False)
+    assert [p.node_mnk(s) for s in range(len(tree))] == ref
