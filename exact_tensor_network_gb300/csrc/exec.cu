@@ -599,6 +599,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 fl->gather = reinterpret_cast<const FuseGather *>(ws + p->fuse_gather_off);
                 fl->levels = reinterpret_cast<const int32_t *>(ws + p->fuse_lvl_off);
                 fl->offs = reinterpret_cast<const int32_t *>(ws + p->fuse_offs_off);
+                fl->chunks = reinterpret_cast<const int32_t *>(ws + p->fuse_chunk_off);
                 fl->arena = arena;
                 fl->out = out;
                 int nsrc = 0, smem = 0;

@@ -24,7 +24,7 @@ namespace tn {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 
 __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__ FuseLaunch a) {
     extern __shared__ float2 sm[];
@@ -40,17 +40,22 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
     __syncthreads();
     const FuseGroup g = gs;
     pdl_wait();
-    // descriptors after the tensors: steps, level starts, output offsets
+    // descriptors after the tensors: steps, level starts (steps, then warp
+    // chunks), output offsets, the step of every warp chunk
     FuseNode *nodes = reinterpret_cast<FuseNode *>(sm + g.smem);
     int32_t *levels = reinterpret_cast<int32_t *>(nodes + g.n_nodes);
-    int32_t *offs = levels + g.n_levels + 1;
+    int32_t *lchunk = levels + g.n_levels + 1;
+    int32_t *offs = lchunk + g.n_levels + 1;
+    int32_t *cnode = offs + g.n_off;
     {
         const int32_t *src = reinterpret_cast<const int32_t *>(a.nodes + g.first_node);
         int32_t *dst = reinterpret_cast<int32_t *>(nodes);
         const int words = g.n_nodes * (int)(sizeof(FuseNode) / 4);
         for (int w = threadIdx.x; w < words; w += kThreads) dst[w] = src[w];
-        for (int w = threadIdx.x; w <= g.n_levels; w += kThreads) levels[w] = a.levels[g.first_level + w];
+        for (int w = threadIdx.x; w < 2 * (g.n_levels + 1); w += kThreads)
+            levels[w] = a.levels[g.first_level + w];
         for (int w = threadIdx.x; w < g.n_off; w += kThreads) offs[w] = a.offs[g.first_off + w];
+        for (int w = threadIdx.x; w < g.n_chunks; w += kThreads) cnode[w] = a.chunks[g.first_chunk + w];
     }
     // leaves: slot e <- the caller's leaf at its source offset (these loads
     // overlap the descriptor copies above)
@@ -64,15 +69,12 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
     const int accumulate = g.is_root ? a.accumulate_root : 0;
     const int lane = threadIdx.x & 31;
     for (int lv = 0; lv < g.n_levels; ++lv) {
-        const int n0 = levels[lv], n1 = levels[lv + 1];
-        const FuseNode &last = nodes[n1 - 1];
-        const int total = last.obase + (last.m * last.n * last.lanes + 31) / 32 * 32;
+        const int c0 = lchunk[lv], total = (lchunk[lv + 1] - c0) * 32;
         // warp by warp over the level's items (a step's items start at a
-        // multiple of 32, so a warp's lanes all belong to one step)
+        // multiple of 32, so a warp's lanes all belong to one step, read from
+        // the chunk table)
         for (int base = threadIdx.x - lane; base < total; base += kThreads) {
-            int s = n0;
-            while (s + 1 < n1 && nodes[s + 1].obase <= base) ++s;
-            const FuseNode &nd = nodes[s];
+            const FuseNode &nd = nodes[cnode[c0 + (base >> 5)]];
             const int L = nd.lanes;
             const int item = base + lane - nd.obase;
             const int o = item / L, l = item - o * L;
@@ -83,8 +85,16 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
                 i = o / nd.n;
                 j = o - i * nd.n;
                 const float2 *ar = sm + nd.a + i * nd.k, *br = sm + nd.b + j * nd.k;
-#pragma unroll 4
-                for (int kk = l; kk < nd.k; kk += L) cfma(acc, ar[kk], br[kk]);
+                // two independent chains of multiply-adds
+                float2 acc1 = make_float2(0.f, 0.f);
+                int kk = l;
+                for (; kk + L < nd.k; kk += 2 * L) {
+                    cfma(acc, ar[kk], br[kk]);
+                    cfma(acc1, ar[kk + L], br[kk + L]);
+                }
+                if (kk < nd.k) cfma(acc, ar[kk], br[kk]);
+                acc.x += acc1.x;
+                acc.y += acc1.y;
             }
             for (int off = L >> 1; off > 0; off >>= 1) {
                 acc.x += __shfl_down_sync(0xffffffffu, acc.x, off, L);

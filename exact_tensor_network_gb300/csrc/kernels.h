@@ -175,6 +175,7 @@ struct FuseLaunch {
     const FuseGather *gather;
     const int32_t *levels;
     const int32_t *offs;
+    const int32_t *chunks;
     char *arena;
     float2 *out;
     int32_t group[kFuseBatch];

@@ -292,7 +292,7 @@ struct Launch {
 // kFuseMaxDescBytes of step descriptors and output offsets.
 constexpr int64_t kFuseMaxTensor = 2048;
 constexpr int64_t kFuseSmemEntries = 8192;   // 64 KiB of complex64
-constexpr int64_t kFuseMaxMacs = 1 << 17;    // complex multiply-adds of a group (one CTA)
+constexpr int64_t kFuseMaxMacs = 1 << 15;    // complex multiply-adds of a group (one CTA)
 constexpr int64_t kFuseMaxDescBytes = 24 * 1024;
 constexpr int kFuseBatch = 256;              // groups per launch
 constexpr int kFuseSrc = 2048;               // leaf pointers per launch
@@ -319,7 +319,9 @@ struct FuseGroup {
     int32_t first_leaf, n_leaves;    // host leaf list (launch pointers)
     int32_t first_gather, n_gather;  // leaf entries (= shared-memory slots 0 .. n_gather-1)
     int32_t first_node, n_nodes;
-    int32_t first_level, n_levels;   // level l: nodes [lvl[l], lvl[l + 1]) of the node list
+    int32_t first_level, n_levels;   // level l: nodes [lvl[l], lvl[l + 1]) of the node list;
+                                     // then lvl[n_levels + 1 + l]: its first warp chunk
+    int32_t first_chunk, n_chunks;   // warp chunk (32 thread items) -> its step
     int32_t first_off, n_off;        // output offset table
     int32_t smem;                    // shared-memory entries of the group's tensors
     int32_t smem_bytes;              // tensors + descriptors (nodes, levels, offsets)
@@ -425,6 +427,7 @@ struct Plan {
     std::vector<int32_t> fuse_all, fuse_rest;   // groups each program runs
     uint64_t fuse_off = 0;                      // workspace offsets of FuseGroup[], FuseNode[],
     uint64_t fuse_node_off = 0, fuse_gather_off = 0, fuse_lvl_off = 0, fuse_offs_off = 0;   // FuseGather[], levels, offsets
+    uint64_t fuse_chunk_off = 0;                // chunk -> step tables
     int32_t fuse_smem = 0;                      // largest group's shared memory (bytes)
     std::vector<FuseLeaf> fuse_leaves_host;     // host copy of FuseLeaf[] (launch parameters)
     std::vector<int32_t> fmt;                   // per SSA id (Fmt)

@@ -174,13 +174,14 @@ bool make_ep_table(const NodePlan &nd, EpTable *t) {
 // kFuseMaxMacs and its descriptors kFuseMaxDescBytes.  A group is a maximal
 // such subtree (at least one step); its root is a step whose consumer cannot
 // join it.
-int64_t fuse_desc_bytes(int64_t nodes, int64_t offsets, int64_t levels) {
-    return nodes * (int64_t)sizeof(FuseNode) + 4 * (offsets + levels + 1);
+int64_t fuse_desc_bytes(int64_t nodes, int64_t offsets, int64_t levels, int64_t chunks) {
+    return nodes * (int64_t)sizeof(FuseNode) + 4 * (offsets + 2 * (levels + 1) + chunks);
 }
 
 void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather> &fgather,
                  std::vector<int32_t> &flevels, std::vector<int32_t> &foffs,
-                 std::vector<FuseLeaf> &fleaves, std::vector<uint8_t> &leaf_fused) {
+                 std::vector<int32_t> &fchunks, std::vector<FuseLeaf> &fleaves,
+                 std::vector<uint8_t> &leaf_fused) {
     const int n = p->n_tensors, S = (int)p->nodes.size();
     std::vector<uint8_t> ok(n + S, 0);
     std::vector<int64_t> cost(n + S, 0), macs(n + S, 0), nsteps(n + S, 0), noffs(n + S, 0);
@@ -199,7 +200,8 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
         ok[nd.out] = nd.cls == TN_NODE_TINY && ok[nd.a] && ok[nd.b] && mn <= kFuseMaxTensor &&
                      (int64_t)nd.k <= kFuseMaxTensor && cost[nd.out] <= kFuseSmemEntries &&
                      macs[nd.out] <= kFuseMaxMacs &&
-                     fuse_desc_bytes(nsteps[nd.out], noffs[nd.out], nsteps[nd.out]) <= kFuseMaxDescBytes;
+                     fuse_desc_bytes(nsteps[nd.out], noffs[nd.out], nsteps[nd.out],
+                                     (macs[nd.out] + 31) / 32 + 32 * nsteps[nd.out]) <= kFuseMaxDescBytes;
     }
     for (int r = 0; r < S; ++r) {
         const NodePlan &rn = p->nodes[r];
@@ -270,8 +272,11 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
         G.first_level = (int32_t)flevels.size();
         G.n_levels = nlev;
         G.first_off = (int32_t)foffs.size();
+        G.first_chunk = (int32_t)fchunks.size();
+        std::vector<int32_t> lchunk;
         for (int lv = 1; lv <= nlev; ++lv) {
             flevels.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
+            lchunk.push_back((int32_t)(fchunks.size() - (size_t)G.first_chunk));
             int32_t obase = 0;
             for (int s : steps) {
                 const NodePlan &nd = p->nodes[s];
@@ -290,6 +295,9 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
                 while (f.lanes < 32 && f.lanes * 4 < f.k) f.lanes *= 2;
                 f.obase = obase;
                 obase += (f.m * f.n * f.lanes + 31) / 32 * 32;
+                // the step of every warp chunk of this level
+                for (int32_t c = f.obase; c < obase; c += 32)
+                    fchunks.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
                 f.off = (int32_t)(foffs.size() - (size_t)G.first_off);
                 for (uint64_t i = 0; i < nd.m; ++i) foffs.push_back((int32_t)sep_offset_host(nd.lm, (int64_t)i));
                 for (uint64_t j = 0; j < nd.n; ++j) foffs.push_back((int32_t)sep_offset_host(nd.ln, (int64_t)j));
@@ -297,8 +305,12 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
             }
         }
         flevels.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
+        lchunk.push_back((int32_t)(fchunks.size() - (size_t)G.first_chunk));
+        flevels.insert(flevels.end(), lchunk.begin(), lchunk.end());
         G.n_off = (int32_t)(foffs.size() - (size_t)G.first_off);
-        G.smem_bytes = (int32_t)(8 * (int64_t)G.smem + fuse_desc_bytes(G.n_nodes, G.n_off, G.n_levels));
+        G.n_chunks = (int32_t)(fchunks.size() - (size_t)G.first_chunk);
+        G.smem_bytes = (int32_t)(8 * (int64_t)G.smem +
+                                 fuse_desc_bytes(G.n_nodes, G.n_off, G.n_levels, G.n_chunks));
         for (int s : steps) p->fused[s] = gi;
         p->fuse_smem = std::max(p->fuse_smem, G.smem_bytes);
         p->fuse_groups.push_back(G);
@@ -376,13 +388,13 @@ tn_status layout_plan(Plan *p) {
     std::vector<FuseNode> fnodes;
     std::vector<FuseGather> fgather;
     std::vector<FuseLeaf> fleaves;
-    std::vector<int32_t> flevels, foffs;
+    std::vector<int32_t> flevels, foffs, fchunks;
     std::vector<uint8_t> leaf_fused(n, 0);
     p->fused.assign(S, -1);
     p->fuse_groups.clear();
     p->fuse_smem = 0;
     if (p->fuse && p->policy == TN_POLICY_AUTO && S > 0)
-        form_groups(p, fnodes, fgather, flevels, foffs, fleaves, leaf_fused);
+        form_groups(p, fnodes, fgather, flevels, foffs, fchunks, fleaves, leaf_fused);
 
     // 3. schedule (group roots are ready after the fused launch at the start)
     std::vector<int> stage(n + S, 0);
@@ -535,8 +547,11 @@ tn_status layout_plan(Plan *p) {
             d.vec4 = d.rank >= 1 && d.sstride[d.rank - 1] == 1 && d.dims[d.rank - 1] % 4 == 0 &&
                      d.size % 4 == 0;
             d.contig = d.rank == 1 && d.sstride[0] == 1 && d.size % 16 == 0;
+            // (small leaves stay on the general path: their transposes are a
+            // few loads of latency, not bandwidth)
             d.tax = -1;
-            if (d.rank >= 2 && d.sstride[d.rank - 1] != 1 && d.dims[d.rank - 1] >= 8)
+            if (d.rank >= 2 && d.size >= (1 << 16) && d.sstride[d.rank - 1] != 1 &&
+                d.dims[d.rank - 1] >= 8)
                 for (int x = 0; x < d.rank - 1; ++x)
                     if (d.sstride[x] == 1 && d.dims[x] >= 8) d.tax = x;
             p->perm_table.push_back(d);
@@ -662,13 +677,15 @@ tn_status layout_plan(Plan *p) {
     const uint64_t fl_start = align_up(fn_start + fnodes.size() * sizeof(FuseNode));
     const uint64_t fv_start = align_up(fl_start + fgather.size() * sizeof(FuseGather));
     const uint64_t fo_start = align_up(fv_start + flevels.size() * sizeof(int32_t));
+    const uint64_t fc_start = align_up(fo_start + foffs.size() * sizeof(int32_t));
+    p->fuse_chunk_off = p->table_off + fc_start;
     p->fuse_off = p->table_off + fg_start;
     p->fuse_node_off = p->table_off + fn_start;
     p->fuse_gather_off = p->table_off + fl_start;
     p->fuse_lvl_off = p->table_off + fv_start;
     p->fuse_offs_off = p->table_off + fo_start;
     // tail-tile counters (zero; every run leaves them zero again)
-    const uint64_t cnt_start = align_up(fo_start + foffs.size() * sizeof(int32_t));
+    const uint64_t cnt_start = align_up(fc_start + fchunks.size() * sizeof(int32_t));
     uint64_t cnt = 0;
     for (auto &nd : p->nodes) {
         nd.tail_cnt_off = -1;
@@ -695,6 +712,7 @@ tn_status layout_plan(Plan *p) {
         std::memcpy(p->table_blob.data() + fl_start, fgather.data(), fgather.size() * sizeof(FuseGather));
         std::memcpy(p->table_blob.data() + fv_start, flevels.data(), flevels.size() * sizeof(int32_t));
         std::memcpy(p->table_blob.data() + fo_start, foffs.data(), foffs.size() * sizeof(int32_t));
+        std::memcpy(p->table_blob.data() + fc_start, fchunks.data(), fchunks.size() * sizeof(int32_t));
     }
     p->fuse_leaves_host = fleaves;
     p->table_bytes = align_up(p->table_blob.size());
