@@ -409,6 +409,33 @@ __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t n
     nt = r / gm;
 }
 
+// The products of one stage into one accumulator of the single-CTA kernel:
+// D1 (IM = false) = Ar [Br; Bi] or D2 (IM = true) = Ai [Br; Bi]; split
+// precisions form hi*lo + lo*hi + hi*hi.  Fully unrolled with compile-time
+// plane offsets: one thread issues every MMA, and its instruction count
+// per MMA bounds how fast it can keep the tensor core fed.
+template <int MODE, bool IM>
+__device__ __forceinline__ void stage_products(uint32_t d, uint32_t base, uint32_t bbase,
+                                               uint32_t b_plane, bool fresh, uint32_t idesc) {
+    using C = Cfg<MODE>;
+    const uint32_t ah = base + (IM ? PLANE_TILE : 0);
+#pragma unroll
+    for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+        const uint32_t off = kk * 32;   // 32 bytes of K per instruction
+        const uint32_t acc = (fresh && kk == 0) ? 0u : 1u;
+        if constexpr (C::BF16) {
+            mma<MODE>(d, sdesc(ah + off), sdesc(bbase + off), acc, idesc);
+        } else {
+            const uint32_t al = base + (IM ? 3 : 2) * PLANE_TILE;
+            const uint64_t bh = sdesc(bbase + off);
+            const uint64_t bl = sdesc(bbase + 2 * b_plane + off);
+            mma<MODE>(d, sdesc(al + off), bh, acc, idesc);
+            mma<MODE>(d, sdesc(ah + off), bl, 1, idesc);
+            mma<MODE>(d, sdesc(ah + off), bh, 1, idesc);
+        }
+    }
+}
+
 // PAIR: the kernel runs as clusters of two CTAs (cta_group::2).  A pair
 // owns output tiles of 256 rows x 128 columns: CTA r loads rows
 // 128 r .. 128 r + 127 of the tile's A and columns 64 r .. 64 r + 63 of its
@@ -652,7 +679,91 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             }
             mma_commit_pair(drain);
             drain_wait(drain, 0);
-        } else if (!PAIR && warp == 1 && lane == 0) {
+        } else if (!PAIR && !C::THREE && warp == 1 && lane == 0) {
+            // ---- MMA issuer (single CTA) ----
+            // D1 = Ar [Br; Bi] and D2 = Ai [Br; Bi], 2 bn columns each, are
+            // promoted in chunks of CS stages whose boundaries lie one stage
+            // apart: D2's first chunk is the tile's first stage alone.  At the
+            // first stage of a D1 chunk the D2 products go first, so the drain
+            // reads the finished D1 chunk while the tensor core runs two
+            // stages' worth of D2 products, and likewise for D2 (one stage
+            // later, behind two stages' D1 products).  The drain therefore
+            // sees the chunks in the order D2, D1, D2, D1, ...
+            const uint32_t d1 = tmem, d2 = tmem + 2 * bn;
+            const uint32_t idesc = C::idesc((uint32_t)(2 * bn));
+            uint32_t stage = 0, phase = 0, ph1 = 0, ph2 = 0;
+            bool ok = true;
+            for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const int kb0 = it.kb0, kb1 = it.kb1;
+                for (int kb = kb0; kb < kb1 && ok; ++kb) {
+                    const int r = kb - kb0;
+                    const bool last = kb == kb1 - 1;
+                    const bool d1_start = r % CS == 0, d1_end = r % CS == CS - 1 || last;
+                    const bool d2_start = r == 0 || CS == 1 || r % CS == 1;
+                    const bool d2_end = r % CS == 0 || last;
+                    if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t base = smem_u32(smem + stage * stage_bytes);
+                    const uint32_t bbase = base + C::PLANES * PLANE_TILE;
+                    // the first stage of a D1 chunk issues D2 first; the
+                    // others D1 first
+                    if (d1_start) {
+                        if (d2_start) {
+                            if (!wait_bounded(tmem_empty2, ph2 ^ 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
+                        }
+                        stage_products<MODE, true>(d2, base, bbase, b_plane, d2_start, idesc);
+                        if (d2_end) {
+                            mma_commit(tmem_full2);   // the drain may read D2
+                            ph2 ^= 1;
+                        }
+                        if (!wait_bounded(tmem_empty, ph1 ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        stage_products<MODE, false>(d1, base, bbase, b_plane, true, idesc);
+                        if (d1_end) {
+                            mma_commit(tmem_full);    // the drain may read D1
+                            ph1 ^= 1;
+                        }
+                    } else {
+                        stage_products<MODE, false>(d1, base, bbase, b_plane, false, idesc);
+                        if (d1_end) {
+                            mma_commit(tmem_full);
+                            ph1 ^= 1;
+                        }
+                        if (d2_start) {
+                            if (!wait_bounded(tmem_empty2, ph2 ^ 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            fence_after();
+                        }
+                        stage_products<MODE, true>(d2, base, bbase, b_plane, d2_start, idesc);
+                        if (d2_end) {
+                            mma_commit(tmem_full2);
+                            ph2 ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(empty0 + 8 * stage);
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            mma_commit(drain);
+            drain_wait(drain, 0);
+        } else if (!PAIR && C::THREE && warp == 1 && lane == 0) {
             // ---- MMA issuer ----
             // four products: D1 = Ar [Br; Bi], D2 = Ai [Br; Bi], 2 bn columns each
             const uint32_t d1 = tmem, d2 = tmem + 2 * bn;
@@ -802,7 +913,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         const bool quads =
             ep_s && ep_s->vec && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
         const PlanarTile ep_tile = pretiled ? PlanarTile{0, 0, -1, 0} : a.out_tile;
-        uint32_t tphase = 0, pcnt = 0;
+        uint32_t tphase = 0, pcnt = 0, q1 = 0, q2 = 0;
         bool ok = true;
         for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
             const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
@@ -850,7 +961,63 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     if (lane == 0) mbar_arrive_cluster(map_to_rank(b ? tmem_empty2 : tmem_empty, 0));
                 }
             }
-            for (int ch = 0; !PAIR && ch < nch; ++ch) {
+            if constexpr (!PAIR && !C::THREE) {
+                // the chunks of D1 and D2 alternate, D2 first (see the MMA
+                // issuer): n1 of D1 and n2 of D2
+                const int st = kb1 - kb0;
+                const int n1 = (st + CS - 1) / CS;
+                const int n2 = st <= 1 ? 1 : 1 + (st - 1 + CS - 1) / CS;
+                for (int e = 0; e < n1 + n2; ++e) {
+                    const bool im = (e & 1) == 0;
+                    int okv = 0;
+                    if (lane == 0)
+                        okv = wait_bounded(im ? tmem_full2 : tmem_full, im ? q2 : q1, abort_flag) ? 1 : 0;
+                    okv = __shfl_sync(0xffffffffu, okv, 0);
+                    if (!okv) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    // D1 = [ArBr | ArBi]: re += ArBr, im += ArBi; D2 = [AiBr | AiBi]:
+                    // re -= AiBi, im += AiBr.  Two column blocks (four loads) in
+                    // flight per round
+                    const uint32_t dcol = im ? 2 * bn : 0;
+#pragma unroll
+                    for (int cp = 0; cp < 4; cp += 2) {
+                        if (cp >= ncc) break;   // warp-uniform (narrow tiles: 2 blocks)
+                        const uint32_t col = dcol + h * half_cols + cp * 16;
+                        float xr0[16], xi0[16], xr1[16], xi1[16];
+                        tmem_ld16(lane_base + col, xr0);
+                        tmem_ld16(lane_base + bn + col, xi0);
+                        tmem_ld16(lane_base + col + 16, xr1);
+                        tmem_ld16(lane_base + bn + col + 16, xi1);
+                        tmem_wait_ld();
+                        if (im) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                sr[cp * 16 + c] -= xi0[c];
+                                si[cp * 16 + c] += xr0[c];
+                                sr[cp * 16 + 16 + c] -= xi1[c];
+                                si[cp * 16 + 16 + c] += xr1[c];
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                sr[cp * 16 + c] += xr0[c];
+                                si[cp * 16 + c] += xi0[c];
+                                sr[cp * 16 + 16 + c] += xr1[c];
+                                si[cp * 16 + 16 + c] += xi1[c];
+                            }
+                        }
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(im ? tmem_empty2 : tmem_empty);
+                    if (im) q2 ^= 1;
+                    else q1 ^= 1;
+                }
+            }
+            for (int ch = 0; !PAIR && C::THREE && ch < nch; ++ch) {
                 int okv = 0;
                 if (lane == 0) okv = wait_bounded(tmem_full, tphase, abort_flag) ? 1 : 0;
                 okv = __shfl_sync(0xffffffffu, okv, 0);
