@@ -344,7 +344,7 @@ TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
  * core's accumulation rounds toward zero, so every node's sums shrink by a
  * relative bias that grows with the chunk (measured ~1.3e-6 per node with
  * 256, ~0.33e-6 with 64), and the nodes' biases add up at the root; shorter
- * chunks cost throughput (4096^3 node: ~346 TFLOP/s with 256, ~300 with 64).
+ * chunks cost throughput (4096^3 node: ~349 TFLOP/s with 256, ~323 with 64).
  * chunk_k = 0 (the default) picks, per plan, the longest of 256, 128 and 64
  * whose bias times the number of tensor-core nodes stays within 4e-6 (256 for
  * plain bf16 operands); otherwise a multiple of 32 in [32, 1024] for every
