@@ -285,6 +285,126 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
     }
 }
 
+// Gate-like node with n = k = 16 (a 4-mode gate on a large state): 1024 fp32
+// FMAs per 256 bytes of HBM traffic, so on the shared-memory B of
+// stream_rows_kernel the loads of B and the store loop cost as many issue
+// slots as the arithmetic.  Here eight lanes share a row: lane (h, q) owns
+// the outputs 8h .. 8h+7 and the complex k entries {2q, 2q+1, 8+2q, 9+2q},
+// and keeps the matching 8 x 4 slice of B in registers for the whole
+// launch, so the inner loop is FMAs only (and the registers leave room for
+// four warps per scheduler).  The four lanes of an output half combine
+// their partial sums by a reduce-scatter (two shuffle steps), after which
+// lane (h, q) holds outputs 8h + 2q and 8h + 2q + 1.  So that every lane
+// runs the same code, lane q's register i holds output 8h + (i ^ 2q): the
+// partner lane q ^ 2 keeps the same outputs in registers i ^ 4, and lane
+// q ^ 1 in registers i ^ 2.  Rows arrive through a per-warp ring of
+// cp.async copies (kG16Depth groups of 4 rows, 512 bytes, in flight per
+// warp; each lane copies 16 bytes and the warp syncs before reading).
+constexpr int kG16Warps = 16;
+constexpr int kG16Depth = 16;
+constexpr int kG16Smem = kG16Warps * kG16Depth * 512;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kG16Warps * 32, 1) stream_g16_kernel(const __grid_constant__ StreamArgs a) {
+    extern __shared__ __align__(16) float4 g16_ring[];
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rr = lane >> 3, h = (lane >> 2) & 1, q = lane & 3;
+    float4 *ring = g16_ring + warp * kG16Depth * 32;
+    // B slice: register i, entry t holds B[8h + (i ^ 2q)][kt], kt = 2q + (t & 1) + 8 (t >> 1)
+    float2 b[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int j = 8 * h + (i ^ (2 * q));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) b[i][t] = a.B[j * 16 + 2 * q + (t & 1) + 8 * (t >> 1)];
+    }
+    int64_t offn[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) offn[i] = a.rows_contig ? 8 * h + 2 * q + i : sep_offset(a.ln, 8 * h + 2 * q + i);
+    const int64_t ngroups = (a.m + 3) / 4;
+    const int64_t g0 = (int64_t)blockIdx.x * kG16Warps + warp;
+    const int64_t gstride = (int64_t)gridDim.x * kG16Warps;
+    // the warp's group g is rows 4g .. 4g+3, 512 contiguous bytes: lane l
+    // copies bytes 16 l .. 16 l + 15 (zero-filled past the last row)
+    auto issue = [&](int64_t g, int slot) {
+        const int64_t r = g * 4 + (lane >> 3);
+        const bool ok = r < a.m;
+        const float2 *src = a.A + (ok ? g * 64 + 2 * lane : 0);
+        cp_async16(ring + slot * 32 + lane, src, ok ? 16 : 0);
+    };
+#pragma unroll
+    for (int s = 0; s < kG16Depth - 1; ++s) {
+        const int64_t g = g0 + s * gstride;
+        if (g < ngroups) issue(g, s);
+        cp_async_commit();
+    }
+    int slot = 0;
+    for (int64_t g = g0; g < ngroups; g += gstride) {
+        const int64_t gn = g + (kG16Depth - 1) * gstride;
+        if (gn < ngroups) issue(gn, slot == 0 ? kG16Depth - 1 : slot - 1);
+        cp_async_commit();
+        cp_async_wait<kG16Depth - 1>();
+        __syncwarp();
+        // row rr's entries 2q, 2q+1 (16 bytes at 16 q) and 8+2q, 9+2q (at 64 + 16 q)
+        const float4 p0 = ring[slot * 32 + rr * 8 + q], p1 = ring[slot * 32 + rr * 8 + 4 + q];
+        __syncwarp();   // every lane has read the slot before it is refilled
+        slot = slot == kG16Depth - 1 ? 0 : slot + 1;
+        const float2 av[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w), make_float2(p1.x, p1.y),
+                              make_float2(p1.z, p1.w)};
+        float2 acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) cfma(acc[i], av[t], b[i][t]);
+        }
+        // reduce-scatter over the four lanes of the output half: keep
+        // registers 0..3 and receive lane ^ 2's 4..7 (the same outputs),
+        // then keep 0..1 and receive lane ^ 1's 2..3
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[i].x += __shfl_xor_sync(0xffffffffu, acc[i + 4].x, 2);
+            acc[i].y += __shfl_xor_sync(0xffffffffu, acc[i + 4].y, 2);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            acc[i].x += __shfl_xor_sync(0xffffffffu, acc[i + 2].x, 1);
+            acc[i].y += __shfl_xor_sync(0xffffffffu, acc[i + 2].y, 1);
+        }
+        const int64_t r = g * 4 + rr;
+        if (r < a.m) {
+            if (a.rows_contig && a.out_fmt == FMT_C64) {
+                float4 *p = reinterpret_cast<float4 *>(static_cast<float2 *>(a.C) + r * 16 + 8 * h + 2 * q);
+                float4 v = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                if (a.accumulate) {
+                    const float4 o = *p;
+                    v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                }
+                *p = v;
+            } else {
+                const int64_t offm = a.rows_contig ? r * 16 : sep_offset(a.lm, r);
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    store_entry(a.C, a.out_fmt, a.m * 16, offm + offn[i], acc[i], a.accumulate,
+                                a.out_tile);
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 __global__ void __launch_bounds__(kThreads) splitk_reduce_kernel(const __grid_constant__ ReduceArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -339,6 +459,22 @@ cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
         a2.rows_contig = args.n >= 4 &&
                          (args.lm.nrun == 0 || (args.lm.nrun == 1 && args.lm.stride[0] == args.n)) &&
                          (args.ln.nrun == 0 || (args.ln.nrun == 1 && args.ln.stride[0] == 1));
+        const bool a_aligned = (reinterpret_cast<uintptr_t>(args.A) & 15) == 0;
+        const bool c_aligned = (reinterpret_cast<uintptr_t>(args.C) & 15) == 0;
+        if (args.k == 16 && args.n == 16 && a_aligned && (c_aligned || !a2.rows_contig)) {
+            static bool attr_set = false;
+            if (!attr_set) {
+                cudaError_t e = cudaFuncSetAttribute(stream_g16_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kG16Smem);
+                if (e != cudaSuccess) return e;
+                attr_set = true;
+            }
+            const int64_t groups = (args.m + 7) / 8;
+            int64_t blocks = (groups + kG16Warps - 1) / kG16Warps;
+            if (blocks > 152) blocks = 152;
+            return launch_pdl(stream_g16_kernel, dim3((unsigned)blocks), dim3(kG16Warps * 32),
+                              (size_t)kG16Smem, stream, a2);
+        }
         const int K = args.k <= 2 ? 2 : args.k <= 4 ? 4 : args.k <= 8 ? 8 : 16;
         const int64_t pass = (int64_t)kThreads * (16 / K);
         int64_t blocks = (args.m + pass - 1) / pass;

@@ -14,7 +14,7 @@ import oracle
 from workloads import greedy_tree, grid_circuit_network
 from workloads.network import Network
 
-from helpers import TOL_C64, assert_close, node_network, run_gpu
+from helpers import TOL_BF16, TOL_BF16X3, TOL_C64, assert_close, node_network, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -91,3 +91,63 @@ def test_gate_like_root_with_slices_accumulates():
     assert plan.node_class(0) == tn.TN_NODE_STREAM and plan.num_slices == 3
     got, _ = run_gpu(net, [(0, 1)], slices=[3], policy=tn.TN_POLICY_NO_TINY)
     assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced gate-like root")
+
+
+def _rnd(rng, shape):
+    return ((rng.standard_normal(shape) + 1j * rng.standard_normal(shape)) * 0.5).astype(np.complex64)
+
+
+@pytest.mark.parametrize("m", [20, 8 * 152 * 8 + 3, 100003])
+def test_gate16_rows_ragged(m):
+    """n = k = 16 (four-lane rows, B in registers): row counts that leave a
+    partial group of 8 rows and a partial last pass over the grid."""
+    net = node_network(m, 16, 16, m + 11)
+    p = tn.Plan.from_network(net, [(0, 1)], (), "tf32x3", tn.TN_POLICY_NO_TINY)
+    assert p.node_class(0) == tn.TN_NODE_STREAM
+    got, _ = run_gpu(net, [(0, 1)], policy=tn.TN_POLICY_NO_TINY)
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, f"gate16 m={m}")
+
+
+def test_gate16_transposed_root():
+    """n = k = 16 with the root's axes in the order (j, i): the entries of a
+    row are not contiguous, so each lane stores its four outputs one by one
+    through the separable offsets."""
+    rng = np.random.default_rng(21)
+    ext = [30001, 2, 2, 2, 2, 2, 2, 2, 2]   # i, j0..j3, x0..x3
+    a = _rnd(rng, (30001, 2, 2, 2, 2))
+    b = _rnd(rng, (2, 2, 2, 2, 2, 2, 2, 2))
+    net = Network([[0, 5, 6, 7, 8], [1, 2, 3, 4, 5, 6, 7, 8]], ext, [1, 2, 3, 4, 0], [a, b])
+    p = tn.Plan.from_network(net, [(0, 1)], (), "tf32x3", tn.TN_POLICY_NO_TINY)
+    assert p.node_class(0) == tn.TN_NODE_STREAM
+    got, _ = run_gpu(net, [(0, 1)], policy=tn.TN_POLICY_NO_TINY)
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "gate16 transposed root")
+
+
+@pytest.mark.parametrize("prec", ["tf32x3", "bf16x3", "bf16"])
+def test_gate16_feeds_tensor_core_node(prec):
+    """An n = k = 16 node whose output is an operand of a tensor-core node:
+    the gate kernel writes the consumer's planar (K-tiled) format."""
+    rng = np.random.default_rng(22)
+    # modes: a(256) b(256) x(16) j(16) l(256)
+    ext = [256, 256, 16, 16, 256]
+    A = _rnd(rng, (256, 256, 16))
+    B = _rnd(rng, (16, 16))
+    D = _rnd(rng, (256, 16, 256))
+    net = Network([[0, 1, 2], [3, 2], [1, 3, 4]], ext, [0, 4], [A, B, D])
+    tree = [(0, 1), (3, 2)]
+    p = tn.Plan.from_network(net, tree, (), prec, tn.TN_POLICY_NO_TINY)
+    assert p.node_class(0) == tn.TN_NODE_STREAM and p.node_class(1) == tn.TN_NODE_DENSE
+    got, _ = run_gpu(net, tree, precision=prec, policy=tn.TN_POLICY_NO_TINY)
+    tol = {"tf32x3": TOL_C64, "bf16x3": TOL_BF16X3, "bf16": TOL_BF16}[prec]
+    assert_close(got, _ref(net, tree), tol, f"gate16 -> dense ({prec})")
+
+
+def test_gate16_root_with_slices_accumulates():
+    """n = k = 16 root summed over three slices (write, then add twice)."""
+    rng = np.random.default_rng(23)
+    ext = [40000, 16, 16, 3]                 # i j x z
+    net = Network([[0, 2, 3], [1, 2, 3]], ext, [0, 1], [_rnd(rng, (40000, 16, 3)), _rnd(rng, (16, 16, 3))])
+    plan = tn.Plan.from_network(net, [(0, 1)], [3], "tf32x3", tn.TN_POLICY_NO_TINY)
+    assert plan.node_class(0) == tn.TN_NODE_STREAM and plan.num_slices == 3
+    got, _ = run_gpu(net, [(0, 1)], slices=[3], policy=tn.TN_POLICY_NO_TINY)
+    assert_close(got, _ref(net, [(0, 1)]), TOL_C64, "sliced gate16 root")
