@@ -111,8 +111,8 @@ tn_status tn_plan_node_class(const tn_plan_t *plan, int32_t step, int32_t *cls) 
 
 tn_status tn_plan_set_promotion_chunk(tn_plan_t *plan, int32_t chunk_k) {
     if (!plan) return TN_EINVAL;
-    if (chunk_k != 0 && (chunk_k < 32 || chunk_k > 1024 || chunk_k % 32 != 0)) {
-        plan->p.last_error = "promotion chunk must be 0 or a multiple of 32 in [32, 1024]";
+    if (chunk_k != 0 && (chunk_k < 32 || chunk_k > 4096 || chunk_k % 32 != 0)) {
+        plan->p.last_error = "promotion chunk must be 0 or a multiple of 32 in [32, 4096]";
         return TN_EINVAL;
     }
     plan->p.chunk_k = chunk_k;

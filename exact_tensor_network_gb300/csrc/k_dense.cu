@@ -28,17 +28,14 @@
 // direction, and the shrinkage grows with the number of accumulations.  So
 // the k range of a tile is cut into chunks (DenseArgs::chunk_kb k-blocks,
 // chosen by the planner: 64, 128 or 256 complex k for the split precisions
-// depending on how many tensor-core nodes the tree holds, 256 for plain bf16
+// depending on how many tensor-core nodes the tree holds, 2048 for plain bf16
 // operands); each chunk is accumulated in TMEM from zero, then drained into
 // fp32 registers of the epilogue warps with ordinary round-to-nearest adds
 // (periodic promotion).  Measured on chains of 2^30-2^32-entry nodes:
 // 256-k chunks leave a relative bias of ~1.3e-6 per node, 64-k chunks about
 // a quarter of it.
-// The two accumulators are handed over separately: the MMA warp commits D1
-// after the chunk's last D1 products, then issues the D2 products while the
-// drain reads D1, and starts the next chunk's D1 products as soon as the
-// drain has released D1 (while it reads D2).  The drain thus hides behind
-// the tensor core's work instead of stalling it once per chunk.
+// The two accumulators are handed over separately: the drain reads D1
+// while the tensor core runs the last stage's D2 products.
 //
 // Structure: persistent kernel, one CTA of 384 threads per SM.  Warpgroup
 // 0: warp 0 issues TMA loads into a ring of shared-memory stages, warp 1
@@ -364,20 +361,24 @@ __device__ __forceinline__ void stage_block(float2 *tile, int lane, const float 
 // Work item w of a launch: its tile t, k-block range [kb0, kb1), k split sp
 // (split-K) and, for a tail tile's half, which half (else -1).  Work items
 // are whole tiles up to tail_first, then two halves per tail tile; with
-// split-K, ksplit items per tile.
+// split-K, the items of split 0 (every tile), then those of split 1, and so
+// on: the CTAs running at the same time then work on the same k range of
+// neighbouring tiles and share its operand pieces in L2 (a node with a huge
+// k and a few hundred tiles runs many waves; split-by-split, each piece of
+// either operand is read from DRAM about once instead of once per wave).
 struct Item {
     int64_t t;
     int sp, kb0, kb1, half;
 };
 __device__ __forceinline__ Item work_item(int64_t w, int ksplit, int kbs, int nkb,
-                                          int64_t tail_first) {
+                                          int64_t tail_first, int64_t tiles) {
     Item it;
     it.half = -1;
     if (ksplit > 1) {
-        // work < 2^31 items with split-K (tiles x splits fill about one wave)
-        const uint32_t q = static_cast<uint32_t>(w) / static_cast<uint32_t>(ksplit);
-        it.t = q;
-        it.sp = static_cast<int>(static_cast<uint32_t>(w) - q * static_cast<uint32_t>(ksplit));
+        // work < 2^31 items with split-K (tiles x splits is bounded)
+        const uint32_t q = static_cast<uint32_t>(w) / static_cast<uint32_t>(tiles);
+        it.sp = static_cast<int>(q);
+        it.t = static_cast<int64_t>(static_cast<uint32_t>(w) - q * static_cast<uint32_t>(tiles));
         it.kb0 = it.sp * kbs;
         it.kb1 = min(nkb, it.kb0 + kbs);
     } else if (w < tail_first) {
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
     const int64_t mtiles = (a.m + tile_rows - 1) / tile_rows, ntiles = (a.n + bn - 1) / bn;
     const int64_t tiles = mtiles * ntiles;
     const int nkb = static_cast<int>((a.k + C::KB - 1) / C::KB);
-    // work item w = (tile w / ksplit, k split w % ksplit); a split covers kbs
+    // work item w = (tile w % tiles, k split w / tiles); a split covers kbs
     // k-blocks
     const int ksplit = a.ksplit > 1 ? a.ksplit : 1;
     const int kbs = ksplit > 1 ? static_cast<int>(a.kchunk / C::KB) : nkb;
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t issued = 0, last_par = 0;   // bit s: stage s has a load; its parity
             bool ok = true;
             for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
-                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
                 int64_t mt, nt;
                 tile_coords(it.t, mtiles, ntiles, mt, nt);
                 // pairs: this CTA's 128 rows of A and 64 rows (columns of the
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0, cnt = 0;
             bool ok = true;
             for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
-                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
                 const int kb0 = it.kb0, kb1 = it.kb1;
                 const int nch = (kb1 - kb0 + CS - 1) / CS;
                 for (int ch = 0; ch < nch && ok; ++ch, ++cnt) {
@@ -682,26 +683,24 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         } else if (!PAIR && !C::THREE && warp == 1 && lane == 0) {
             // ---- MMA issuer (single CTA) ----
             // D1 = Ar [Br; Bi] and D2 = Ai [Br; Bi], 2 bn columns each, are
-            // promoted in chunks of CS stages whose boundaries lie one stage
-            // apart: D2's first chunk is the tile's first stage alone.  At the
-            // first stage of a D1 chunk the D2 products go first, so the drain
-            // reads the finished D1 chunk while the tensor core runs two
-            // stages' worth of D2 products, and likewise for D2 (one stage
-            // later, behind two stages' D1 products).  The drain therefore
-            // sees the chunks in the order D2, D1, D2, D1, ...
+            // promoted in chunks of CS stages, ending at the same stages; each
+            // is committed to the drain right after its own products, so the
+            // drain reads D1 while the tensor core runs the stage's D2
+            // products.  (Boundaries of D2 offset from D1's, so that each
+            // accumulator's drain hides behind two stages of the other's
+            // products, measured 1-3 % slower on 4096^3 nodes and up to a
+            // third slower on tiles of one or two chunks.)
             const uint32_t d1 = tmem, d2 = tmem + 2 * bn;
             const uint32_t idesc = C::idesc((uint32_t)(2 * bn));
             uint32_t stage = 0, phase = 0, ph1 = 0, ph2 = 0;
             bool ok = true;
             for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
-                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
                 const int kb0 = it.kb0, kb1 = it.kb1;
+                int cpos = 0;   // stage within the chunk, stepped without a division
                 for (int kb = kb0; kb < kb1 && ok; ++kb) {
-                    const int r = kb - kb0;
-                    const bool last = kb == kb1 - 1;
-                    const bool d1_start = r % CS == 0, d1_end = r % CS == CS - 1 || last;
-                    const bool d2_start = r == 0 || CS == 1 || r % CS == 1;
-                    const bool d2_end = r % CS == 0 || last;
+                    const bool cstart = cpos == 0, cend = cpos == CS - 1 || kb == kb1 - 1;
+                    cpos = cpos == CS - 1 ? 0 : cpos + 1;
                     if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
                         ok = false;
                         break;
@@ -709,49 +708,29 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     fence_after();
                     const uint32_t base = smem_u32(smem + stage * stage_bytes);
                     const uint32_t bbase = base + C::PLANES * PLANE_TILE;
-                    // the first stage of a D1 chunk issues D2 first; the
-                    // others D1 first
-                    if (d1_start) {
-                        if (d2_start) {
-                            if (!wait_bounded(tmem_empty2, ph2 ^ 1, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            fence_after();
-                        }
-                        stage_products<MODE, true>(d2, base, bbase, b_plane, d2_start, idesc);
-                        if (d2_end) {
-                            mma_commit(tmem_full2);   // the drain may read D2
-                            ph2 ^= 1;
-                        }
+                    if (cstart) {
                         if (!wait_bounded(tmem_empty, ph1 ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         fence_after();
-                        stage_products<MODE, false>(d1, base, bbase, b_plane, true, idesc);
-                        if (d1_end) {
-                            mma_commit(tmem_full);    // the drain may read D1
-                            ph1 ^= 1;
+                    }
+                    stage_products<MODE, false>(d1, base, bbase, b_plane, cstart, idesc);
+                    if (cend) {
+                        mma_commit(tmem_full);    // the drain may read D1
+                        ph1 ^= 1;
+                    }
+                    if (cstart) {
+                        if (!wait_bounded(tmem_empty2, ph2 ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
                         }
-                    } else {
-                        stage_products<MODE, false>(d1, base, bbase, b_plane, false, idesc);
-                        if (d1_end) {
-                            mma_commit(tmem_full);
-                            ph1 ^= 1;
-                        }
-                        if (d2_start) {
-                            if (!wait_bounded(tmem_empty2, ph2 ^ 1, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            fence_after();
-                        }
-                        stage_products<MODE, true>(d2, base, bbase, b_plane, d2_start, idesc);
-                        if (d2_end) {
-                            mma_commit(tmem_full2);
-                            ph2 ^= 1;
-                        }
+                        fence_after();
+                    }
+                    stage_products<MODE, true>(d2, base, bbase, b_plane, cstart, idesc);
+                    if (cend) {
+                        mma_commit(tmem_full2);   // the drain may read D2
+                        ph2 ^= 1;
                     }
                     if (!ok) break;
                     mma_commit(empty0 + 8 * stage);
@@ -771,7 +750,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             uint32_t stage = 0, phase = 0, tphase = 0;
             bool ok = true;
             for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
-                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+                const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
                 const int kb0 = it.kb0, kb1 = it.kb1;
                 const int nch = (kb1 - kb0 + CS - 1) / CS;
                 for (int ch = 0; ch < nch && ok; ++ch) {
@@ -916,7 +895,7 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
         uint32_t tphase = 0, pcnt = 0, q1 = 0, q2 = 0;
         bool ok = true;
         for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
-            const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST);
+            const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
             const int sp = it.sp;
             const int kb0 = it.kb0, kb1 = it.kb1;
             const int nch = (kb1 - kb0 + CS - 1) / CS;
@@ -962,13 +941,11 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                 }
             }
             if constexpr (!PAIR && !C::THREE) {
-                // the chunks of D1 and D2 alternate, D2 first (see the MMA
-                // issuer): n1 of D1 and n2 of D2
-                const int st = kb1 - kb0;
-                const int n1 = (st + CS - 1) / CS;
-                const int n2 = st <= 1 ? 1 : 1 + (st - 1 + CS - 1) / CS;
-                for (int e = 0; e < n1 + n2; ++e) {
-                    const bool im = (e & 1) == 0;
+                // the chunks of D1 and D2 alternate, D1 first (see the MMA
+                // issuer)
+                const int nch2 = 2 * ((kb1 - kb0 + CS - 1) / CS);
+                for (int e = 0; e < nch2; ++e) {
+                    const bool im = (e & 1) == 1;
                     int okv = 0;
                     if (lane == 0)
                         okv = wait_bounded(im ? tmem_full2 : tmem_full, im ? q2 : q1, abort_flag) ? 1 : 0;

@@ -325,13 +325,14 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
 // longest whose bias times the number of tensor-core nodes stays within 4e-6
 // (the complex64 tolerance is 1e-5): a longer chunk costs less bookkeeping
 // per k.  CTA pairs accumulate six products per k-step into one accumulator
-// instead of three: half the chunk.  Plain bf16 operands (tolerance 2e-2)
-// keep 256.
+// instead of three: half the chunk.  Plain bf16 operands (tolerance 2e-2,
+// rounding error of the operands ~1e-3) take 2048: their stages are short on
+// the tensor core, so each promotion's drain costs relatively more.
 void choose_chunks(Plan *p) {
     int dense = 0;
     for (const auto &nd : p->nodes) dense += nd.cls == TN_NODE_DENSE ? 1 : 0;
     int32_t chunk = dense <= 3 ? 256 : dense <= 6 ? 128 : 64;
-    if (p->precision == TN_PREC_BF16) chunk = 256;
+    if (p->precision == TN_PREC_BF16) chunk = 2048;
     if (p->chunk_k > 0) chunk = p->chunk_k;   // tn_plan_set_promotion_chunk
     // at least one pipeline stage (16 complex k of tf32 planes, 32 of bf16)
     const int32_t stage = (p->precision == TN_PREC_BF16 || p->precision == TN_PREC_BF16X3) ? 32 : 16;

@@ -346,9 +346,10 @@ TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
  * 256, ~0.33e-6 with 64), and the nodes' biases add up at the root; shorter
  * chunks cost throughput (4096^3 node: ~349 TFLOP/s with 256, ~323 with 64).
  * chunk_k = 0 (the default) picks, per plan, the longest of 256, 128 and 64
- * whose bias times the number of tensor-core nodes stays within 4e-6 (256 for
- * plain bf16 operands); otherwise a multiple of 32 in [32, 1024] for every
- * tensor-core node (CTA pairs use half of it).  Re-plans the layout (like
+ * whose bias times the number of tensor-core nodes stays within 4e-6 (2048
+ * for plain bf16 operands, whose own rounding is ~1e-3); otherwise a
+ * multiple of 32 in [32, 4096] for every tensor-core node (CTA pairs use
+ * half of it).  Re-plans the layout (like
  * tn_plan_set_policy): bind the workspace again afterwards.
  * Errors: TN_EINVAL (NULL plan or a value outside that set).
  */

@@ -245,14 +245,14 @@ def test_fused_leaf_subtrees_plan():
 
 def test_promotion_chunk_and_pairs_settings():
     """The promotion chunk accepts 0 (per plan) or multiples of 32 up to
-    1024 and rejects the rest; CTA pairs and the chunk only re-plan."""
+    4096 and rejects the rest; CTA pairs and the chunk only re-plan."""
     net = random_network(60, 1, with_data=False)
     tree = greedy_tree(net, 0)
     p = tn.Plan.from_network(net, tree)
     ref = [p.node_mnk(s) for s in range(len(tree))]
-    for c in (0, 32, 64, 256, 1024):
+    for c in (0, 32, 64, 256, 1024, 4096):
         p.set_promotion_chunk(c)
-    for bad in (-1, 16, 48, 2048):
+    for bad in (-1, 16, 48, 4128, 8192):
         with pytest.raises(tn.TNError) as e:
             p.set_promotion_chunk(bad)
         assert e.value.status == tn.TN_EINVAL
