@@ -410,6 +410,19 @@ __device__ __forceinline__ void tile_coords(int64_t t, int64_t mtiles, int64_t n
     nt = r / gm;
 }
 
+// Stages in the first promotion chunk of a tile with st k-stages and chunks
+// of cs stages.  When a tile starts, the drain is still storing the previous
+// tile's outputs; a first chunk of two chunks' length lets the tensor core
+// run that long before it needs the drain again, which hides the stores.
+// Only tiles of at least eight chunks take it.  A chunk's rounding bias
+// grows with its length and weighs by its share of k, so a tile of k = n c
+// whose first chunk is 2c has (4 + (n - 2)) / n times the bias of plain
+// c-chunks: at most a quarter more (n = 8), an eighth at n = 16.  Measured:
+// 4096^3 node +1.4 % (256-k chunks), `circuit_7x7_d10` +2.7 %; the 2^30- and
+// 2^32-entry exact-value norm networks' errors 4.0e-6 -> 4.3e-6 and 6.2e-6
+// -> 6.4e-6.
+__device__ __forceinline__ int first_chunk(int st, int cs) { return st >= 8 * cs ? 2 * cs : cs; }
+
 // The products of one stage into one accumulator of the single-CTA kernel:
 // D1 (IM = false) = Ar [Br; Bi] or D2 (IM = true) = Ai [Br; Bi]; split
 // precisions form hi*lo + lo*hi + hi*hi.  Fully unrolled with compile-time
@@ -697,10 +710,17 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             for (int64_t w = wfirst; w < WORK && ok; w += wstride) {
                 const Item it = work_item(w, ksplit, kbs, nkb, TAIL_FIRST, tiles);
                 const int kb0 = it.kb0, kb1 = it.kb1;
-                int cpos = 0;   // stage within the chunk, stepped without a division
+                // stage within the chunk, stepped without a division; the
+                // first chunk of a long tile is two chunks (first_chunk)
+                int cpos = 0, clen = first_chunk(kb1 - kb0, CS);
                 for (int kb = kb0; kb < kb1 && ok; ++kb) {
-                    const bool cstart = cpos == 0, cend = cpos == CS - 1 || kb == kb1 - 1;
-                    cpos = cpos == CS - 1 ? 0 : cpos + 1;
+                    const bool cstart = cpos == 0, cend = cpos == clen - 1 || kb == kb1 - 1;
+                    if (cpos == clen - 1) {
+                        cpos = 0;
+                        clen = CS;
+                    } else {
+                        ++cpos;
+                    }
                     if (!wait_bounded(full0 + 8 * stage, phase, abort_flag)) {
                         ok = false;
                         break;
@@ -943,7 +963,8 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
             if constexpr (!PAIR && !C::THREE) {
                 // the chunks of D1 and D2 alternate, D1 first (see the MMA
                 // issuer)
-                const int nch2 = 2 * ((kb1 - kb0 + CS - 1) / CS);
+                const int st = kb1 - kb0, f = first_chunk(st, CS);
+                const int nch2 = 2 * (st <= f ? 1 : 1 + (st - f + CS - 1) / CS);
                 for (int e = 0; e < nch2; ++e) {
                     const bool im = (e & 1) == 1;
                     int okv = 0;
