@@ -378,3 +378,31 @@ def test_cta_pairs_network_and_slices():
     got, plan = run_gpu(net, [(0, 1)], [3], policy=NT, pairs=True)
     assert plan.num_slices == 4 and plan.node_class(0) == tn.TN_NODE_DENSE
     assert_close(got, _ref(net, [(0, 1)], [3]), TOL_C64, "sliced pair node")
+
+
+@pytest.mark.parametrize("m,n,k,chunk,precision,tol", [
+    (2048, 1280, 2048, 32, "tf32x3", TOL_C64),     # whole tiles of 128 stages and tail halves of 64, 2-stage chunks
+    (2048, 1280, 1040, 64, "tf32x3", TOL_C64),     # 65 stages: halves of 32 and 33, 4-stage chunks
+    (2000, 1300, 2064, 128, "tf32x3", TOL_C64),    # ragged tiles, 129 stages, 8-stage chunks
+    (64, 4096, 4096, 32, "tf32x3", TOL_C64),       # swapped narrow tiles, split-K with long splits
+    (2048, 1280, 2048, 64, "bf16x3", TOL_BF16X3),  # bf16 stages of 32 k: 2-stage chunks
+    (2048, 1280, 4096, 256, "bf16", TOL_BF16),     # 8-stage chunks, tail halves of 64 stages
+])
+def test_promotion_chunk_boundaries(m, n, k, chunk, precision, tol):
+    """Promotion chunks of every length the planner or the caller can pick,
+    on whole tiles, tail halves and split-K items: a tile of at least eight
+    chunks starts with one of two chunks' length, shorter tiles do not, and
+    every k-block is accumulated exactly once (oracle)."""
+    import torch
+    net = node_network(m, n, k, m + 5 * n + 3 * k + chunk)
+    plan = tn.Plan.from_network(net, [(0, 1)], (), precision, NT)
+    plan.set_promotion_chunk(chunk)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE
+    dev = torch.device("cuda:0")
+    leaves = [torch.from_numpy(np.ascontiguousarray(d)).to(dev) for d in net.data]
+    out = torch.full(plan.out_shape, complex(7.0, -3.0), dtype=torch.complex64, device=dev)
+    plan.execute(leaves, out)
+    torch.cuda.synchronize(dev)
+    plan.check()
+    assert_close(out.cpu().numpy().astype(np.complex128), _ref(net, [(0, 1)]), tol,
+                 f"{m}x{n}x{k} chunk {chunk} {precision}")
