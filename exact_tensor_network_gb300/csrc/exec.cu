@@ -570,7 +570,7 @@ tn_status issue_range(Plan *p, const void *const *leaf_ptrs, void *out_ptr, cuda
                 pl->job[j] = job;
                 pl->cta_start[j] = ctas;
                 pl->src[j] = leaf_src[p->perm_leaves[job]];
-                ctas += permute_ctas(p->perm_table[job].size);
+                ctas += permute_job_ctas(p->perm_table[job]);
             }
             pl->cta_start[cnt] = ctas;
             // algorithmic bytes: every entry read once (complex64) and written

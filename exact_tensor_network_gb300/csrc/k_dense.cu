@@ -213,11 +213,25 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 
 // Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, rows of
 // 64 bytes, 8-row core groups 512 bytes apart.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+__host__ __device__ constexpr uint64_t sdesc(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>(512 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(4) << 61);
 }
+// The same descriptor as two words: the upper one is a constant, the lower
+// one holds the address in 16-byte units.  Shared-memory addresses stay
+// below 256 KiB, so moving the address by `off` bytes (a multiple of 16)
+// adds off / 16 to the lower word without a carry out of its 14-bit field:
+// the MMA thread forms a stage's descriptors once and steps them with
+// 32-bit adds.
+constexpr uint32_t kDescHi = static_cast<uint32_t>(sdesc(0) >> 32);
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr) {
+    return static_cast<uint32_t>(sdesc(saddr));
+}
+static_assert(sdesc(0x2A3C0) == ((static_cast<uint64_t>(kDescHi) << 32) | sdesc_lo(0x2A3C0)) &&
+                  sdesc_lo(0x2A3C0 + 96) == sdesc_lo(0x2A3C0) + 6 &&
+                  sdesc_lo(0x37FF0) + 1 == sdesc_lo(0x38000),
+              "split descriptor words");
 
 template <int MODE>
 __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc, uint32_t idesc) {
@@ -231,6 +245,40 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
             "l"(a), "l"(b), "r"(idesc), "r"(acc));
+    }
+}
+
+// The same MMA from the two descriptor words (lower words of A and B, the
+// constant upper word); ACC < 0 takes the accumulate flag from `acc`, else
+// it is the constant ACC.
+template <int MODE, int ACC>
+__device__ __forceinline__ void mma_w(uint32_t d, uint32_t alo, uint32_t blo, uint32_t acc, uint32_t idesc) {
+    if constexpr (ACC < 0) {
+        if constexpr (Cfg<MODE>::HALF)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+                "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi));
+        else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+                "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+                "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(kDescHi));
+    } else {
+        if constexpr (Cfg<MODE>::HALF)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+                "r"(alo), "r"(blo), "r"(idesc), "n"(ACC), "r"(kDescHi));
+        else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+                "tcgen05.mma.cta_group::1.kind::tf32 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+                "r"(alo), "r"(blo), "r"(idesc), "n"(ACC), "r"(kDescHi));
     }
 }
 
@@ -432,20 +480,22 @@ template <int MODE, bool IM>
 __device__ __forceinline__ void stage_products(uint32_t d, uint32_t base, uint32_t bbase,
                                                uint32_t b_plane, bool fresh, uint32_t idesc) {
     using C = Cfg<MODE>;
-    const uint32_t ah = base + (IM ? PLANE_TILE : 0);
+    // descriptor lower words of the stage's planes; each instruction takes
+    // 32 bytes of K (2 in 16-byte units)
+    const uint32_t ah = sdesc_lo(base + (IM ? PLANE_TILE : 0)), bh = sdesc_lo(bbase);
+    const uint32_t acc0 = fresh ? 0u : 1u;
+    if constexpr (C::BF16) {
+        mma_w<MODE, -1>(d, ah, bh, acc0, idesc);
 #pragma unroll
-    for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
-        const uint32_t off = kk * 32;   // 32 bytes of K per instruction
-        const uint32_t acc = (fresh && kk == 0) ? 0u : 1u;
-        if constexpr (C::BF16) {
-            mma<MODE>(d, sdesc(ah + off), sdesc(bbase + off), acc, idesc);
-        } else {
-            const uint32_t al = base + (IM ? 3 : 2) * PLANE_TILE;
-            const uint64_t bh = sdesc(bbase + off);
-            const uint64_t bl = sdesc(bbase + 2 * b_plane + off);
-            mma<MODE>(d, sdesc(al + off), bh, acc, idesc);
-            mma<MODE>(d, sdesc(ah + off), bl, 1, idesc);
-            mma<MODE>(d, sdesc(ah + off), bh, 1, idesc);
+        for (int kk = 1; kk < C::KB / C::K_INSTR; ++kk) mma_w<MODE, 1>(d, ah + 2 * kk, bh + 2 * kk, 1, idesc);
+    } else {
+        const uint32_t al = sdesc_lo(base + (IM ? 3 : 2) * PLANE_TILE), bl = sdesc_lo(bbase + 2 * b_plane);
+#pragma unroll
+        for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+            if (kk == 0) mma_w<MODE, -1>(d, al, bh, acc0, idesc);
+            else mma_w<MODE, 1>(d, al + 2 * kk, bh + 2 * kk, 1, idesc);
+            mma_w<MODE, 1>(d, ah + 2 * kk, bl + 2 * kk, 1, idesc);
+            mma_w<MODE, 1>(d, ah + 2 * kk, bh + 2 * kk, 1, idesc);
         }
     }
 }

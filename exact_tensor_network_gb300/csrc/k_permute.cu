@@ -17,7 +17,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kItems = 4;
 
-__global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant__ PermLaunch a) {
+__global__ void __launch_bounds__(kThreads, 3) permute_kernel(const __grid_constant__ PermLaunch a) {
     pdl_trigger();
     pdl_wait();
     // Find this CTA's job (uniform across the CTA).
@@ -124,20 +124,34 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
         const int kt = tl.kt;
         const int64_t nrb = (rows + 31) / 32, ncb = (kk + 127) / 128;
         const PlanarTile untiled{0, 0, -1, 0};
-        for (int64_t u = local; u < nrb * ncb; u += ctas) {
+        // each CTA takes several blocks; the next block's loads are in flight
+        // while this one's tile rows are stored
+        const int64_t nblk = nrb * ncb;
+        // thread: rows trow + 4 i of the block, entries c2, c2 + 1 (64 pairs
+        // of entries per row)
+        const int trow = threadIdx.x >> 6, c2 = (threadIdx.x & 63) * 2;
+        float4 nxt[8];
+        auto load_block = [&](int64_t u) {
+            const int64_t r0 = (u / ncb) * 32, c0 = (u % ncb) * 128;
+            if (c2 >= (int)min((int64_t)128, kk - c0)) return;
+            const float4 *p = reinterpret_cast<const float4 *>(src + (r0 + trow) * kk + c0 + c2);
+            const int64_t rstep = 2 * kk;   // four rows, in float4 units
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (r0 + trow + 4 * i < rows) nxt[i] = p[i * rstep];
+        };
+        if (local < nblk) load_block(local);
+        for (int64_t u = local; u < nblk; u += ctas) {
             const int64_t r0 = (u / ncb) * 32, c0 = (u % ncb) * 128;
             const int cw = (int)min((int64_t)128, kk - c0);   // a multiple of kt
             __syncthreads();   // the previous block's readers are done
+            if (c2 < cw) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int f = threadIdx.x + kThreads * i;   // 64 pairs of entries per row
-                const int row = f >> 6, c2 = (f & 63) * 2;
-                if (r0 + row < rows && c2 < cw) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src + (r0 + row) * kk + c0 + c2);
-                    *reinterpret_cast<float4 *>(&blk[row][c2]) = v;
-                }
+                for (int i = 0; i < 8; ++i)
+                    if (r0 + trow + 4 * i < rows) *reinterpret_cast<float4 *>(&blk[trow + 4 * i][c2]) = nxt[i];
             }
             __syncthreads();
+            if (u + ctas < nblk) load_block(u + ctas);
             // quads of 4 entries: 8 kt quads per tile row block of 32 rows
             const int quads = (cw / kt) * 8 * kt;
             for (int q = threadIdx.x; q < quads; q += kThreads) {
@@ -326,6 +340,19 @@ int permute_ctas(int64_t size) {
     if (c < 1) c = 1;
     if (c > 4096) c = 4096;
     return (int)c;
+}
+
+int permute_job_ctas(const PermDesc &d) {
+    if (d.tax < 0 && d.contig && d.tile.kt != 0) {
+        // K-tiled conversion: blocks of 32 rows x 128 entries, four per CTA
+        // (the next block's loads overlap this one's stores)
+        const int64_t blocks = ((d.tile.rows + 31) / 32) * ((d.tile.k + 127) / 128);
+        int64_t c = (blocks + 3) / 4;
+        if (c < 1) c = 1;
+        if (c > 4096) c = 4096;
+        return (int)c;
+    }
+    return permute_ctas(d.size);
 }
 
 cudaError_t launch_permute(const PermLaunch &args, int total_ctas, cudaStream_t stream) {

@@ -150,6 +150,9 @@ cudaError_t launch_simt_node(const NodeArgs &args, cudaStream_t stream);
 
 // CTAs a permutation job of `size` elements gets.
 int permute_ctas(int64_t size);
+// CTAs for one leaf job of permute_kernel (K-tiled conversions take several
+// 32 x 128 blocks per CTA)
+int permute_job_ctas(const PermDesc &d);
 
 // Copy of whole leaves from pinned host memory (read through its device
 // mapping over the host link) into device buffers: one launch for many
