@@ -355,6 +355,25 @@ __device__ __forceinline__ void mma_pair(uint32_t d, uint64_t a, uint64_t b, uin
     }
 }
 
+// The pair MMA from the two descriptor words (see mma_w).
+template <int MODE, int ACC>
+__device__ __forceinline__ void mma_pair_w(uint32_t d, uint32_t alo, uint32_t blo, uint32_t acc,
+                                           uint32_t idesc) {
+    const uint32_t en = ACC < 0 ? acc : static_cast<uint32_t>(ACC);
+    if constexpr (Cfg<MODE>::HALF)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+            "r"(alo), "r"(blo), "r"(idesc), "r"(en), "r"(kDescHi));
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+            "r"(alo), "r"(blo), "r"(idesc), "r"(en), "r"(kDescHi));
+}
+
 // Arrive on the mbarrier at this shared-memory offset in both CTAs of the
 // pair once the leader's MMAs issued so far have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
@@ -695,40 +714,55 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                         fence_after();
                         const uint32_t base = smem_u32(smem + stage * stage_bytes);
                         const uint32_t bbase = base + C::PLANES * PLANE_TILE;
-                        const bool first = kb == kb_beg;
+                        const uint32_t acc0 = kb == kb_beg ? 0u : 1u;
+                        constexpr uint32_t id = C::IDESC_PAIR, idn = C::IDESC_PAIR_NEG;
+                        // descriptor lower words of the stage's planes, stepped
+                        // by 2 (32 bytes of K) per instruction
+                        const uint32_t arh = sdesc_lo(base), aih = sdesc_lo(base + PLANE_TILE);
+                        const uint32_t brh = sdesc_lo(bbase), bih = sdesc_lo(bbase + b_plane);
+                        if constexpr (C::BF16) {
 #pragma unroll
-                        for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
-                            const uint32_t off = kk * 32;   // 32 bytes of K per instruction
-                            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-                            constexpr uint32_t id = C::IDESC_PAIR, idn = C::IDESC_PAIR_NEG;
-                            if constexpr (C::BF16) {
-                                const uint64_t ar = sdesc(base + off), ai = sdesc(base + PLANE_TILE + off);
-                                const uint64_t br = sdesc(bbase + off), bi = sdesc(bbase + b_plane + off);
-                                mma_pair<MODE>(cr, ar, br, acc, id);
-                                mma_pair<MODE>(cr, ai, bi, 1, idn);   // - Ai Bi
-                                mma_pair<MODE>(ci, ar, bi, acc, id);
-                                mma_pair<MODE>(ci, ai, br, 1, id);
-                            } else {
-                                // planes [re_hi, im_hi, re_lo, im_lo]; each
-                                // product is hi*lo + lo*hi + hi*hi
-                                const uint64_t arh = sdesc(base + off), aih = sdesc(base + PLANE_TILE + off);
-                                const uint64_t arl = sdesc(base + 2 * PLANE_TILE + off);
-                                const uint64_t ail = sdesc(base + 3 * PLANE_TILE + off);
-                                const uint64_t brh = sdesc(bbase + off), bih = sdesc(bbase + b_plane + off);
-                                const uint64_t brl = sdesc(bbase + 2 * b_plane + off);
-                                const uint64_t bil = sdesc(bbase + 3 * b_plane + off);
-                                mma_pair<MODE>(cr, arl, brh, acc, id);
-                                mma_pair<MODE>(cr, arh, brl, 1, id);
-                                mma_pair<MODE>(cr, arh, brh, 1, id);
-                                mma_pair<MODE>(cr, ail, bih, 1, idn);
-                                mma_pair<MODE>(cr, aih, bil, 1, idn);
-                                mma_pair<MODE>(cr, aih, bih, 1, idn);
-                                mma_pair<MODE>(ci, arl, bih, acc, id);
-                                mma_pair<MODE>(ci, arh, bil, 1, id);
-                                mma_pair<MODE>(ci, arh, bih, 1, id);
-                                mma_pair<MODE>(ci, ail, brh, 1, id);
-                                mma_pair<MODE>(ci, aih, brl, 1, id);
-                                mma_pair<MODE>(ci, aih, brh, 1, id);
+                            for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+                                const uint32_t o = 2 * kk;
+                                if (kk == 0) {
+                                    mma_pair_w<MODE, -1>(cr, arh, brh, acc0, id);
+                                    mma_pair_w<MODE, 1>(cr, aih, bih, 1, idn);   // - Ai Bi
+                                    mma_pair_w<MODE, -1>(ci, arh, bih, acc0, id);
+                                } else {
+                                    mma_pair_w<MODE, 1>(cr, arh + o, brh + o, 1, id);
+                                    mma_pair_w<MODE, 1>(cr, aih + o, bih + o, 1, idn);
+                                    mma_pair_w<MODE, 1>(ci, arh + o, bih + o, 1, id);
+                                }
+                                mma_pair_w<MODE, 1>(ci, aih + o, brh + o, 1, id);
+                            }
+                        } else {
+                            // planes [re_hi, im_hi, re_lo, im_lo]; each product
+                            // is hi*lo + lo*hi + hi*hi
+                            const uint32_t arl = sdesc_lo(base + 2 * PLANE_TILE), ail = sdesc_lo(base + 3 * PLANE_TILE);
+                            const uint32_t brl = sdesc_lo(bbase + 2 * b_plane), bil = sdesc_lo(bbase + 3 * b_plane);
+#pragma unroll
+                            for (int kk = 0; kk < C::KB / C::K_INSTR; ++kk) {
+                                const uint32_t o = 2 * kk;
+                                if (kk == 0) {
+                                    mma_pair_w<MODE, -1>(cr, arl, brh, acc0, id);
+                                } else {
+                                    mma_pair_w<MODE, 1>(cr, arl + o, brh + o, 1, id);
+                                }
+                                mma_pair_w<MODE, 1>(cr, arh + o, brl + o, 1, id);
+                                mma_pair_w<MODE, 1>(cr, arh + o, brh + o, 1, id);
+                                mma_pair_w<MODE, 1>(cr, ail + o, bih + o, 1, idn);
+                                mma_pair_w<MODE, 1>(cr, aih + o, bil + o, 1, idn);
+                                mma_pair_w<MODE, 1>(cr, aih + o, bih + o, 1, idn);
+                                if (kk == 0) {
+                                    mma_pair_w<MODE, -1>(ci, arl, bih, acc0, id);
+                                } else {
+                                    mma_pair_w<MODE, 1>(ci, arl + o, bih + o, 1, id);
+                                }
+                                mma_pair_w<MODE, 1>(ci, arh + o, bil + o, 1, id);
+                                mma_pair_w<MODE, 1>(ci, arh + o, bih + o, 1, id);
+                                mma_pair_w<MODE, 1>(ci, ail + o, brh + o, 1, id);
+                                mma_pair_w<MODE, 1>(ci, aih + o, brl + o, 1, id);
+                                mma_pair_w<MODE, 1>(ci, aih + o, brh + o, 1, id);
                             }
                         }
                         mma_commit_pair(empty0 + 8 * stage);   // both CTAs may refill the stage

@@ -85,6 +85,13 @@ def test_6x6_d12_two_trees_agree():
     assert a.shape == (2,) * 6
     assert np.all(np.isfinite(a)) and np.abs(a).max() > 0
     assert_close(b, a, 2 * TOL_C64, "6x6 d12: second tree, sliced")
+    # Porter-Thomas sanity (reported): over the random single-qubit gates of
+    # the last layer, E |<x|C|0>|^2 = 2^-36 for every x, so the mean of
+    # 2^36 |amp|^2 over the 64 amplitudes is about 1; the loose bound only
+    # catches a gross scale error (the exact-value norm networks pin it)
+    pt = float(np.mean(np.abs(a.astype(np.complex128)) ** 2) * 2.0 ** 36)
+    print(f"6x6 d12: mean of 2^36 |amp|^2 over 64 amplitudes = {pt:.3f}")
+    assert 0.05 < pt < 20
 
 
 def test_7x7_d10_two_slicings_agree():
