@@ -75,15 +75,21 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
         // the chunk table)
         for (int base = threadIdx.x - lane; base < total; base += kThreads) {
             const FuseNode &nd = nodes[cnode[c0 + (base >> 5)]];
-            const int L = nd.lanes;
+            // shifts, not divisions: every level waits for its slowest chain
+            const int L = 1 << nd.lshift;
             const int item = base + lane - nd.obase;
-            const int o = item / L, l = item - o * L;
+            const int o = item >> nd.lshift, l = item & (L - 1);
             const bool valid = o < nd.m * nd.n;
             float2 acc = make_float2(0.f, 0.f);
             int i = 0, j = 0;
             if (valid) {
-                i = o / nd.n;
-                j = o - i * nd.n;
+                if (nd.nshift >= 0) {
+                    i = o >> nd.nshift;
+                    j = o & (nd.n - 1);
+                } else {
+                    i = o / nd.n;
+                    j = o - i * nd.n;
+                }
                 const float2 *ar = sm + nd.a + i * nd.k, *br = sm + nd.b + j * nd.k;
                 // two independent chains of multiply-adds
                 float2 acc1 = make_float2(0.f, 0.f);

@@ -310,7 +310,8 @@ struct FuseNode {        // one step of a group (copied to shared memory)
     int32_t a, b;        // shared-memory offsets of the operands
     int32_t c;           // shared-memory offset of the output; -1: the group's root
     int32_t m, n, k;
-    int32_t lanes;       // threads that split one output's k range (power of two <= 32)
+    int32_t lshift;      // log2 of the threads that split one output's k range (<= 5)
+    int32_t nshift;      // log2(n) when n is a power of two, else -1
     int32_t obase;       // first thread item of this step in its level (a multiple of
                          // 32: a warp never holds two steps)
     int32_t off;         // output offsets: offM(i) at off + i, offN(j) at off + m + j

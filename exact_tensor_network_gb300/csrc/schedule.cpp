@@ -291,10 +291,13 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
                 // a few k entries per thread: long k ranges are split over
                 // up to 32 threads (one serial chain of k multiply-adds per
                 // thread would be the group's critical path)
-                f.lanes = 1;
-                while (f.lanes < 32 && f.lanes * 4 < f.k) f.lanes *= 2;
+                f.lshift = 0;
+                while (f.lshift < 5 && (4 << f.lshift) < f.k) ++f.lshift;
+                f.nshift = -1;
+                for (int32_t t = 0; t < 31; ++t)
+                    if ((int32_t(1) << t) == f.n) f.nshift = t;
                 f.obase = obase;
-                obase += (f.m * f.n * f.lanes + 31) / 32 * 32;
+                obase += (((f.m * f.n) << f.lshift) + 31) / 32 * 32;
                 // the step of every warp chunk of this level
                 for (int32_t c = f.obase; c < obase; c += 32)
                     fchunks.push_back((int32_t)(fnodes.size() - (size_t)G.first_node));
