@@ -298,8 +298,9 @@ __global__ void __launch_bounds__(kThreads) stream_rows_kernel(const __grid_cons
 // runs the same code, lane q's register i holds output 8h + (i ^ 2q): the
 // partner lane q ^ 2 keeps the same outputs in registers i ^ 4, and lane
 // q ^ 1 in registers i ^ 2.  Rows arrive through a per-warp ring of
-// cp.async copies (kG16Depth groups of 4 rows, 512 bytes, in flight per
-// warp; each lane copies 16 bytes and the warp syncs before reading).
+// cp.async copies (kG16Depth groups of 4 rows, 512 bytes, per warp; each
+// lane copies 16 bytes, and one warp sync per group makes the group
+// readable and frees the slot read last for the next copy).
 constexpr int kG16Warps = 16;
 constexpr int kG16Depth = 16;
 constexpr int kG16Smem = kG16Warps * kG16Depth * 512;
@@ -352,14 +353,15 @@ __global__ void __launch_bounds__(kG16Warps * 32, 1) stream_g16_kernel(const __g
     }
     int slot = 0;
     for (int64_t g = g0; g < ngroups; g += gstride) {
-        const int64_t gn = g + (kG16Depth - 1) * gstride;
-        if (gn < ngroups) issue(gn, slot == 0 ? kG16Depth - 1 : slot - 1);
-        cp_async_commit();
-        cp_async_wait<kG16Depth - 1>();
+        // this group's copies (every lane's) are complete and visible, and
+        // every lane has read the previous slot: it can be refilled
+        cp_async_wait<kG16Depth - 2>();
         __syncwarp();
         // row rr's entries 2q, 2q+1 (16 bytes at 16 q) and 8+2q, 9+2q (at 64 + 16 q)
         const float4 p0 = ring[slot * 32 + rr * 8 + q], p1 = ring[slot * 32 + rr * 8 + 4 + q];
-        __syncwarp();   // every lane has read the slot before it is refilled
+        const int64_t gn = g + (kG16Depth - 1) * gstride;
+        if (gn < ngroups) issue(gn, slot == 0 ? kG16Depth - 1 : slot - 1);
+        cp_async_commit();
         slot = slot == kG16Depth - 1 ? 0 : slot + 1;
         const float2 av[4] = {make_float2(p0.x, p0.y), make_float2(p0.z, p0.w), make_float2(p1.x, p1.y),
                               make_float2(p1.z, p1.w)};
