@@ -327,7 +327,11 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
 // relative errors of a tree's nodes add up at its root.  The chunk is the
 // longest whose bias times the number of tensor-core nodes stays within 4e-6
 // (the complex64 tolerance is 1e-5): a longer chunk costs less bookkeeping
-// per k.  CTA pairs accumulate six products per k-step into one accumulator
+// per k.  The kernel makes the first chunk of a tile of eight or more chunks
+// twice as long (the tile's bias grows by at most a quarter, an eighth at
+// sixteen chunks); the budget leaves room for it: on the 7x7 x 10-cycle
+// circuit (six nodes, 128-k chunks) the estimate grows from 3.9e-6 to
+// 4.1e-6.  CTA pairs accumulate six products per k-step into one accumulator
 // instead of three: half the chunk.  Plain bf16 operands (tolerance 2e-2,
 // rounding error of the operands ~1e-3) take 2048: their stages are short on
 // the tensor core, so each promotion's drain costs relatively more.
