@@ -329,10 +329,12 @@ void form_groups(Plan *p, std::vector<FuseNode> &fnodes, std::vector<FuseGather>
 // (the complex64 tolerance is 1e-5): a longer chunk costs less bookkeeping
 // per k.  The kernel makes the first chunk of a tile of eight or more chunks
 // twice as long (the tile's bias grows by at most a quarter, an eighth at
-// sixteen chunks); the budget leaves room for it: on the 7x7 x 10-cycle
+// sixteen chunks), which the budget does not count: on the 7x7 x 10-cycle
 // circuit (six nodes, 128-k chunks) the estimate grows from 3.9e-6 to
-// 4.1e-6.  CTA pairs accumulate six products per k-step into one accumulator
-// instead of three: half the chunk.  Plain bf16 operands (tolerance 2e-2,
+// 4.1e-6, still well inside the tolerance (the exact-value norm networks
+// measure 4.3e-6 and 6.4e-6 in all).  CTA pairs accumulate six products per
+// k-step into one accumulator instead of three: half the chunk.  Plain bf16
+// operands (tolerance 2e-2,
 // rounding error of the operands ~1e-3) take 2048: their stages are short on
 // the tensor core, so each promotion's drain costs relatively more.
 void choose_chunks(Plan *p) {
