@@ -344,12 +344,14 @@ int permute_ctas(int64_t size) {
 
 int permute_job_ctas(const PermDesc &d) {
     if (d.tax < 0 && d.contig && d.tile.kt != 0) {
-        // K-tiled conversion: blocks of 32 rows x 128 entries, four per CTA
-        // (the next block's loads overlap this one's stores)
+        // K-tiled conversion: blocks of 32 rows x 128 entries, at least four
+        // per CTA (the next block's loads overlap this one's stores), and at
+        // most one full wave of CTAs (three per SM) per leaf: a large leaf's
+        // CTAs then walk its blocks in one wave instead of several
         const int64_t blocks = ((d.tile.rows + 31) / 32) * ((d.tile.k + 127) / 128);
         int64_t c = (blocks + 3) / 4;
         if (c < 1) c = 1;
-        if (c > 4096) c = 4096;
+        if (c > 3 * 152) c = 3 * 152;
         return (int)c;
     }
     return permute_ctas(d.size);
