@@ -471,7 +471,7 @@ cudaError_t launch_stream_node(const StreamArgs &args, cudaStream_t stream) {
                 if (e != cudaSuccess) return e;
                 attr_set = true;
             }
-            const int64_t groups = (args.m + 7) / 8;
+            const int64_t groups = (args.m + 3) / 4;   // groups of four rows, one per warp pass
             int64_t blocks = (groups + kG16Warps - 1) / kG16Warps;
             if (blocks > 152) blocks = 152;
             return launch_pdl(stream_g16_kernel, dim3((unsigned)blocks), dim3(kG16Warps * 32),
