@@ -405,6 +405,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive columns of this thread's TMEM lane (one instruction for
+// what two 16-column loads read).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -1061,34 +1080,28 @@ __global__ void __launch_bounds__(THREADS, 1) dense_kernel(const __grid_constant
                     }
                     fence_after();
                     // D1 = [ArBr | ArBi]: re += ArBr, im += ArBi; D2 = [AiBr | AiBi]:
-                    // re -= AiBi, im += AiBr.  Two column blocks (four loads) in
-                    // flight per round
+                    // re -= AiBi, im += AiBr.  Two column blocks (two 32-column
+                    // loads) in flight per round
                     const uint32_t dcol = im ? 2 * bn : 0;
 #pragma unroll
                     for (int cp = 0; cp < 4; cp += 2) {
                         if (cp >= ncc) break;   // warp-uniform (narrow tiles: 2 blocks)
                         const uint32_t col = dcol + h * half_cols + cp * 16;
-                        float xr0[16], xi0[16], xr1[16], xi1[16];
-                        tmem_ld16(lane_base + col, xr0);
-                        tmem_ld16(lane_base + bn + col, xi0);
-                        tmem_ld16(lane_base + col + 16, xr1);
-                        tmem_ld16(lane_base + bn + col + 16, xi1);
+                        float xr[32], xi[32];
+                        tmem_ld32(lane_base + col, xr);
+                        tmem_ld32(lane_base + bn + col, xi);
                         tmem_wait_ld();
                         if (im) {
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                sr[cp * 16 + c] -= xi0[c];
-                                si[cp * 16 + c] += xr0[c];
-                                sr[cp * 16 + 16 + c] -= xi1[c];
-                                si[cp * 16 + 16 + c] += xr1[c];
+                            for (int c = 0; c < 32; ++c) {
+                                sr[cp * 16 + c] -= xi[c];
+                                si[cp * 16 + c] += xr[c];
                             }
                         } else {
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                sr[cp * 16 + c] += xr0[c];
-                                si[cp * 16 + c] += xi0[c];
-                                sr[cp * 16 + 16 + c] += xr1[c];
-                                si[cp * 16 + 16 + c] += xi1[c];
+                            for (int c = 0; c < 32; ++c) {
+                                sr[cp * 16 + c] += xr[c];
+                                si[cp * 16 + c] += xi[c];
                             }
                         }
                     }
