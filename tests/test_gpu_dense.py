@@ -406,3 +406,17 @@ def test_promotion_chunk_boundaries(m, n, k, chunk, precision, tol):
     plan.check()
     assert_close(out.cpu().numpy().astype(np.complex128), _ref(net, [(0, 1)]), tol,
                  f"{m}x{n}x{k} chunk {chunk} {precision}")
+
+
+@pytest.mark.parametrize("precision,tol", [("tf32x3", TOL_C64), ("bf16x3", TOL_BF16X3), ("bf16", TOL_BF16)])
+@pytest.mark.parametrize("m,n,k", [(512, 2048, 32), (300, 1000, 48), (1024, 640, 256), (130, 4000, 64),
+                                   (2048, 512, 32)])
+def test_short_k_nodes_on_narrow_tiles(m, n, k, precision, tol):
+    """Short-k nodes whose 128 x 128 tiles would fill at most half the SMs
+    run 128 x 64 tiles with neither side narrow (ragged rows and columns,
+    k not a multiple of the stage)."""
+    net = node_network(m, n, k, m + 2 * n + 5 * k)
+    plan = tn.Plan.from_network(net, [(0, 1)], (), precision, NT)
+    assert plan.node_class(0) == tn.TN_NODE_DENSE
+    got, _ = run_gpu(net, [(0, 1)], precision=precision, policy=NT)
+    assert_close(got, _ref(net, [(0, 1)]), tol, f"short-k {m}x{n}x{k} {precision}")
