@@ -344,7 +344,7 @@ TN_API tn_status tn_plan_set_three_products(tn_plan_t *plan, int32_t enable);
  * core's accumulation rounds toward zero, so every node's sums shrink by a
  * relative bias that grows with the chunk (measured ~1.3e-6 per node with
  * 256, ~0.33e-6 with 64), and the nodes' biases add up at the root; shorter
- * chunks cost throughput (4096^3 node: ~349 TFLOP/s with 256, ~323 with 64).
+ * chunks cost throughput (4096^3 node: ~352 TFLOP/s with 256, ~340 with 128).
  * chunk_k = 0 (the default) picks, per plan, the longest of 256, 128 and 64
  * whose bias times the number of tensor-core nodes stays within 4e-6 (2048
  * for plain bf16 operands, whose own rounding is ~1e-3); otherwise a
@@ -363,8 +363,9 @@ TN_API tn_status tn_plan_set_promotion_chunk(tn_plan_t *plan, int32_t chunk_k);
  * half of its B rows, so it reads half as much of B per MMA) and the real
  * and imaginary parts accumulated directly (negated-A MMAs for -Ai Bi) in
  * double-buffered TMEM.  Measured on a GB300 it is not faster than the
- * single-CTA kernel at equal accuracy (4096^3 node, split tf32: 272 against
- * 300 TFLOP/s), so the default is 0.  Re-plans the layout (like
+ * single-CTA kernel at equal accuracy (4096^3 node, split tf32: 318 against
+ * 349 TFLOP/s with 256-k chunks; under the power cap it draws less power but
+ * still takes longer), so the default is 0.  Re-plans the layout (like
  * tn_plan_set_policy): bind the workspace again afterwards.
  * Errors: TN_EINVAL (NULL plan).
  */
