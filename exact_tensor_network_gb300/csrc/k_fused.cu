@@ -39,9 +39,10 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
     }
     __syncthreads();
     const FuseGroup g = gs;
-    pdl_wait();
     // descriptors after the tensors: steps, level starts (steps, then warp
-    // chunks), output offsets, the step of every warp chunk
+    // chunks), output offsets, the step of every warp chunk; like the group
+    // descriptor they are written before any launch, so they are read
+    // before waiting for the previous grid
     FuseNode *nodes = reinterpret_cast<FuseNode *>(sm + g.smem);
     int32_t *levels = reinterpret_cast<int32_t *>(nodes + g.n_nodes);
     int32_t *lchunk = levels + g.n_levels + 1;
@@ -57,12 +58,20 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(const __grid_constant__
         for (int w = threadIdx.x; w < g.n_off; w += kThreads) offs[w] = a.offs[g.first_off + w];
         for (int w = threadIdx.x; w < g.n_chunks; w += kThreads) cnode[w] = a.chunks[g.first_chunk + w];
     }
-    // leaves: slot e <- the caller's leaf at its source offset (these loads
-    // overlap the descriptor copies above)
-    const float2 *const *src = a.src + a.src_first[x];
+    // leaves: slot e <- the caller's leaf at its source offset.  The (leaf,
+    // offset) pairs are static too: each thread parks its slots' pairs in the
+    // slots themselves, then, once the previous grid (which may have written
+    // the leaves) is done, replaces each by the leaf entry: one round trip
+    // after the wait instead of two
     for (int e = threadIdx.x; e < g.n_gather; e += kThreads) {
         const FuseGather ge = a.gather[g.first_gather + e];
-        sm[e] = src[ge.leaf][ge.src];
+        reinterpret_cast<int2 *>(sm)[e] = make_int2(ge.leaf, ge.src);
+    }
+    pdl_wait();
+    const float2 *const *src = a.src + a.src_first[x];
+    for (int e = threadIdx.x; e < g.n_gather; e += kThreads) {
+        const int2 ge = reinterpret_cast<const int2 *>(sm)[e];
+        sm[e] = src[ge.x][ge.y];
     }
     __syncthreads();
     void *out = g.out_off < 0 ? static_cast<void *>(a.out) : static_cast<void *>(a.arena + g.out_off);
